@@ -1,0 +1,164 @@
+"""CPU oracle for the ternary-weight linear layer -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The library's product path never
+does and has no fallback to it.
+
+The arithmetic lives in ``oracle.c`` (plain C, fp64), written from the
+pages' packing rule and the plain definition of the layer; this module only
+compiles it with gcc and marshals numpy arrays.  Its pins (the checks that
+tie it to the pages and to mathematics rather than to itself) are in
+``tests/test_oracle_pins.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``oracle.c`` into ``_build/liboracle.so`` (gcc, OpenMP)."""
+    src = os.path.join(_HERE, "oracle.c")
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(src)):
+        return _LIB_PATH
+    os.makedirs(_BUILD, exist_ok=True)
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    # -ffp-contract=off keeps x*w and the fp64 sums as separately rounded ops
+    subprocess.check_call(["gcc", "-O2", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared",
+                           "-std=c11", "-o", tmp, src, "-lm"])
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB_PATH)
+            i64, vp, dbl = ctypes.c_int64, ctypes.c_void_p, ctypes.c_double
+            lib.orc_fp16_to_double.argtypes = [ctypes.c_uint16]
+            lib.orc_fp16_to_double.restype = dbl
+            lib.orc_bf16_to_double.argtypes = [ctypes.c_uint16]
+            lib.orc_bf16_to_double.restype = dbl
+            lib.orc_code_to_ternary.argtypes = [ctypes.c_uint]
+            lib.orc_code_to_ternary.restype = ctypes.c_int
+            lib.orc_pack.argtypes = [vp, i64, i64, vp]
+            lib.orc_pack.restype = i64
+            lib.orc_unpack.argtypes = [vp, i64, i64, vp]
+            lib.orc_unpack.restype = i64
+            lib.orc_tiled_bytes.argtypes = [i64, i64]
+            lib.orc_tiled_bytes.restype = i64
+            lib.orc_repack.argtypes = [vp, vp, i64, i64, vp]
+            lib.orc_repack.restype = i64
+            lib.orc_unrepack.argtypes = [vp, i64, i64, vp, vp]
+            lib.orc_unrepack.restype = i64
+            lib.orc_linear.argtypes = [vp, i64, vp, vp, i64, i64, i64, vp, vp]
+            lib.orc_linear.restype = None
+            lib.orc_linear_cols.argtypes = [vp, i64, vp, vp, i64, i64, i64, vp, i64, vp, vp]
+            lib.orc_linear_cols.restype = None
+            lib.orc_num_threads.argtypes = []
+            lib.orc_num_threads.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _c(a: np.ndarray, dtype) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def fp16_to_double(bits: int) -> float:
+    return float(_load().orc_fp16_to_double(bits))
+
+
+def bf16_to_double(bits: int) -> float:
+    return float(_load().orc_bf16_to_double(bits))
+
+
+def code_to_ternary(code: int) -> int:
+    return int(_load().orc_code_to_ternary(code))
+
+
+def pack(t: np.ndarray):
+    """t int8 [N, K] -> (packed uint8 [N, K/4], number of invalid entries)."""
+    t = _c(t, np.int8)
+    N, K = t.shape
+    if K % 4:
+        raise ValueError("K must be a multiple of 4")
+    out = np.empty((N, K // 4), dtype=np.uint8)
+    bad = _load().orc_pack(t.ctypes.data, N, K, out.ctypes.data)
+    return out, int(bad)
+
+
+def unpack(packed: np.ndarray, K: int):
+    """packed uint8 [N, K/4] -> (t int8 [N, K], number of reserved code-11 entries)."""
+    packed = _c(packed, np.uint8)
+    N = packed.shape[0]
+    out = np.empty((N, K), dtype=np.int8)
+    bad = _load().orc_unpack(packed.ctypes.data, N, K, out.ctypes.data)
+    return out, int(bad)
+
+
+def tiled_bytes(N: int, K: int) -> int:
+    return int(_load().orc_tiled_bytes(N, K))
+
+
+def repack(packed: np.ndarray, scales: np.ndarray, K: int):
+    """(packed [N,K/4], fp16 bits [N,K/128]) -> (tiled uint8 bytes, reserved count)."""
+    packed = _c(packed, np.uint8)
+    scales = _c(scales, np.uint16)
+    N = packed.shape[0]
+    out = np.empty(tiled_bytes(N, K), dtype=np.uint8)
+    bad = _load().orc_repack(packed.ctypes.data, scales.ctypes.data, N, K, out.ctypes.data)
+    return out, int(bad)
+
+
+def unrepack(tiled: np.ndarray, N: int, K: int):
+    """tiled bytes -> (packed [N,K/4], fp16 bits [N,K/128], invalid count)."""
+    tiled = _c(tiled, np.uint8)
+    packed = np.empty((N, K // 4), dtype=np.uint8)
+    scales = np.empty((N, K // 128), dtype=np.uint16)
+    bad = _load().orc_unrepack(tiled.ctypes.data, N, K, packed.ctypes.data, scales.ctypes.data)
+    return packed, scales, int(bad)
+
+
+def linear(x_bf16: np.ndarray, packed: np.ndarray, scales: np.ndarray, K: int):
+    """Y[M, N] = X . (s (.) T)^T in fp64, and the per-output bound sum_k |x w|."""
+    x = _c(x_bf16, np.uint16)
+    packed = _c(packed, np.uint8)
+    scales = _c(scales, np.uint16)
+    M, N = x.shape[0], packed.shape[0]
+    y = np.empty((M, N), dtype=np.float64)
+    b = np.empty((M, N), dtype=np.float64)
+    _load().orc_linear(x.ctypes.data, K, packed.ctypes.data, scales.ctypes.data,
+                       M, N, K, y.ctypes.data, b.ctypes.data)
+    return y, b
+
+
+def linear_cols(x_bf16: np.ndarray, packed: np.ndarray, scales: np.ndarray, K: int, cols):
+    """Like ``linear`` for the output columns ``cols`` only: returns [M, len(cols)]."""
+    x = _c(x_bf16, np.uint16)
+    packed = _c(packed, np.uint8)
+    scales = _c(scales, np.uint16)
+    cols = _c(np.asarray(cols), np.int64)
+    M, N = x.shape[0], packed.shape[0]
+    y = np.empty((M, cols.size), dtype=np.float64)
+    b = np.empty((M, cols.size), dtype=np.float64)
+    _load().orc_linear_cols(x.ctypes.data, K, packed.ctypes.data, scales.ctypes.data,
+                            M, N, K, cols.ctypes.data, cols.size, y.ctypes.data, b.ctypes.data)
+    return y, b
+
+
+def num_threads() -> int:
+    return int(_load().orc_num_threads())
