@@ -1,0 +1,186 @@
+/*
+ * tern.h -- C ABI of libtern, the ternary-weight linear layer for one
+ * NVIDIA GB300 GPU (sm_103a).
+ *
+ * The layer computes Y[M,N] = X[M,K] . W^T with W[n,k] = t[n,k] * s[n, k/128]:
+ * ternary weights t in {-1,0,+1}, one FP16 scale per 128 consecutive weights
+ * along K, BF16 activations X, fp32 accumulation and fp32 output Y.
+ *
+ * Sources (web pages, cited by a short name, address and section):
+ *   [EMB] "Ternary embedding model in vLLM", 2kiu.com/news/5082861
+ *         §1.1 ternary weights with a shared FP16 scale per 128 weights;
+ *         §2.2 the packed weight tensor is [out_features, in_features/4]
+ *              uint8; fused QKV tensors are cut by offsets, and the scales
+ *              must be cut the same way;
+ *         §3.1 the packing rule (2-bit codes 00->0, 01->+1, 10->-1,
+ *              11->reserved read as 0; four codes per byte, little-endian,
+ *              first weight in the lowest bits; scale blocks cut
+ *              contiguously along K);
+ *         §3   disk layout and GPU layout must be reconciled;
+ *         §4.2 the op: x [M,K], packed w [N,K/4], scale [N,K/128] -> y [M,N];
+ *              signs accumulated inside a 128-block, scale applied once at
+ *              the block boundary;
+ *         §4.4 inputs are reshaped to a 2-D contiguous [tokens, hidden].
+ *   [B27] "Porting ternary Bonsai 2 27B to vLLM", m.xxqk.cn/news/594847
+ *         §5.2 FP16 scales are stored little-endian.
+ *
+ * Conventions for every call
+ *   - Pointers named d_* or documented as "device" are device pointers on
+ *     the current CUDA device; arrays documented as "host" live in host
+ *     memory.  The caller owns and allocates every buffer, including the
+ *     workspace; the library allocates no memory and keeps no state.
+ *   - `stream` is a cudaStream_t passed as void* (NULL: the legacy default
+ *     stream).  Calls only enqueue work and return; results are ready when
+ *     the stream reaches them.
+ *   - Argument problems (null pointers, bad shapes, misalignment, small
+ *     buffers) return an error code before anything is enqueued.  Launch
+ *     failures return TERN_ERR_CUDA.  Data problems (values outside the
+ *     format) never stop a call; where a `d_err` counter is given, the
+ *     kernel adds their count to it with an atomic add.
+ *   - No call throws; no call synchronises the device.
+ *   - Sizes are int64_t elements unless named *_bytes.
+ */
+#ifndef TERN_H
+#define TERN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TERN_OK = 0,
+    TERN_ERR_NULL = 1,        /* a required pointer is NULL */
+    TERN_ERR_SHAPE = 2,       /* bad dimension: negative, K not a multiple of 128, ... */
+    TERN_ERR_ALIGN = 3,       /* a pointer or leading dimension breaks an alignment rule */
+    TERN_ERR_SIZE = 4,        /* a buffer given with its size is too small */
+    TERN_ERR_UNSUPPORTED = 5, /* valid request this build cannot serve (e.g. no GPU) */
+    TERN_ERR_CUDA = 6         /* a CUDA runtime call or kernel launch failed */
+} tern_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* tern_status_string(int status);
+
+/* Library ABI version: major*10000 + minor*100 + patch. */
+int tern_version(void);
+
+/* ------------------------------------------------------------------------
+ * On-disk format ([EMB] §2.2, §3.1)
+ *   packed : uint8 [N, K/4], row-major.  Weight (n,k) is in byte
+ *            n*(K/4) + k/4 at bits 2*(k%4)..2*(k%4)+1.  Codes: 00 -> 0,
+ *            01 -> +1, 10 -> -1, 11 -> reserved, read as 0.
+ *   scales : raw IEEE FP16 bits, uint16 [N, K/128], row-major,
+ *            little-endian ([B27] §5.2); scale (n,g) covers k in
+ *            [128g, 128g+128).
+ * ---------------------------------------------------------------------- */
+
+/* Pack ternary values into 2-bit codes ([EMB] §3.1).
+ *   d_t      device int8 [N, K] row-major, values in {-1, 0, +1}
+ *   d_packed device uint8 [N, K/4] output
+ *   d_err    optional device int32: incremented by the number of entries of
+ *            d_t outside {-1,0,+1}; those are written as code 00 (weight 0).
+ * Requires N >= 0, K >= 0, K % 4 == 0.  N*K == 0 is a no-op. */
+tern_status tern_pack(const int8_t* d_t, int64_t N, int64_t K, uint8_t* d_packed,
+                      int32_t* d_err, void* stream);
+
+/* Unpack 2-bit codes into ternary values ([EMB] §3.1, the unpack routine).
+ *   d_packed device uint8 [N, K/4];  d_t device int8 [N, K] output.
+ *   d_err    optional: incremented by the number of reserved code-11
+ *            entries, which unpack to 0.
+ * Requires N >= 0, K >= 0, K % 4 == 0. */
+tern_status tern_unpack(const uint8_t* d_packed, int64_t N, int64_t K, int8_t* d_t,
+                        int32_t* d_err, void* stream);
+
+/* ------------------------------------------------------------------------
+ * GPU tile layout ("tiled"): this library's own format, built by
+ * tern_repack from the on-disk pair.  The pages give no GPU layout; they
+ * only ask that it be reconciled with the disk layout ([EMB] §3).
+ *
+ * Rows are padded to Np = 16*ceil(N/16) with weight 0 and scale 0.  With
+ * G = K/128 scale groups and R = Np/16 row tiles:
+ *   codes : R*G blocks of 512 bytes; block (b,g) at byte (b*G + g)*512.
+ *           Lane L = 4*r8 + c (r8 in 0..7, c in 0..3) at byte 16*L holds
+ *           four little-endian uint32 words:
+ *             word 0: row 16b+r8,   k in [128g +      16c, +16)
+ *             word 1: row 16b+r8+8, k in [128g +      16c, +16)
+ *             word 2: row 16b+r8,   k in [128g + 64 + 16c, +16)
+ *             word 3: row 16b+r8+8, k in [128g + 64 + 16c, +16)
+ *           In a word covering k0..k0+15, weight k0+2i is at bits 2i..2i+1
+ *           and weight k0+2i+1 at bits 16+2i..17+2i (i = 0..7).  The value
+ *           stored is the biased code v = t + 1 in {0,1,2}.
+ *   scales: R*G blocks of 32 bytes starting at byte R*G*512; block (b,g) at
+ *           R*G*512 + (b*G + g)*32 holds eight little-endian uint32 words,
+ *           word r8 = s[16b+r8][g] | s[16b+r8+8][g] << 16 (FP16 bits).
+ * A warp streams one block per 16x128 tile: lane L's 16 bytes are exactly
+ * the four 16-weight runs that its tensor-core fragments need.
+ * ---------------------------------------------------------------------- */
+
+/* Bytes of the tiled layout for an N x K weight: 544 * ceil(N/16) * (K/128).
+ * Returns 0 for invalid shapes (N < 0, K <= 0 or K % 128 != 0). */
+size_t tern_tiled_bytes(int64_t N, int64_t K);
+
+/* On-disk (packed, scales) -> tiled.  Reserved code 11 is stored as weight
+ * 0 and counted in d_err.  Requires K > 0, K % 128 == 0, N >= 0,
+ * d_packed 4-byte aligned, d_tiled 16-byte aligned,
+ * tiled_bytes >= tern_tiled_bytes(N, K). */
+tern_status tern_repack(const uint8_t* d_packed, const uint16_t* d_scales, int64_t N, int64_t K,
+                        void* d_tiled, size_t tiled_bytes, int32_t* d_err, void* stream);
+
+/* tiled -> on-disk (packed, scales), rows < N only; the inverse of
+ * tern_repack on valid data (code 11 comes back as 00).  A stored value of
+ * 3 (never written by tern_repack) unpacks to weight 0 and is counted in
+ * d_err.  Requires the same shapes and alignments as tern_repack, and
+ * d_packed 4-byte aligned. */
+tern_status tern_unrepack(const void* d_tiled, int64_t N, int64_t K, uint8_t* d_packed,
+                          uint16_t* d_scales, int32_t* d_err, void* stream);
+
+/* ------------------------------------------------------------------------
+ * The linear layer ([EMB] §4.2).
+ *
+ *   Y[m, n] = sum_k X[m, k] * t[n, k] * s[n, k/128]
+ *
+ * computed as: per 128-wide group, an fp32 partial of exact products
+ * x * t; the FP16 scale (converted exactly to fp32) multiplies the partial
+ * once per group; the scaled partials are summed in fp32.  The result
+ * satisfies |Y - Y_exact| <= 1e-4 * sum_k |X[m,k] * W[n,k]| per output.
+ *
+ *   d_X      device bf16 bits [M, ldx] row-major; 16-byte aligned,
+ *            ldx % 8 == 0, ldx >= K
+ *   d_tiled  device tiled weights for N x K (tern_repack); 16-byte aligned
+ *   d_Y      device fp32 [M, ldy] row-major output, ldy >= N; 4-byte aligned
+ *   d_ws     device workspace of ws_bytes >= tern_workspace_bytes(M, N, K),
+ *            256-byte aligned; may be NULL when that size is 0.  It must
+ *            be zero-filled before its first use; every completed call
+ *            leaves it zero-filled again, so one workspace can serve a
+ *            sequence of calls on one stream.  Calls that may overlap in
+ *            time need separate workspaces.
+ * M == 0 or N == 0 is a no-op.  K must be a positive multiple of 128.
+ * X is read after any preceding kernel on the stream completes; kernels
+ * launched with programmatic dependent launch may begin streaming weights
+ * earlier. */
+size_t tern_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+tern_status tern_linear(const uint16_t* d_X, int64_t ldx, const void* d_tiled,
+                        int64_t M, int64_t N, int64_t K,
+                        float* d_Y, int64_t ldy, void* d_ws, size_t ws_bytes, void* stream);
+
+/* Multi-output variant for fused projections (QKV, gate+up; [EMB] §2.2):
+ * one weight stream over the concatenated rows, N = sum(n_sizes), with
+ * output rows [off_j, off_j + n_sizes[j]) written to d_Ys[j] (row stride
+ * ldys[j] >= n_sizes[j]).  Each scale travels with its own row, so the
+ * cut applies to weights and scales alike.  n_sizes, d_Ys and ldys are
+ * HOST arrays of n_out entries (1 <= n_out <= 4); d_Ys[j] are device
+ * pointers.  Other arguments as tern_linear; the workspace size is
+ * tern_workspace_bytes(M, N, K) for the total N. */
+tern_status tern_linear_multi(const uint16_t* d_X, int64_t ldx, const void* d_tiled,
+                              int64_t M, int64_t K, int n_out, const int64_t* n_sizes,
+                              float* const* d_Ys, const int64_t* ldys,
+                              void* d_ws, size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TERN_H */

@@ -93,6 +93,7 @@ static unsigned packed_code(const uint8_t* packed, int64_t K, int64_t n, int64_t
    Returns the number of entries outside {-1,0,+1} (written as code 00). */
 int64_t orc_pack(const int8_t* t, int64_t N, int64_t K, uint8_t* packed) {
     int64_t invalid = 0;
+    #pragma omp parallel for schedule(static) reduction(+:invalid)
     for (int64_t n = 0; n < N; ++n) {
         for (int64_t kb = 0; kb < K / 4; ++kb) {
             unsigned byte = 0;

@@ -1,0 +1,156 @@
+"""ctypes binding of libtern's C ABI (include/tern.h).
+
+Argument marshalling only: every step of the layer runs in libtern's CUDA
+kernels.  Functions carry the C names; tensor arguments may be torch
+tensors (their ``data_ptr()`` is passed) or raw integer addresses, and
+``stream`` may be a ``torch.cuda.Stream``, a raw ``cudaStream_t`` integer or
+None (the current torch stream).  A non-zero status raises ``TernError``.
+If the library has not been built, importing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+TERN_OK = 0
+STATUS_NAMES = {0: "TERN_OK", 1: "TERN_ERR_NULL", 2: "TERN_ERR_SHAPE", 3: "TERN_ERR_ALIGN",
+                4: "TERN_ERR_SIZE", 5: "TERN_ERR_UNSUPPORTED", 6: "TERN_ERR_CUDA"}
+
+# Every symbol include/tern.h declares.
+EXPORTED = ("tern_status_string", "tern_version", "tern_pack", "tern_unpack", "tern_tiled_bytes",
+            "tern_repack", "tern_unrepack", "tern_workspace_bytes", "tern_linear",
+            "tern_linear_multi")
+
+
+class TernError(RuntimeError):
+    def __init__(self, status: int, func: str):
+        self.status = status
+        super().__init__(f"{func}: {status_string(status)}")
+
+
+def _load():
+    if not os.path.exists(_build.LIB):
+        raise ImportError(f"libtern.so is not built ({_build.LIB}); run "
+                          "`python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(_build.LIB)
+    i64, vp, sz, i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+    lib.tern_status_string.argtypes = [i32]
+    lib.tern_status_string.restype = ctypes.c_char_p
+    lib.tern_version.argtypes = []
+    lib.tern_version.restype = i32
+    lib.tern_pack.argtypes = [vp, i64, i64, vp, vp, vp]
+    lib.tern_pack.restype = i32
+    lib.tern_unpack.argtypes = [vp, i64, i64, vp, vp, vp]
+    lib.tern_unpack.restype = i32
+    lib.tern_tiled_bytes.argtypes = [i64, i64]
+    lib.tern_tiled_bytes.restype = sz
+    lib.tern_repack.argtypes = [vp, vp, i64, i64, vp, sz, vp, vp]
+    lib.tern_repack.restype = i32
+    lib.tern_unrepack.argtypes = [vp, i64, i64, vp, vp, vp, vp]
+    lib.tern_unrepack.restype = i32
+    lib.tern_workspace_bytes.argtypes = [i64, i64, i64]
+    lib.tern_workspace_bytes.restype = sz
+    lib.tern_linear.argtypes = [vp, i64, vp, i64, i64, i64, vp, i64, vp, sz, vp]
+    lib.tern_linear.restype = i32
+    lib.tern_linear_multi.argtypes = [vp, i64, vp, i64, i64, i32, ctypes.POINTER(i64),
+                                      ctypes.POINTER(vp), ctypes.POINTER(i64), vp, sz, vp]
+    lib.tern_linear_multi.restype = i32
+    return lib
+
+
+_lib = _load()
+
+
+def library():
+    """The loaded ctypes library object."""
+    return _lib
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def _p(x):
+    """Device/host address of a tensor or an int (None -> NULL)."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _s(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, func: str):
+    if status != TERN_OK:
+        raise TernError(status, func)
+
+
+def status_string(status: int) -> str:
+    return _lib.tern_status_string(status).decode()
+
+
+def tern_status_string(status: int) -> str:
+    return status_string(status)
+
+
+def tern_version() -> int:
+    return int(_lib.tern_version())
+
+
+def tern_pack(t, N: int, K: int, packed, err=None, stream=None):
+    _check(_lib.tern_pack(_p(t), N, K, _p(packed), _p(err), _s(stream)), "tern_pack")
+
+
+def tern_unpack(packed, N: int, K: int, t, err=None, stream=None):
+    _check(_lib.tern_unpack(_p(packed), N, K, _p(t), _p(err), _s(stream)), "tern_unpack")
+
+
+def tern_tiled_bytes(N: int, K: int) -> int:
+    return int(_lib.tern_tiled_bytes(N, K))
+
+
+def tern_repack(packed, scales, N: int, K: int, tiled, tiled_bytes: int | None = None, err=None,
+                stream=None):
+    if tiled_bytes is None:
+        tiled_bytes = tiled.numel() * tiled.element_size()
+    _check(_lib.tern_repack(_p(packed), _p(scales), N, K, _p(tiled), tiled_bytes, _p(err), _s(stream)),
+           "tern_repack")
+
+
+def tern_unrepack(tiled, N: int, K: int, packed, scales, err=None, stream=None):
+    _check(_lib.tern_unrepack(_p(tiled), N, K, _p(packed), _p(scales), _p(err), _s(stream)),
+           "tern_unrepack")
+
+
+def tern_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(_lib.tern_workspace_bytes(M, N, K))
+
+
+def tern_linear(X, ldx: int, tiled, M: int, N: int, K: int, Y, ldy: int, ws=None,
+                ws_bytes: int | None = None, stream=None):
+    if ws_bytes is None:
+        ws_bytes = 0 if ws is None or isinstance(ws, int) else ws.numel() * ws.element_size()
+    _check(_lib.tern_linear(_p(X), ldx, _p(tiled), M, N, K, _p(Y), ldy, _p(ws), ws_bytes, _s(stream)),
+           "tern_linear")
+
+
+def tern_linear_multi(X, ldx: int, tiled, M: int, K: int, n_sizes, Ys, ldys, ws=None,
+                      ws_bytes: int | None = None, stream=None):
+    n_out = len(n_sizes)
+    sizes = (ctypes.c_int64 * n_out)(*[int(v) for v in n_sizes])
+    ptrs = (ctypes.c_void_p * n_out)(*[_p(y) for y in Ys])
+    lds = (ctypes.c_int64 * n_out)(*[int(v) for v in ldys])
+    if ws_bytes is None:
+        ws_bytes = 0 if ws is None or isinstance(ws, int) else ws.numel() * ws.element_size()
+    _check(_lib.tern_linear_multi(_p(X), ldx, _p(tiled), M, K, n_out, sizes, ptrs, lds, _p(ws),
+                                  ws_bytes, _s(stream)), "tern_linear_multi")

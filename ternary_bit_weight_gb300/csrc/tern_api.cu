@@ -1,0 +1,189 @@
+// Host entry points of libtern (the C ABI declared in include/tern.h):
+// argument checks, kernel selection and launches.  Nothing here allocates
+// memory or keeps state between calls.
+
+#include "tern.h"
+#include "tern_common.cuh"
+#include "tern_internal.h"
+
+namespace {
+
+using tern::ceil_div;
+
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+inline cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+inline tern_status from_cuda(cudaError_t e) { return e == cudaSuccess ? TERN_OK : TERN_ERR_CUDA; }
+
+inline bool valid_group_shape(int64_t N, int64_t K) { return N >= 0 && K > 0 && K % tern::kGroup == 0; }
+
+// Workspace of the decode path for one launch of up to 16 rows of X, and the
+// maximum over the launches a call with M rows makes.
+size_t decode_ws_bytes(int64_t M, int64_t N, int64_t K, int sms) {
+    if (M <= 0 || N <= 0) return 0;
+    size_t need = 0;
+    const int64_t full = M >= tern::kDecodeMaxM ? tern::kDecodeMaxM : M;
+    need = tern::plan_decode(full, N, K, sms).ws_bytes;
+    const int64_t rem = M % tern::kDecodeMaxM;
+    if (M > tern::kDecodeMaxM && rem != 0) {
+        const size_t r = tern::plan_decode(rem, N, K, sms).ws_bytes;
+        if (r > need) need = r;
+    }
+    return need;
+}
+
+tern_status run_linear(const uint16_t* X, int64_t ldx, const void* tiled, int64_t M, int64_t N,
+                       int64_t K, const tern::OutputSplit& out, void* ws, size_t ws_bytes,
+                       cudaStream_t stream) {
+    const int sms = tern::device_sm_count();
+    if (sms <= 0) return TERN_ERR_UNSUPPORTED;
+    const size_t need = decode_ws_bytes(M, N, K, sms);
+    if (need > 0) {
+        if (ws == nullptr) return TERN_ERR_NULL;
+        if (ws_bytes < need) return TERN_ERR_SIZE;
+        if (!aligned(ws, 256)) return TERN_ERR_ALIGN;
+    }
+    // Batches of up to 16 rows go through the decode kernel; larger M is
+    // processed 16 rows at a time.
+    for (int64_t m0 = 0; m0 < M; m0 += tern::kDecodeMaxM) {
+        const int64_t mc = (M - m0) < tern::kDecodeMaxM ? (M - m0) : tern::kDecodeMaxM;
+        tern::OutputSplit o = out;
+        for (int j = 0; j < o.n_out; ++j) o.y[j] = out.y[j] + m0 * out.ldy[j];
+        const tern::DecodePlan plan = tern::plan_decode(mc, N, K, sms);
+        const cudaError_t e = tern::launch_decode(X + m0 * ldx, ldx, static_cast<const uint8_t*>(tiled),
+                                                  mc, N, K, o, ws, plan, stream);
+        if (e != cudaSuccess) return TERN_ERR_CUDA;
+    }
+    return TERN_OK;
+}
+
+tern_status check_x_w(const uint16_t* X, int64_t ldx, const void* tiled, int64_t M, int64_t K) {
+    if (X == nullptr || tiled == nullptr) return TERN_ERR_NULL;
+    if (ldx < K) return TERN_ERR_SHAPE;
+    if (M > (int64_t(1) << 30)) return TERN_ERR_SHAPE;
+    if (!aligned(X, 16) || ldx % 8 != 0) return TERN_ERR_ALIGN;
+    if (!aligned(tiled, 16)) return TERN_ERR_ALIGN;
+    return TERN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* tern_status_string(int status) {
+    switch (status) {
+        case TERN_OK: return "TERN_OK";
+        case TERN_ERR_NULL: return "TERN_ERR_NULL: a required pointer is NULL";
+        case TERN_ERR_SHAPE: return "TERN_ERR_SHAPE: invalid dimension or leading dimension";
+        case TERN_ERR_ALIGN: return "TERN_ERR_ALIGN: pointer or leading dimension misaligned";
+        case TERN_ERR_SIZE: return "TERN_ERR_SIZE: buffer too small";
+        case TERN_ERR_UNSUPPORTED: return "TERN_ERR_UNSUPPORTED: request not supported on this device";
+        case TERN_ERR_CUDA: return "TERN_ERR_CUDA: CUDA call or kernel launch failed";
+        default: return "TERN_ERR_UNKNOWN";
+    }
+}
+
+int tern_version(void) { return 10000; }
+
+tern_status tern_pack(const int8_t* d_t, int64_t N, int64_t K, uint8_t* d_packed, int32_t* d_err,
+                      void* stream) {
+    if (N < 0 || K < 0 || K % 4 != 0) return TERN_ERR_SHAPE;
+    if (N == 0 || K == 0) return TERN_OK;
+    if (d_t == nullptr || d_packed == nullptr) return TERN_ERR_NULL;
+    if (d_err != nullptr && !aligned(d_err, 4)) return TERN_ERR_ALIGN;
+    return from_cuda(tern::launch_pack(d_t, N * K, d_packed, d_err, as_stream(stream)));
+}
+
+tern_status tern_unpack(const uint8_t* d_packed, int64_t N, int64_t K, int8_t* d_t, int32_t* d_err,
+                        void* stream) {
+    if (N < 0 || K < 0 || K % 4 != 0) return TERN_ERR_SHAPE;
+    if (N == 0 || K == 0) return TERN_OK;
+    if (d_t == nullptr || d_packed == nullptr) return TERN_ERR_NULL;
+    if (d_err != nullptr && !aligned(d_err, 4)) return TERN_ERR_ALIGN;
+    return from_cuda(tern::launch_unpack(d_packed, N * K, d_t, d_err, as_stream(stream)));
+}
+
+size_t tern_tiled_bytes(int64_t N, int64_t K) {
+    if (!valid_group_shape(N, K)) return 0;
+    return (size_t)ceil_div(N, tern::kTileRows) * (size_t)(K / tern::kGroup) *
+           (size_t)(tern::kCodeBlockBytes + tern::kScaleBlockBytes);
+}
+
+tern_status tern_repack(const uint8_t* d_packed, const uint16_t* d_scales, int64_t N, int64_t K,
+                        void* d_tiled, size_t tiled_bytes, int32_t* d_err, void* stream) {
+    if (!valid_group_shape(N, K)) return TERN_ERR_SHAPE;
+    if (N == 0) return TERN_OK;
+    if (d_packed == nullptr || d_scales == nullptr || d_tiled == nullptr) return TERN_ERR_NULL;
+    if (!aligned(d_packed, 4) || !aligned(d_scales, 2) || !aligned(d_tiled, 16)) return TERN_ERR_ALIGN;
+    if (d_err != nullptr && !aligned(d_err, 4)) return TERN_ERR_ALIGN;
+    if (tiled_bytes < tern_tiled_bytes(N, K)) return TERN_ERR_SIZE;
+    return from_cuda(tern::launch_repack(d_packed, d_scales, N, K, static_cast<uint8_t*>(d_tiled),
+                                         d_err, as_stream(stream)));
+}
+
+tern_status tern_unrepack(const void* d_tiled, int64_t N, int64_t K, uint8_t* d_packed,
+                          uint16_t* d_scales, int32_t* d_err, void* stream) {
+    if (!valid_group_shape(N, K)) return TERN_ERR_SHAPE;
+    if (N == 0) return TERN_OK;
+    if (d_packed == nullptr || d_scales == nullptr || d_tiled == nullptr) return TERN_ERR_NULL;
+    if (!aligned(d_packed, 4) || !aligned(d_scales, 2) || !aligned(d_tiled, 16)) return TERN_ERR_ALIGN;
+    if (d_err != nullptr && !aligned(d_err, 4)) return TERN_ERR_ALIGN;
+    return from_cuda(tern::launch_unrepack(static_cast<const uint8_t*>(d_tiled), N, K, d_packed,
+                                           d_scales, d_err, as_stream(stream)));
+}
+
+size_t tern_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+    if (M <= 0 || !valid_group_shape(N, K) || N == 0) return 0;
+    return decode_ws_bytes(M, N, K, tern::device_sm_count());
+}
+
+tern_status tern_linear(const uint16_t* d_X, int64_t ldx, const void* d_tiled, int64_t M, int64_t N,
+                        int64_t K, float* d_Y, int64_t ldy, void* d_ws, size_t ws_bytes,
+                        void* stream) {
+    if (M < 0 || !valid_group_shape(N, K)) return TERN_ERR_SHAPE;
+    if (M == 0 || N == 0) return TERN_OK;
+    tern_status st = check_x_w(d_X, ldx, d_tiled, M, K);
+    if (st != TERN_OK) return st;
+    if (d_Y == nullptr) return TERN_ERR_NULL;
+    if (ldy < N) return TERN_ERR_SHAPE;
+    if (!aligned(d_Y, 4)) return TERN_ERR_ALIGN;
+    tern::OutputSplit out = {};
+    out.n_out = 1;
+    out.offset[0] = 0;
+    out.offset[1] = N;
+    out.y[0] = d_Y;
+    out.ldy[0] = ldy;
+    return run_linear(d_X, ldx, d_tiled, M, N, K, out, d_ws, ws_bytes, as_stream(stream));
+}
+
+tern_status tern_linear_multi(const uint16_t* d_X, int64_t ldx, const void* d_tiled, int64_t M,
+                              int64_t K, int n_out, const int64_t* n_sizes, float* const* d_Ys,
+                              const int64_t* ldys, void* d_ws, size_t ws_bytes, void* stream) {
+    if (n_out < 1 || n_out > tern::kMaxOutputs) return TERN_ERR_SHAPE;
+    if (n_sizes == nullptr || d_Ys == nullptr || ldys == nullptr) return TERN_ERR_NULL;
+    tern::OutputSplit out = {};
+    out.n_out = n_out;
+    int64_t N = 0;
+    for (int j = 0; j < n_out; ++j) {
+        if (n_sizes[j] < 0) return TERN_ERR_SHAPE;
+        out.offset[j] = N;
+        N += n_sizes[j];
+    }
+    for (int j = n_out; j <= tern::kMaxOutputs; ++j) out.offset[j] = N;
+    if (M < 0 || !valid_group_shape(N, K)) return TERN_ERR_SHAPE;
+    if (M == 0 || N == 0) return TERN_OK;
+    tern_status st = check_x_w(d_X, ldx, d_tiled, M, K);
+    if (st != TERN_OK) return st;
+    for (int j = 0; j < n_out; ++j) {
+        if (n_sizes[j] == 0) { out.y[j] = nullptr; out.ldy[j] = 0; continue; }
+        if (d_Ys[j] == nullptr) return TERN_ERR_NULL;
+        if (ldys[j] < n_sizes[j]) return TERN_ERR_SHAPE;
+        if (!aligned(d_Ys[j], 4)) return TERN_ERR_ALIGN;
+        out.y[j] = d_Ys[j];
+        out.ldy[j] = ldys[j];
+    }
+    return run_linear(d_X, ldx, d_tiled, M, N, K, out, d_ws, ws_bytes, as_stream(stream));
+}
+
+}  // extern "C"

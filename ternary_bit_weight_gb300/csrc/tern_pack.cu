@@ -1,0 +1,271 @@
+// Byte-format kernels of libtern: pack, unpack, repack (disk -> tiled) and
+// unrepack (tiled -> disk).  All are memory-bound single passes, one thread
+// per 32-bit output word, and bit-exact by construction.
+//
+// Packing rule ("Ternary embedding model in vLLM", 2kiu.com/news/5082861,
+// §3.1): 2-bit codes 00 -> 0, 01 -> +1, 10 -> -1, 11 -> reserved read as 0;
+// four codes per byte, first weight in the lowest two bits.  The tiled
+// layout is the library's own (documented in include/tern.h).
+
+#include "tern_common.cuh"
+#include "tern_internal.h"
+
+namespace tern {
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ void count_errors(int32_t* err, int bad) {
+    if (err == nullptr) return;
+    const unsigned active = __activemask();
+    const int total = __reduce_add_sync(active, bad);
+    if (total != 0 && (threadIdx.x & 31) == (__ffs(active) - 1)) atomicAdd(err, total);
+}
+
+// Code of one int8 ternary value; values outside {-1,0,+1} give 00 and count.
+__device__ __forceinline__ uint32_t code_of(int8_t v, int& bad) {
+    bad += (v < -1 || v > 1);
+    return v == 1 ? 1u : (v == -1 ? 2u : 0u);
+}
+
+// One output word = 16 ternary values (one uint4 of int8) -> 4 packed bytes.
+__global__ void __launch_bounds__(kThreads)
+pack_words_kernel(const uint4* __restrict__ t, int64_t words, uint32_t* __restrict__ packed,
+                  int32_t* err) {
+    int bad = 0;
+    for (int64_t i = blockIdx.x * (int64_t)kThreads + threadIdx.x; i < words;
+         i += (int64_t)gridDim.x * kThreads) {
+        const uint4 v = t[i];
+        const uint32_t part[4] = {v.x, v.y, v.z, v.w};
+        uint32_t out = 0;
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            out |= code_of(static_cast<int8_t>(part[j >> 2] >> (8 * (j & 3))), bad) << (2 * j);
+        packed[i] = out;
+    }
+    count_errors(err, bad);
+}
+
+// Fallback for unaligned or ragged data: one packed byte per iteration.
+__global__ void __launch_bounds__(kThreads)
+pack_bytes_kernel(const int8_t* __restrict__ t, int64_t first_byte, int64_t bytes,
+                  uint8_t* __restrict__ packed, int32_t* err) {
+    int bad = 0;
+    for (int64_t i = first_byte + blockIdx.x * (int64_t)kThreads + threadIdx.x; i < bytes;
+         i += (int64_t)gridDim.x * kThreads) {
+        uint32_t out = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) out |= code_of(t[4 * i + j], bad) << (2 * j);
+        packed[i] = static_cast<uint8_t>(out);
+    }
+    count_errors(err, bad);
+}
+
+__device__ __forceinline__ int8_t value_of(uint32_t code) {
+    return code == 1u ? int8_t(1) : (code == 2u ? int8_t(-1) : int8_t(0));
+}
+
+// One packed word (16 codes) -> 16 int8 values.
+__global__ void __launch_bounds__(kThreads)
+unpack_words_kernel(const uint32_t* __restrict__ packed, int64_t words, uint4* __restrict__ t,
+                    int32_t* err) {
+    int bad = 0;
+    for (int64_t i = blockIdx.x * (int64_t)kThreads + threadIdx.x; i < words;
+         i += (int64_t)gridDim.x * kThreads) {
+        const uint32_t w = packed[i];
+        bad += __popc(w & (w >> 1) & 0x55555555u);   // code 11
+        uint32_t part[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            part[j >> 2] |= (uint32_t)(uint8_t)value_of((w >> (2 * j)) & 3u) << (8 * (j & 3));
+        t[i] = make_uint4(part[0], part[1], part[2], part[3]);
+    }
+    count_errors(err, bad);
+}
+
+__global__ void __launch_bounds__(kThreads)
+unpack_bytes_kernel(const uint8_t* __restrict__ packed, int64_t first_byte, int64_t bytes,
+                    int8_t* __restrict__ t, int32_t* err) {
+    int bad = 0;
+    for (int64_t i = first_byte + blockIdx.x * (int64_t)kThreads + threadIdx.x; i < bytes;
+         i += (int64_t)gridDim.x * kThreads) {
+        const uint32_t b = packed[i];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t c = (b >> (2 * j)) & 3u;
+            bad += (c == 3u);
+            t[4 * i + j] = value_of(c);
+        }
+    }
+    count_errors(err, bad);
+}
+
+// Disk word (16 codes of weights k0..k0+15, code j at bits 2j) -> tiled word
+// (biased v = t + 1, weight k0+2i at bits 2i, k0+2i+1 at bits 16+2i).
+__device__ __forceinline__ uint32_t disk_to_tiled_word(uint32_t src, int& bad) {
+    const uint32_t lo = src & 0x55555555u;          // code bit 0 of each field
+    const uint32_t hi = (src >> 1) & 0x55555555u;   // code bit 1
+    bad += __popc(lo & hi);
+    // v = t + 1: code 01 (+1) -> 10, code 10 (-1) -> 00, codes 00/11 -> 01
+    const uint32_t v_bit1 = lo & ~hi;
+    const uint32_t v_bit0 = ~(lo ^ hi) & 0x55555555u;
+    const uint32_t v = v_bit0 | (v_bit1 << 1);
+    uint32_t out = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        out |= ((v >> (4 * i)) & 3u) << (2 * i);            // weight 2i
+        out |= ((v >> (4 * i + 2)) & 3u) << (16 + 2 * i);   // weight 2i+1
+    }
+    return out;
+}
+
+// Tiled word -> disk word (inverse of the above; v = 3 gives code 00 and counts).
+__device__ __forceinline__ uint32_t tiled_to_disk_word(uint32_t w, int& bad) {
+    uint32_t out = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const uint32_t v = (w >> (16 * e + 2 * i)) & 3u;
+            bad += (v == 3u);
+            const uint32_t code = v == 0u ? 2u : (v == 2u ? 1u : 0u);
+            out |= code << (2 * (2 * i + e));
+        }
+    }
+    return out;
+}
+
+// Position of tiled code word `idx`: row n and first weight k0.
+__device__ __forceinline__ void tiled_word_coords(int64_t idx, int64_t G, int64_t& n, int64_t& k0) {
+    const int64_t blk = idx >> 7;              // 128 words per (b, g) block
+    const int within = static_cast<int>(idx & 127);
+    const int lane = within >> 2, q = within & 3;
+    const int r8 = lane >> 2, c = lane & 3;
+    const int64_t b = blk / G, g = blk - b * G;
+    n = 16 * b + r8 + 8 * (q & 1);
+    k0 = 128 * g + 64 * (q >> 1) + 16 * c;
+}
+
+__global__ void __launch_bounds__(kThreads)
+repack_kernel(const uint8_t* __restrict__ packed, const uint16_t* __restrict__ scales, int64_t N,
+              int64_t K, int64_t code_words, int64_t scale_words, uint32_t* __restrict__ tiled,
+              int32_t* err) {
+    const int64_t G = K / kGroup;
+    int bad = 0;
+    for (int64_t i = blockIdx.x * (int64_t)kThreads + threadIdx.x; i < code_words + scale_words;
+         i += (int64_t)gridDim.x * kThreads) {
+        if (i < code_words) {
+            int64_t n, k0;
+            tiled_word_coords(i, G, n, k0);
+            uint32_t src = 0;   // padding rows: code 00 (weight 0)
+            if (n < N) src = *reinterpret_cast<const uint32_t*>(packed + n * (K / 4) + k0 / 4);
+            tiled[i] = disk_to_tiled_word(src, bad);
+        } else {
+            const int64_t j = i - code_words;
+            const int64_t blk = j >> 3;
+            const int r8 = static_cast<int>(j & 7);
+            const int64_t b = blk / G, g = blk - b * G;
+            const int64_t n_lo = 16 * b + r8, n_hi = n_lo + 8;
+            const uint32_t s_lo = n_lo < N ? scales[n_lo * G + g] : 0u;
+            const uint32_t s_hi = n_hi < N ? scales[n_hi * G + g] : 0u;
+            tiled[i] = s_lo | (s_hi << 16);
+        }
+    }
+    count_errors(err, bad);
+}
+
+__global__ void __launch_bounds__(kThreads)
+unrepack_kernel(const uint32_t* __restrict__ tiled, int64_t N, int64_t K, int64_t code_words,
+                int64_t scale_words, uint8_t* __restrict__ packed, uint16_t* __restrict__ scales,
+                int32_t* err) {
+    const int64_t G = K / kGroup;
+    int bad = 0;
+    for (int64_t i = blockIdx.x * (int64_t)kThreads + threadIdx.x; i < code_words + scale_words;
+         i += (int64_t)gridDim.x * kThreads) {
+        if (i < code_words) {
+            int64_t n, k0;
+            tiled_word_coords(i, G, n, k0);
+            if (n < N) {
+                const uint32_t w = tiled[i];
+                *reinterpret_cast<uint32_t*>(packed + n * (K / 4) + k0 / 4) = tiled_to_disk_word(w, bad);
+            }
+        } else {
+            const int64_t j = i - code_words;
+            const int64_t blk = j >> 3;
+            const int r8 = static_cast<int>(j & 7);
+            const int64_t b = blk / G, g = blk - b * G;
+            const int64_t n_lo = 16 * b + r8, n_hi = n_lo + 8;
+            const uint32_t w = tiled[i];
+            if (n_lo < N) scales[n_lo * G + g] = static_cast<uint16_t>(w & 0xFFFFu);
+            if (n_hi < N) scales[n_hi * G + g] = static_cast<uint16_t>(w >> 16);
+        }
+    }
+    count_errors(err, bad);
+}
+
+template <typename Kernel, typename... Args>
+cudaError_t launch_flat(Kernel kernel, int64_t items, cudaStream_t stream, Args... args) {
+    if (items <= 0) return cudaSuccess;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    // grid-stride loops: enough blocks to fill every SM several times over
+    const int64_t want = ceil_div(items, kThreads);
+    const int64_t cap = (int64_t)sms * 16;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(want < cap ? want : cap));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+}  // namespace
+
+cudaError_t launch_pack(const int8_t* t, int64_t count, uint8_t* packed, int32_t* err,
+                        cudaStream_t stream) {
+    const int64_t bytes = count / 4;
+    int64_t words = 0;
+    if ((reinterpret_cast<uintptr_t>(t) & 15) == 0 && (reinterpret_cast<uintptr_t>(packed) & 3) == 0)
+        words = count / 16;
+    cudaError_t e = launch_flat(pack_words_kernel, words, stream, reinterpret_cast<const uint4*>(t),
+                                words, reinterpret_cast<uint32_t*>(packed), err);
+    if (e != cudaSuccess) return e;
+    return launch_flat(pack_bytes_kernel, bytes - 4 * words, stream, t, 4 * words, bytes, packed, err);
+}
+
+cudaError_t launch_unpack(const uint8_t* packed, int64_t count, int8_t* t, int32_t* err,
+                          cudaStream_t stream) {
+    const int64_t bytes = count / 4;
+    int64_t words = 0;
+    if ((reinterpret_cast<uintptr_t>(t) & 15) == 0 && (reinterpret_cast<uintptr_t>(packed) & 3) == 0)
+        words = count / 16;
+    cudaError_t e = launch_flat(unpack_words_kernel, words, stream,
+                                reinterpret_cast<const uint32_t*>(packed), words,
+                                reinterpret_cast<uint4*>(t), err);
+    if (e != cudaSuccess) return e;
+    return launch_flat(unpack_bytes_kernel, bytes - 4 * words, stream, packed, 4 * words, bytes, t, err);
+}
+
+cudaError_t launch_repack(const uint8_t* packed, const uint16_t* scales, int64_t N, int64_t K,
+                          uint8_t* tiled, int32_t* err, cudaStream_t stream) {
+    const int64_t R = ceil_div(N, kTileRows), G = K / kGroup;
+    const int64_t code_words = R * G * (kCodeBlockBytes / 4);
+    const int64_t scale_words = R * G * (kScaleBlockBytes / 4);
+    return launch_flat(repack_kernel, code_words + scale_words, stream, packed, scales, N, K,
+                       code_words, scale_words, reinterpret_cast<uint32_t*>(tiled), err);
+}
+
+cudaError_t launch_unrepack(const uint8_t* tiled, int64_t N, int64_t K, uint8_t* packed,
+                            uint16_t* scales, int32_t* err, cudaStream_t stream) {
+    const int64_t R = ceil_div(N, kTileRows), G = K / kGroup;
+    const int64_t code_words = R * G * (kCodeBlockBytes / 4);
+    const int64_t scale_words = R * G * (kScaleBlockBytes / 4);
+    return launch_flat(unrepack_kernel, code_words + scale_words, stream,
+                       reinterpret_cast<const uint32_t*>(tiled), N, K, code_words, scale_words,
+                       packed, scales, err);
+}
+
+}  // namespace tern

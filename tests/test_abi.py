@@ -1,0 +1,142 @@
+"""Host-side checks of libtern's C ABI (no GPU needed).
+
+The library must load, export every function include/tern.h declares, and
+reject bad arguments with the documented status before touching the GPU.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import oracle
+from conftest import ROOT
+
+tbw = pytest.importorskip("ternary_bit_weight_gb300")
+from ternary_bit_weight_gb300 import binding  # noqa: E402
+
+HEADER = os.path.join(ROOT, "include", "tern.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tern_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declarations_match_binding():
+    assert declared_functions() == sorted(binding.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(binding.library_path())
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", binding.library_path()],
+                         capture_output=True, text=True, check=True).stdout
+    exported = set(line.split()[-1] for line in out.splitlines() if line.strip())
+    for name in declared_functions():
+        assert name in exported, name
+
+
+def test_status_strings_and_version():
+    for code, name in binding.STATUS_NAMES.items():
+        assert binding.status_string(code).startswith(name)
+    assert binding.status_string(99) == "TERN_ERR_UNKNOWN"
+    assert binding.tern_version() == 10000
+
+
+@pytest.mark.parametrize("N,K", [(1, 128), (16, 128), (17, 256), (5120, 5120), (55296, 5120),
+                                 (5120, 27648)])
+def test_tiled_bytes_matches_layout(N, K):
+    assert binding.tern_tiled_bytes(N, K) == oracle.tiled_bytes(N, K)
+
+
+def test_tiled_bytes_rejects_bad_shapes():
+    for N, K in [(-1, 128), (16, 0), (16, 100), (16, -128)]:
+        assert binding.tern_tiled_bytes(N, K) == 0
+
+
+def _raw(func, *args):
+    return getattr(binding.library(), func)(*args)
+
+
+FAKE = 1 << 40       # a 256-byte-aligned address that is never dereferenced
+
+
+def test_pack_unpack_argument_errors():
+    assert _raw("tern_pack", FAKE, 4, 6, FAKE, None, None) == 2      # K % 4
+    assert _raw("tern_pack", FAKE, -1, 8, FAKE, None, None) == 2
+    assert _raw("tern_pack", None, 4, 8, FAKE, None, None) == 1
+    assert _raw("tern_pack", FAKE, 0, 8, None, None, None) == 0       # empty: no-op
+    assert _raw("tern_pack", FAKE, 4, 8, FAKE, FAKE + 1, None) == 3   # misaligned counter
+    assert _raw("tern_unpack", FAKE, 4, 6, FAKE, None, None) == 2
+    assert _raw("tern_unpack", FAKE, 4, 8, None, None, None) == 1
+
+
+def test_repack_argument_errors():
+    need = binding.tern_tiled_bytes(32, 256)
+    assert _raw("tern_repack", FAKE, FAKE, 32, 200, FAKE, need, None, None) == 2
+    assert _raw("tern_repack", None, FAKE, 32, 256, FAKE, need, None, None) == 1
+    assert _raw("tern_repack", FAKE, FAKE, 32, 256, FAKE + 8, need, None, None) == 3
+    assert _raw("tern_repack", FAKE + 2, FAKE, 32, 256, FAKE, need, None, None) == 3
+    assert _raw("tern_repack", FAKE, FAKE, 32, 256, FAKE, need - 1, None, None) == 4
+    assert _raw("tern_repack", FAKE, FAKE, 0, 256, FAKE, 0, None, None) == 0
+    assert _raw("tern_unrepack", FAKE, 32, 100, FAKE, FAKE, None, None) == 2
+    assert _raw("tern_unrepack", FAKE, 32, 256, None, FAKE, None, None) == 1
+
+
+def test_linear_argument_errors():
+    f = "tern_linear"
+    # shape: K not a multiple of 128, negative M, ldx < K, ldy < N
+    assert _raw(f, FAKE, 256, FAKE, 1, 64, 200, FAKE, 64, None, 0, None) == 2
+    assert _raw(f, FAKE, 256, FAKE, -1, 64, 256, FAKE, 64, None, 0, None) == 2
+    assert _raw(f, FAKE, 128, FAKE, 1, 64, 256, FAKE, 64, None, 0, None) == 2
+    assert _raw(f, FAKE, 256, FAKE, 1, 64, 256, FAKE, 63, None, 0, None) == 2
+    # empty problems are no-ops
+    assert _raw(f, None, 256, None, 0, 64, 256, None, 64, None, 0, None) == 0
+    assert _raw(f, None, 256, None, 4, 0, 256, None, 0, None, 0, None) == 0
+    # null pointers
+    assert _raw(f, None, 256, FAKE, 1, 64, 256, FAKE, 64, None, 0, None) == 1
+    assert _raw(f, FAKE, 256, None, 1, 64, 256, FAKE, 64, None, 0, None) == 1
+    assert _raw(f, FAKE, 256, FAKE, 1, 64, 256, None, 64, None, 0, None) == 1
+    # alignment: X 16 B, ldx % 8, tiled 16 B, Y 4 B
+    assert _raw(f, FAKE + 2, 256, FAKE, 1, 64, 256, FAKE, 64, None, 0, None) == 3
+    assert _raw(f, FAKE, 260, FAKE, 1, 64, 256, FAKE, 64, None, 0, None) == 3
+    assert _raw(f, FAKE, 256, FAKE + 4, 1, 64, 256, FAKE, 64, None, 0, None) == 3
+    assert _raw(f, FAKE, 256, FAKE, 1, 64, 256, FAKE + 2, 64, None, 0, None) == 3
+
+
+def test_linear_multi_argument_errors():
+    lib = binding.library()
+    i64 = ctypes.c_int64
+    sizes = (i64 * 2)(64, 64)
+    ptrs = (ctypes.c_void_p * 2)(FAKE, FAKE)
+    lds = (i64 * 2)(64, 64)
+    f = lib.tern_linear_multi
+    assert f(FAKE, 256, FAKE, 1, 256, 0, sizes, ptrs, lds, None, 0, None) == 2   # n_out
+    assert f(FAKE, 256, FAKE, 1, 256, 5, sizes, ptrs, lds, None, 0, None) == 2
+    assert f(FAKE, 256, FAKE, 1, 256, 2, None, ptrs, lds, None, 0, None) == 1
+    bad = (i64 * 2)(64, -1)
+    assert f(FAKE, 256, FAKE, 1, 256, 2, bad, ptrs, lds, None, 0, None) == 2
+    small_ld = (i64 * 2)(64, 32)
+    assert f(FAKE, 256, FAKE, 1, 256, 2, sizes, ptrs, small_ld, None, 0, None) == 2
+    nullp = (ctypes.c_void_p * 2)(FAKE, None)
+    assert f(FAKE, 256, FAKE, 1, 256, 2, sizes, nullp, lds, None, 0, None) == 1
+    assert f(FAKE, 256, FAKE, 1, 200, 2, sizes, ptrs, lds, None, 0, None) == 2   # K % 128
+
+
+def test_workspace_bytes_is_zero_for_empty_or_invalid():
+    assert binding.tern_workspace_bytes(0, 64, 256) == 0
+    assert binding.tern_workspace_bytes(4, 0, 256) == 0
+    assert binding.tern_workspace_bytes(4, 64, 100) == 0
+
+
+def test_product_package_never_imports_the_oracle():
+    pkg = os.path.join(ROOT, "ternary_bit_weight_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h", ".c", ".cpp")):
+                text = open(os.path.join(dirpath, fn)).read()
+                assert "oracle" not in text.replace("oracle_", ""), fn
