@@ -103,7 +103,7 @@ def test_unrepack_bit_exact(N, K):
     raw = rng.integers(0, 256, size=(N, K // 4), dtype=np.uint8)
     scales = rng.integers(0, 1 << 16, size=(N, K // 128), dtype=np.uint16)
     tiled_ref, _ = oracle.repack(raw, scales, K)
-    tiled_ref[5] |= 0x03      # plant one stored value 3 (invalid) in row 0
+    tiled_ref[0] |= 0x03      # plant one stored value 3 (invalid) at weight (0, 0)
     p_ref, s_ref, invalid = oracle.unrepack(tiled_ref, N, K)
     packed = torch.empty((N, K // 4), dtype=torch.uint8, device=DEV)
     sc = torch.empty((N, K // 128), dtype=torch.int16, device=DEV)
