@@ -17,19 +17,15 @@ __host__ __device__ constexpr int64_t ceil_div(int64_t a, int64_t b) { return (a
 
 // ---------------------------------------------------------------- loads
 
-// 16-byte streaming load of data read exactly once (weights): bypasses L1.
+// Loads of data read exactly once (weights): cache-streaming (evict-first).
+// Plain load intrinsics let the compiler schedule them as loads (issued as
+// early as the prefetch ring allows), which opaque asm would not.
 __device__ __forceinline__ uint4 ldg_stream_v4(const void* p) {
-    uint4 r;
-    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-        : "l"(p));
-    return r;
+    return __ldcs(reinterpret_cast<const uint4*>(p));
 }
 
 __device__ __forceinline__ uint32_t ldg_stream_u32(const void* p) {
-    uint32_t r;
-    asm("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(r) : "l"(p));
-    return r;
+    return __ldcs(reinterpret_cast<const unsigned int*>(p));
 }
 
 __device__ __forceinline__ uint4 lds_v4(const void* smem_ptr) {

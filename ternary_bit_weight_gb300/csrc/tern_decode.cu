@@ -36,7 +36,7 @@ namespace {
 
 constexpr int kWarps = 8;                 // row tiles per CTA (128 rows)
 constexpr int kThreads = kWarps * 32;
-constexpr int kPrefetch = 4;              // groups in flight per warp
+constexpr int kPrefetch = 8;              // groups in flight per warp
 constexpr int kRowsPerBlock = kWarps * kTileRows;
 constexpr size_t kMaxSmem = 200 * 1024;
 
@@ -132,11 +132,14 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
                         cbuf[d] = ldg_stream_v4(cptr + (int64_t)(gi + kPrefetch) * kCodeBlockBytes);
                         sbuf[d] = ldg_stream_u32(sptr + (int64_t)(gi + kPrefetch) * kScaleBlockBytes);
                     }
-                    float cg[MT][4];
+                    // two independent MMA chains (one per 64-wide half)
+                    float cg[2][MT][4];
 #pragma unroll
-                    for (int mt = 0; mt < MT; ++mt)
+                    for (int h = 0; h < 2; ++h)
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) cg[mt][e] = 0.f;
+                        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) cg[h][mt][e] = 0.f;
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         uint32_t lo[8], hi[8];
@@ -160,16 +163,16 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
                         for (int j = 0; j < 4; ++j)
 #pragma unroll
                             for (int mt = 0; mt < MT; ++mt)
-                                mma_bf16_m16n8k16(cg[mt], lo[2 * j], hi[2 * j], lo[2 * j + 1],
+                                mma_bf16_m16n8k16(cg[h][mt], lo[2 * j], hi[2 * j], lo[2 * j + 1],
                                                   hi[2 * j + 1], xb[mt][2 * j], xb[mt][2 * j + 1]);
                     }
                     const float s_lo = fp16_bits_to_float(sw), s_hi = fp16_bits_to_float(sw >> 16);
 #pragma unroll
                     for (int mt = 0; mt < MT; ++mt) {
-                        acc[mt][0] = fmaf(s_lo, cg[mt][0], acc[mt][0]);
-                        acc[mt][1] = fmaf(s_lo, cg[mt][1], acc[mt][1]);
-                        acc[mt][2] = fmaf(s_hi, cg[mt][2], acc[mt][2]);
-                        acc[mt][3] = fmaf(s_hi, cg[mt][3], acc[mt][3]);
+                        acc[mt][0] = fmaf(s_lo, cg[0][mt][0] + cg[1][mt][0], acc[mt][0]);
+                        acc[mt][1] = fmaf(s_lo, cg[0][mt][1] + cg[1][mt][1], acc[mt][1]);
+                        acc[mt][2] = fmaf(s_hi, cg[0][mt][2] + cg[1][mt][2], acc[mt][2]);
+                        acc[mt][3] = fmaf(s_hi, cg[0][mt][3] + cg[1][mt][3], acc[mt][3]);
                     }
                 }
             }

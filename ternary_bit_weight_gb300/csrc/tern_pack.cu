@@ -213,7 +213,7 @@ cudaError_t launch_flat(Kernel kernel, int64_t items, cudaStream_t stream, Args.
     if (e != cudaSuccess) return e;
     // grid-stride loops: enough blocks to fill every SM several times over
     const int64_t want = ceil_div(items, kThreads);
-    const int64_t cap = (int64_t)sms * 16;
+    const int64_t cap = (int64_t)sms * 32;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(want < cap ? want : cap));
     cfg.blockDim = dim3(kThreads);
