@@ -58,6 +58,16 @@ __device__ __forceinline__ void mma_bf16_m16n8k16(float (&d)[4], uint32_t a0, ui
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Same with C = 0 (the first MMA of a chain): no register zeroing needed.
+__device__ __forceinline__ void mma_bf16_m16n8k16_zc(float (&d)[4], uint32_t a0, uint32_t a1,
+                                                     uint32_t a2, uint32_t a3, uint32_t b0,
+                                                     uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%10, %10, %10, %10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+}
+
 // ------------------------------------------------------ code decoding
 //
 // A tiled code word covers 16 consecutive weights of one row: weight k0+2i

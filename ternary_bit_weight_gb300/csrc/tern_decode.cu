@@ -1,4 +1,4 @@
-// Decode / skinny-batch kernel of libtern: Y[M,N] = X[M,K] . (s (.) T)^T for
+// Decode / skinny-batch kernels of libtern: Y[M,N] = X[M,K] . (s (.) T)^T for
 // M <= 16, streaming the tiled 2-bit weights at HBM rate.
 //
 // Method ("Ternary embedding model in vLLM", 2kiu.com/news/5082861, §4.2,
@@ -7,26 +7,33 @@
 // the FP16 scale once per group.  The page's kernels run one thread per
 // output on CUDA cores; here the per-group sum is done by the tensor cores:
 //
-//   * a warp owns a 16-row tile; each group of 128 weights arrives as one
-//     coalesced 512-byte block (one 16-byte load per lane, prefetched
-//     several groups ahead in registers);
+//   * a warp works on 16-row tiles; each group of 128 weights of a tile
+//     arrives as one coalesced 512-byte block (one 16-byte load per lane,
+//     prefetched eight groups ahead in registers);
 //   * each lane decodes its 64 codes to exact bf16 values t in {-1,0,+1}
 //     (one LOP3 + one bf16x2 FMA per pair, see decode_pair) which are
 //     directly the A fragments of mma.m16n8k16 -- weights on the MMA M
 //     side, tokens on the N side (8 per n-tile);
 //   * the group partial (exact products, fp32 sums) is scaled by the fp32
 //     value of the FP16 scale and added to the fp32 accumulator: the scale
-//     is never rounded to bf16;
-//   * K is split into S ranges when N alone does not fill the GPU; the
-//     last CTA of a row block to finish sums the S partials in split order
-//     (deterministic, no spin-waiting) and writes Y.
+//     is never rounded to bf16.
 //
 // K-slot order inside an MMA: the MMA sums over its 16 k-slots, so any
 // consistent permutation of k between A and B is free.  Lane (g, c) of
 // MMA j of half h takes physical k = 128*grp + 64h + 16c + 4j + {0,1,2,3}
 // for its k-slots {2c, 2c+1, 2c+8, 2c+9}: its A registers then come from one
 // 16-weight code word of the tiled layout and its B registers are four
-// consecutive activations, one 64-bit shared-memory read.
+// consecutive activations.
+//
+// Two kernels share the per-tile work:
+//   stream_kernel  (X fits in shared memory, the decode case): persistent
+//       CTAs, two per SM; warp w owns the contiguous run [T*w/W, T*(w+1)/W)
+//       of the T = tiles x groups blocks, which is one contiguous byte range
+//       of the tiled layout, so every warp streams without ever draining
+//       its prefetch ring.  A tile split between warps is summed by the
+//       last warp to finish it, in warp order (deterministic, no waiting).
+//   split_kernel   (larger M x K): one CTA per (128-row block, K range);
+//       the last CTA of a row block sums the K-range partials in order.
 
 #include "tern_common.cuh"
 #include "tern_internal.h"
@@ -34,17 +41,260 @@
 namespace tern {
 namespace {
 
-constexpr int kWarps = 8;                 // row tiles per CTA (128 rows)
+constexpr int kWarps = 8;                 // warps per CTA
 constexpr int kThreads = kWarps * 32;
 constexpr int kPrefetch = 8;              // groups in flight per warp
 constexpr int kRowsPerBlock = kWarps * kTileRows;
-constexpr size_t kMaxSmem = 200 * 1024;
+constexpr size_t kSplitMaxSmem = 200 * 1024;
+constexpr size_t kStreamMaxSmem = 110 * 1024;   // two CTAs per SM
+constexpr int kZeroBytes = 32;
 
-struct DecodeArgs {
+__device__ __forceinline__ void store_y(const OutputSplit& out, int m, int64_t n, float v) {
+    int j = 0;
+#pragma unroll
+    for (int i = 1; i < kMaxOutputs; ++i) j += (i < out.n_out && n >= out.offset[i]);
+    out.y[j][(int64_t)m * out.ldy[j] + (n - out.offset[j])] = v;
+}
+
+// Shared-memory byte offsets of one lane's activation fragments.  Token rows
+// >= M point at a zero block with zero strides, so every lane issues the
+// same loads (no divergence) and padding tokens contribute exact zeros.
+template <int MT>
+struct XLanes {
+    uint32_t base[MT];      // group 0, half 0
+    uint32_t gstride[MT];   // per group (256 bytes, or 0)
+    uint32_t hstride[MT];   // per 64-wide half (128 bytes, or 0)
+};
+
+template <int MT>
+__device__ __forceinline__ XLanes<MT> x_lanes(int M, uint32_t row_bytes, uint32_t zero_off, int gq,
+                                              int cq) {
+    XLanes<MT> xl;
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+        const int m = mt * 8 + gq;
+        const bool valid = m < M;
+        xl.base[mt] = valid ? (uint32_t)m * row_bytes + 32u * cq : zero_off;
+        xl.gstride[mt] = valid ? 256u : 0u;
+        xl.hstride[mt] = valid ? 128u : 0u;
+    }
+    return xl;
+}
+
+// One 16x128 tile-group: decode, 8 MMAs per n-tile in two chains, promote.
+template <int MT>
+__device__ __forceinline__ void group_mac(const uint4 cw, uint32_t sw, const uint8_t* smem,
+                                          const XLanes<MT>& xl, uint32_t g, float (&acc)[MT][4]) {
+    float cg[2][MT][4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t lo[8], hi[8];
+        decode_word(h ? cw.z : cw.x, lo);   // row gq
+        decode_word(h ? cw.w : cw.y, hi);   // row gq + 8
+        uint32_t xb[MT][8];
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            const uint8_t* p = smem + xl.base[mt] + g * xl.gstride[mt] + h * xl.hstride[mt];
+            const uint4 v0 = lds_v4(p), v1 = lds_v4(p + 16);
+            xb[mt][0] = v0.x; xb[mt][1] = v0.y; xb[mt][2] = v0.z; xb[mt][3] = v0.w;
+            xb[mt][4] = v1.x; xb[mt][5] = v1.y; xb[mt][6] = v1.z; xb[mt][7] = v1.w;
+        }
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+            mma_bf16_m16n8k16_zc(cg[h][mt], lo[0], hi[0], lo[1], hi[1], xb[mt][0], xb[mt][1]);
+#pragma unroll
+        for (int j = 1; j < 4; ++j)
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+                mma_bf16_m16n8k16(cg[h][mt], lo[2 * j], hi[2 * j], lo[2 * j + 1], hi[2 * j + 1],
+                                  xb[mt][2 * j], xb[mt][2 * j + 1]);
+    }
+    const float s_lo = fp16_bits_to_float(sw), s_hi = fp16_bits_to_float(sw >> 16);
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+        acc[mt][0] = fmaf(s_lo, cg[0][mt][0] + cg[1][mt][0], acc[mt][0]);
+        acc[mt][1] = fmaf(s_lo, cg[0][mt][1] + cg[1][mt][1], acc[mt][1]);
+        acc[mt][2] = fmaf(s_hi, cg[0][mt][2] + cg[1][mt][2], acc[mt][2]);
+        acc[mt][3] = fmaf(s_hi, cg[0][mt][3] + cg[1][mt][3], acc[mt][3]);
+    }
+}
+
+// Write a finished tile's fragments: element e of n-tile mt is row
+// 16*tile + gq + 8*(e/2), token 8*mt + 2*cq + (e%2).
+template <int MT>
+__device__ __forceinline__ void store_tile(const OutputSplit& out, int M, int64_t N, int64_t tile,
+                                           const float (&acc)[MT][4], int gq, int cq) {
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int m = mt * 8 + 2 * cq + (e & 1);
+            const int64_t n = tile * kTileRows + gq + 8 * (e >> 1);
+            if (m < M && n < N) store_y(out, m, n, acc[mt][e]);
+        }
+}
+
+// Stage rows [0, M) of X columns [k0, k0 + ck) in shared memory with row
+// stride ck + 8 elements (the 16-byte pad spreads token rows over all
+// banks), followed by a 32-byte zero block.  Returns the zero block offset.
+__device__ __forceinline__ uint32_t stage_x(uint8_t* smem, const uint16_t* X, int64_t ldx, int M,
+                                            int64_t k0, int ck) {
+    uint16_t* xs = reinterpret_cast<uint16_t*>(smem);
+    const int sx = ck + 8;
+    const int vec_per_row = ck / 8;
+    const int total = M * vec_per_row;
+    for (int i = threadIdx.x; i < total; i += kThreads) {
+        const int m = i / vec_per_row, j = i - m * vec_per_row;
+        const uint4 v = *reinterpret_cast<const uint4*>(X + (int64_t)m * ldx + k0 + 8 * j);
+        *reinterpret_cast<uint4*>(xs + m * sx + 8 * j) = v;
+    }
+    const uint32_t zero_off = (uint32_t)M * (uint32_t)sx * 2u;
+    if (threadIdx.x < kZeroBytes / 16)
+        *reinterpret_cast<uint4*>(smem + zero_off + 16 * threadIdx.x) = make_uint4(0, 0, 0, 0);
+    return zero_off;
+}
+
+// ----------------------------------------------------------- stream kernel
+
+struct StreamArgs {
     const uint16_t* X;
     int64_t ldx;
     const uint8_t* codes;    // tiled code region
     const uint8_t* scales;   // tiled scale region
+    int M;
+    int K;
+    int64_t N;
+    int64_t G;               // groups per row (K / 128)
+    int64_t T;               // tiles x groups
+    int64_t W;               // working warps (<= T)
+    OutputSplit out;
+    int* counters;           // [tiles] arrival counters
+    float* slots;            // [2W][32][MT*4] partial tiles
+};
+
+// Warp that owns block q under the partition [T*w/W, T*(w+1)/W).
+__device__ __forceinline__ int64_t owner_warp(int64_t q, int64_t T, int64_t W) {
+    return ((q + 1) * W - 1) / T;
+}
+
+template <int MT>
+__device__ __noinline__ void flush_partial(const StreamArgs& a, int64_t w, int64_t tile,
+                                           int64_t first_tile, const float (&acc)[MT][4], int lane) {
+    const int gq = lane >> 2, cq = lane & 3;
+    const int64_t slot = 2 * w + (tile == first_tile ? 0 : 1);
+    float4* sp = reinterpret_cast<float4*>(a.slots + (slot * 32 + lane) * (MT * 4));
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) sp[mt] = make_float4(acc[mt][0], acc[mt][1], acc[mt][2], acc[mt][3]);
+    __threadfence();
+    __syncwarp();
+    const int64_t w_first = owner_warp(tile * a.G, a.T, a.W);
+    const int64_t w_last = owner_warp(tile * a.G + a.G - 1, a.T, a.W);
+    int last = 0;
+    if (lane == 0) last = atomicAdd(a.counters + tile, 1) == (int)(w_last - w_first);
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (!last) return;
+    __threadfence();
+    float sum[MT][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sum[mt][e] = 0.f;
+    for (int64_t ww = w_first; ww <= w_last; ++ww) {
+        const int64_t ww_first_tile = (a.T * ww / a.W) / a.G;
+        const int64_t sl = 2 * ww + (tile == ww_first_tile ? 0 : 1);
+        const float4* src = reinterpret_cast<const float4*>(a.slots + (sl * 32 + lane) * (MT * 4));
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            const float4 v = __ldcg(src + mt);
+            sum[mt][0] += v.x; sum[mt][1] += v.y; sum[mt][2] += v.z; sum[mt][3] += v.w;
+        }
+    }
+    store_tile<MT>(a.out, a.M, a.N, tile, sum, gq, cq);
+    if (lane == 0) a.counters[tile] = 0;   // leave the workspace zeroed
+}
+
+template <int MT>
+__global__ void __launch_bounds__(kThreads, 2) stream_kernel(const StreamArgs a) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gq = lane >> 2, cq = lane & 3;
+    const int64_t w = (int64_t)blockIdx.x * kWarps + warp;
+    const bool live = w < a.W;
+    const int64_t q0 = live ? a.T * w / a.W : 0;
+    const int n = live ? static_cast<int>(a.T * (w + 1) / a.W - q0) : 0;
+
+    // 1. Start streaming: weights do not depend on earlier kernels.
+    const uint8_t* cptr = a.codes + (q0 * 32 + lane) * 16;
+    const uint8_t* sptr = a.scales + (q0 * 8 + gq) * 4;
+    uint4 cbuf[kPrefetch];
+    uint32_t sbuf[kPrefetch];
+#pragma unroll
+    for (int d = 0; d < kPrefetch; ++d) {
+        if (d < n) {
+            cbuf[d] = ldg_stream_v4(cptr + d * kCodeBlockBytes);
+            sbuf[d] = ldg_stream_u32(sptr + d * kScaleBlockBytes);
+        } else {
+            cbuf[d] = make_uint4(0, 0, 0, 0);
+            sbuf[d] = 0;
+        }
+    }
+    grid_launch_dependents();
+    grid_dependency_wait();
+
+    // 2. All of X in shared memory.
+    const uint32_t zero_off = stage_x(smem, a.X, a.ldx, a.M, 0, a.K);
+    __syncthreads();
+    const XLanes<MT> xl = x_lanes<MT>(a.M, (uint32_t)(a.K + 8) * 2u, zero_off, gq, cq);
+
+    // 3. Walk this warp's blocks; flush at tile ends and at the range end.
+    int64_t tile = q0 / a.G;
+    uint32_t g = static_cast<uint32_t>(q0 - tile * a.G);
+    const int64_t first_tile = tile;
+    bool whole = g == 0;
+    float acc[MT][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
+
+    for (int base = 0; base < n; base += kPrefetch) {
+#pragma unroll
+        for (int d = 0; d < kPrefetch; ++d) {
+            const int i = base + d;
+            if (i < n) {
+                const uint4 cw = cbuf[d];
+                const uint32_t sw = sbuf[d];
+                if (i + kPrefetch < n) {
+                    cbuf[d] = ldg_stream_v4(cptr + (int64_t)(i + kPrefetch) * kCodeBlockBytes);
+                    sbuf[d] = ldg_stream_u32(sptr + (int64_t)(i + kPrefetch) * kScaleBlockBytes);
+                }
+                group_mac<MT>(cw, sw, smem, xl, g, acc);
+                ++g;
+                if (g == a.G || i == n - 1) {
+                    if (whole && g == a.G)
+                        store_tile<MT>(a.out, a.M, a.N, tile, acc, gq, cq);
+                    else
+                        flush_partial<MT>(a, w, tile, first_tile, acc, lane);
+#pragma unroll
+                    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
+                    ++tile;
+                    g = 0;
+                    whole = true;
+                }
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------ split kernel
+
+struct SplitArgs {
+    const uint16_t* X;
+    int64_t ldx;
+    const uint8_t* codes;
+    const uint8_t* scales;
     int M;
     int64_t N;
     int64_t Np;              // rows padded to 16
@@ -57,17 +307,9 @@ struct DecodeArgs {
     int* counters;           // [n_rb] arrival counters (S > 1)
 };
 
-__device__ __forceinline__ void store_y(const OutputSplit& out, int m, int64_t n, float v) {
-    int j = 0;
-#pragma unroll
-    for (int i = 1; i < kMaxOutputs; ++i) j += (i < out.n_out && n >= out.offset[i]);
-    out.y[j][(int64_t)m * out.ldy[j] + (n - out.offset[j])] = v;
-}
-
 template <int MT>
-__global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a) {
-    extern __shared__ __align__(16) uint8_t smem_raw[];
-    uint16_t* xs = reinterpret_cast<uint16_t*>(smem_raw);
+__global__ void __launch_bounds__(kThreads, 2) split_kernel(const SplitArgs a) {
+    extern __shared__ __align__(16) uint8_t smem[];
     __shared__ int last_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -79,8 +321,6 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
     const int64_t tile = rb * kWarps + warp;
     const bool active = tile < a.R;
 
-    // 1. Start streaming this warp's weights: they do not depend on earlier
-    //    kernels, so this happens before the grid-dependency wait.
     const uint8_t* cptr = a.codes + ((tile * a.G + g0) * 32 + lane) * 16;
     const uint8_t* sptr = a.scales + ((tile * a.G + g0) * 8 + gq) * 4;
     uint4 cbuf[kPrefetch];
@@ -88,8 +328,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
 #pragma unroll
     for (int d = 0; d < kPrefetch; ++d) {
         if (active && d < ng) {
-            cbuf[d] = ldg_stream_v4(cptr + (int64_t)d * kCodeBlockBytes);
-            sbuf[d] = ldg_stream_u32(sptr + (int64_t)d * kScaleBlockBytes);
+            cbuf[d] = ldg_stream_v4(cptr + d * kCodeBlockBytes);
+            sbuf[d] = ldg_stream_u32(sptr + d * kScaleBlockBytes);
         } else {
             cbuf[d] = make_uint4(0, 0, 0, 0);
             sbuf[d] = 0;
@@ -98,22 +338,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
     grid_launch_dependents();
     grid_dependency_wait();
 
-    // 2. Stage X[0:M, 128*g0 : 128*g1] in shared memory, row stride ck + 8
-    //    (the 16-byte pad spreads the 8 token rows over all banks).
     const int ck = ng * kGroup;
-    const int sx = ck + 8;
-    {
-        const int vec_per_row = ck / 8;
-        const int total = a.M * vec_per_row;
-        for (int i = threadIdx.x; i < total; i += kThreads) {
-            const int m = i / vec_per_row, j = i - m * vec_per_row;
-            const uint4 v = *reinterpret_cast<const uint4*>(a.X + (int64_t)m * a.ldx + g0 * kGroup + 8 * j);
-            *reinterpret_cast<uint4*>(xs + m * sx + 8 * j) = v;
-        }
-    }
+    const uint32_t zero_off = stage_x(smem, a.X, a.ldx, a.M, g0 * kGroup, ck);
     __syncthreads();
+    const XLanes<MT> xl = x_lanes<MT>(a.M, (uint32_t)(ck + 8) * 2u, zero_off, gq, cq);
 
-    // 3. Main loop over this split's groups.
     float acc[MT][4];
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
@@ -132,66 +361,14 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
                         cbuf[d] = ldg_stream_v4(cptr + (int64_t)(gi + kPrefetch) * kCodeBlockBytes);
                         sbuf[d] = ldg_stream_u32(sptr + (int64_t)(gi + kPrefetch) * kScaleBlockBytes);
                     }
-                    // two independent MMA chains (one per 64-wide half)
-                    float cg[2][MT][4];
-#pragma unroll
-                    for (int h = 0; h < 2; ++h)
-#pragma unroll
-                        for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) cg[h][mt][e] = 0.f;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        uint32_t lo[8], hi[8];
-                        decode_word(h ? cw.z : cw.x, lo);   // row gq
-                        decode_word(h ? cw.w : cw.y, hi);   // row gq + 8
-                        uint32_t xb[MT][8];
-#pragma unroll
-                        for (int mt = 0; mt < MT; ++mt) {
-                            const int m = mt * 8 + gq;
-                            if (m < a.M) {
-                                const uint16_t* p = xs + m * sx + gi * kGroup + 64 * h + 16 * cq;
-                                const uint4 v0 = lds_v4(p), v1 = lds_v4(p + 8);
-                                xb[mt][0] = v0.x; xb[mt][1] = v0.y; xb[mt][2] = v0.z; xb[mt][3] = v0.w;
-                                xb[mt][4] = v1.x; xb[mt][5] = v1.y; xb[mt][6] = v1.z; xb[mt][7] = v1.w;
-                            } else {
-#pragma unroll
-                                for (int e = 0; e < 8; ++e) xb[mt][e] = 0u;
-                            }
-                        }
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-#pragma unroll
-                            for (int mt = 0; mt < MT; ++mt)
-                                mma_bf16_m16n8k16(cg[h][mt], lo[2 * j], hi[2 * j], lo[2 * j + 1],
-                                                  hi[2 * j + 1], xb[mt][2 * j], xb[mt][2 * j + 1]);
-                    }
-                    const float s_lo = fp16_bits_to_float(sw), s_hi = fp16_bits_to_float(sw >> 16);
-#pragma unroll
-                    for (int mt = 0; mt < MT; ++mt) {
-                        acc[mt][0] = fmaf(s_lo, cg[0][mt][0] + cg[1][mt][0], acc[mt][0]);
-                        acc[mt][1] = fmaf(s_lo, cg[0][mt][1] + cg[1][mt][1], acc[mt][1]);
-                        acc[mt][2] = fmaf(s_hi, cg[0][mt][2] + cg[1][mt][2], acc[mt][2]);
-                        acc[mt][3] = fmaf(s_hi, cg[0][mt][3] + cg[1][mt][3], acc[mt][3]);
-                    }
+                    group_mac<MT>(cw, sw, smem, xl, (uint32_t)gi, acc);
                 }
             }
         }
     }
 
-    // 4. Epilogue.  Fragment element e of n-tile mt: row 16*tile + gq + 8*(e/2),
-    //    token 8*mt + 2*cq + (e%2).
     if (a.S == 1) {
-        if (active) {
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int m = mt * 8 + 2 * cq + (e & 1);
-                    const int64_t n = tile * kTileRows + gq + 8 * (e >> 1);
-                    if (m < a.M && n < a.N) store_y(a.out, m, n, acc[mt][e]);
-                }
-        }
+        if (active) store_tile<MT>(a.out, a.M, a.N, tile, acc, gq, cq);
         return;
     }
 
@@ -225,6 +402,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
     if (threadIdx.x == 0) a.counters[rb] = 0;   // leave the workspace zeroed
 }
 
+size_t align256(size_t v) { return (v + 255) / 256 * 256; }
+
 }  // namespace
 
 int device_sm_count() {
@@ -240,8 +419,26 @@ DecodePlan plan_decode(int64_t M, int64_t N, int64_t K, int sm_count) {
     p.mt = M <= 8 ? 1 : 2;
     const int64_t R = ceil_div(N, kTileRows);
     const int64_t Np = R * kTileRows;
-    p.n_rb = ceil_div(R, kWarps);
     p.groups = K / kGroup;
+    p.n_rb = ceil_div(R, kWarps);
+
+    const size_t stream_smem = (size_t)M * (size_t)(K + 8) * 2 + kZeroBytes;
+    if (stream_smem <= kStreamMaxSmem) {
+        // persistent: two CTAs per SM, every warp owns at least one block
+        const int64_t T = R * p.groups;
+        int64_t warps = (int64_t)sm_count * 2 * kWarps;
+        if (warps > T) warps = T;
+        p.kind = DecodePlan::kStream;
+        p.warps = warps;
+        p.grid = ceil_div(warps, kWarps);
+        p.smem = stream_smem;
+        p.splits = 1;
+        p.max_gps = p.groups;
+        p.ws_bytes = align256((size_t)R * 4) + (size_t)2 * warps * 32 * p.mt * 4 * sizeof(float);
+        return p;
+    }
+
+    p.kind = DecodePlan::kSplit;
     const int64_t slots = (int64_t)sm_count * 2;   // two 256-thread CTAs per SM
     // Pick the split count that minimises (waves x groups per CTA + a fixed
     // start-up cost of ~2 groups), subject to the X slice fitting in smem.
@@ -250,68 +447,94 @@ DecodePlan plan_decode(int64_t M, int64_t N, int64_t K, int sm_count) {
     const int64_t s_max = p.groups < 256 ? p.groups : 256;
     for (int64_t S = 1; S <= s_max; ++S) {
         const int64_t gps = ceil_div(p.groups, S);
-        const size_t smem = (size_t)M * (size_t)(gps * kGroup + 8) * 2;
-        if (smem > kMaxSmem) continue;
+        const size_t smem = (size_t)M * (size_t)(gps * kGroup + 8) * 2 + kZeroBytes;
+        if (smem > kSplitMaxSmem) continue;
         const int64_t waves = ceil_div(p.n_rb * S, slots);
         const double cost = (double)waves * ((double)gps + 2.0);
         if (cost < best - 1e-9) { best = cost; best_s = static_cast<int>(S); }
     }
     p.splits = best_s;
     p.max_gps = ceil_div(p.groups, best_s);
-    p.smem = (size_t)M * (size_t)(p.max_gps * kGroup + 8) * 2;
-    if (p.splits > 1) {
-        const size_t counters = (size_t)ceil_div(p.n_rb * 4, 256) * 256;
-        p.ws_bytes = counters + (size_t)p.splits * (size_t)M * (size_t)Np * 4;
-    } else {
+    p.smem = (size_t)M * (size_t)(p.max_gps * kGroup + 8) * 2 + kZeroBytes;
+    p.grid = p.n_rb * p.splits;
+    p.warps = p.grid * kWarps;
+    if (p.splits > 1)
+        p.ws_bytes = align256((size_t)p.n_rb * 4) + (size_t)p.splits * (size_t)M * (size_t)Np * 4;
+    else
         p.ws_bytes = 0;
-    }
     return p;
 }
 
-cudaError_t launch_decode(const uint16_t* X, int64_t ldx, const uint8_t* tiled, int64_t M,
-                          int64_t N, int64_t K, const OutputSplit& out, void* ws,
-                          const DecodePlan& plan, cudaStream_t stream) {
-    DecodeArgs a = {};
-    a.X = X;
-    a.ldx = ldx;
-    a.R = ceil_div(N, kTileRows);
-    a.G = K / kGroup;
-    a.codes = tiled;
-    a.scales = tiled + a.R * a.G * kCodeBlockBytes;
-    a.M = static_cast<int>(M);
-    a.N = N;
-    a.Np = a.R * kTileRows;
-    a.n_rb = plan.n_rb;
-    a.S = plan.splits;
-    a.out = out;
-    if (plan.splits > 1) {
-        const size_t counters = (size_t)ceil_div(plan.n_rb * 4, 256) * 256;
-        a.counters = static_cast<int*>(ws);
-        a.part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + counters);
-    }
+namespace {
 
+template <typename Kernel, typename Args>
+cudaError_t launch_pdl(Kernel kernel, const Args& a, int64_t grid, size_t smem, size_t max_smem,
+                       cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(max_smem));
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(plan.n_rb * plan.splits));
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = plan.smem;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, a);
+}
 
-    cudaError_t e;
-    if (plan.mt == 1) {
-        e = cudaFuncSetAttribute(decode_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kMaxSmem));
-        if (e != cudaSuccess) return e;
-        return cudaLaunchKernelEx(&cfg, decode_kernel<1>, a);
+}  // namespace
+
+cudaError_t launch_decode(const uint16_t* X, int64_t ldx, const uint8_t* tiled, int64_t M,
+                          int64_t N, int64_t K, const OutputSplit& out, void* ws,
+                          const DecodePlan& plan, cudaStream_t stream) {
+    const int64_t R = ceil_div(N, kTileRows), G = K / kGroup;
+    const uint8_t* codes = tiled;
+    const uint8_t* scales = tiled + R * G * kCodeBlockBytes;
+
+    if (plan.kind == DecodePlan::kStream) {
+        StreamArgs a = {};
+        a.X = X;
+        a.ldx = ldx;
+        a.codes = codes;
+        a.scales = scales;
+        a.M = static_cast<int>(M);
+        a.K = static_cast<int>(K);
+        a.N = N;
+        a.G = G;
+        a.T = R * G;
+        a.W = plan.warps;
+        a.out = out;
+        a.counters = static_cast<int*>(ws);
+        a.slots = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + align256((size_t)R * 4));
+        if (plan.mt == 1)
+            return launch_pdl(stream_kernel<1>, a, plan.grid, plan.smem, kStreamMaxSmem, stream);
+        return launch_pdl(stream_kernel<2>, a, plan.grid, plan.smem, kStreamMaxSmem, stream);
     }
-    e = cudaFuncSetAttribute(decode_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kMaxSmem));
-    if (e != cudaSuccess) return e;
-    return cudaLaunchKernelEx(&cfg, decode_kernel<2>, a);
+
+    SplitArgs a = {};
+    a.X = X;
+    a.ldx = ldx;
+    a.codes = codes;
+    a.scales = scales;
+    a.R = R;
+    a.G = G;
+    a.M = static_cast<int>(M);
+    a.N = N;
+    a.Np = R * kTileRows;
+    a.n_rb = plan.n_rb;
+    a.S = plan.splits;
+    a.out = out;
+    if (plan.splits > 1) {
+        a.counters = static_cast<int*>(ws);
+        a.part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + align256((size_t)plan.n_rb * 4));
+    }
+    if (plan.mt == 1)
+        return launch_pdl(split_kernel<1>, a, plan.grid, plan.smem, kSplitMaxSmem, stream);
+    return launch_pdl(split_kernel<2>, a, plan.grid, plan.smem, kSplitMaxSmem, stream);
 }
 
 }  // namespace tern

@@ -28,16 +28,21 @@ struct OutputSplit {
     int64_t ldy[kMaxOutputs];
 };
 
-// Decode (small-M) plan: K split into S ranges, 128-row blocks, one CTA
-// per (row block, split).
+// Decode (small-M) plan.  kStream: persistent CTAs, X resident in shared
+// memory, each warp streams a contiguous run of 16x128 blocks.  kSplit: one
+// CTA per (128-row block, K range), X slice per CTA.
 struct DecodePlan {
+    enum Kind { kStream = 0, kSplit = 1 };
+    Kind kind;
     int mt;            // n8 token tiles per MMA row tile (1: M<=8, 2: M<=16)
-    int splits;        // S
+    int splits;        // S (kSplit)
     int64_t n_rb;      // 128-row blocks
     int64_t groups;    // K / 128
     int64_t max_gps;   // largest number of groups in one split
+    int64_t grid;      // CTAs
+    int64_t warps;     // working warps
     size_t smem;       // dynamic shared memory per CTA
-    size_t ws_bytes;   // workspace: counters + split partials (0 when S == 1)
+    size_t ws_bytes;   // workspace: counters + partials
 };
 
 int device_sm_count();
