@@ -98,26 +98,26 @@ tern_status tern_unpack(const uint8_t* d_packed, int64_t N, int64_t K, int8_t* d
  * tern_repack from the on-disk pair.  The pages give no GPU layout; they
  * only ask that it be reconciled with the disk layout ([EMB] §3).
  *
- * Rows are padded to Np = 16*ceil(N/16) with weight 0 and scale 0.  With
- * G = K/128 scale groups and R = Np/16 row tiles:
- *   codes : R*G blocks of 512 bytes; block (b,g) at byte (b*G + g)*512.
- *           Lane L = 4*r8 + c (r8 in 0..7, c in 0..3) at byte 16*L holds
- *           four little-endian uint32 words:
- *             word 0: row 16b+r8,   k in [128g +      16c, +16)
- *             word 1: row 16b+r8+8, k in [128g +      16c, +16)
- *             word 2: row 16b+r8,   k in [128g + 64 + 16c, +16)
- *             word 3: row 16b+r8+8, k in [128g + 64 + 16c, +16)
- *           In a word covering k0..k0+15, weight k0+2i is at bits 2i..2i+1
- *           and weight k0+2i+1 at bits 16+2i..17+2i (i = 0..7).  The value
- *           stored is the biased code v = t + 1 in {0,1,2}.
- *   scales: R*G blocks of 32 bytes starting at byte R*G*512; block (b,g) at
- *           R*G*512 + (b*G + g)*32 holds eight little-endian uint32 words,
- *           word r8 = s[16b+r8][g] | s[16b+r8+8][g] << 16 (FP16 bits).
- * A warp streams one block per 16x128 tile: lane L's 16 bytes are exactly
- * the four 16-weight runs that its tensor-core fragments need.
+ * Rows are padded to Np = 128*ceil(N/128) with weight 0 and scale 0.  With
+ * G = K/128 scale groups and R = Np/128 row tiles, a unit is one 128-row x
+ * 128-weight block:
+ *   codes : R*G units of 4096 bytes; unit (b,g) at byte (b*G + g)*4096.
+ *           Half h (0,1) at byte 2048*h of the unit; row r (0..127) of the
+ *           tile at 16*r within the half; the row's 16 bytes are four
+ *           little-endian uint32 words, word q covering the weights
+ *           k0..k0+15 with k0 = 128g + 64h + 16q.  In a word, weight k0+2i
+ *           is at bits 2i..2i+1 and weight k0+2i+1 at bits 16+2i..17+2i
+ *           (i = 0..7).  The value stored is the biased code v = t + 1 in
+ *           {0,1,2}.
+ *   scales: R*G units of 256 bytes starting at byte R*G*4096; unit (b,g)
+ *           at R*G*4096 + (b*G + g)*256 holds the FP16 scales s[128b+r][g]
+ *           for r = 0..127 (little-endian).
+ * A unit is one contiguous 4 KB stream element; one thread per row reads
+ * its own two 16-byte runs, and each 16-weight word decodes to the eight
+ * bf16 pairs of one tensor-core K-step.
  * ---------------------------------------------------------------------- */
 
-/* Bytes of the tiled layout for an N x K weight: 544 * ceil(N/16) * (K/128).
+/* Bytes of the tiled layout for an N x K weight: 4352 * ceil(N/128) * (K/128).
  * Returns 0 for invalid shapes (N < 0, K <= 0 or K % 128 != 0). */
 size_t tern_tiled_bytes(int64_t N, int64_t K);
 

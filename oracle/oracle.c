@@ -121,30 +121,28 @@ int64_t orc_unpack(const uint8_t* packed, int64_t N, int64_t K, int8_t* t) {
 
 /* ------------------------------------------------------------ tiled layout
  *
- * The GPU tile layout.  Rows are padded to Np = 16*ceil(N/16) (padding rows
- * hold weight 0 and scale 0).  With G = K/128 groups and R = Np/16 row tiles:
+ * The GPU tile layout.  Rows are padded to Np = 128*ceil(N/128) (padding
+ * rows hold weight 0 and scale 0).  With G = K/128 groups and R = Np/128
+ * row tiles, a unit is one 128-row x 128-weight block:
  *
- *   codes:  R*G blocks of 512 bytes; block (b,g) starts at (b*G + g)*512.
- *           Inside a block, 32 lanes of 16 bytes: lane L = 4*r8 + c
- *           (r8 in 0..7, c in 0..3) starts at 16*L and holds four
- *           little-endian 32-bit words:
- *             word 0: row 16b+r8,   k in [128g +      16c, +16)
- *             word 1: row 16b+r8+8, k in [128g +      16c, +16)
- *             word 2: row 16b+r8,   k in [128g + 64 + 16c, +16)
- *             word 3: row 16b+r8+8, k in [128g + 64 + 16c, +16)
- *           In a word covering k0..k0+15, weight k0+2i sits at bits
- *           2i..2i+1 and weight k0+2i+1 at bits 16+2i..17+2i (i in 0..7).
+ *   codes:  R*G units of 4096 bytes; unit (b,g) starts at (b*G + g)*4096.
+ *           Inside a unit, half h (0,1) starts at 2048*h, row r (0..127)
+ *           of the tile at 16*r within the half, and the row's 16 bytes
+ *           are four little-endian 32-bit words; word q covers the weights
+ *           k0..k0+15 with k0 = 128g + 64h + 16q.
+ *           In a word, weight k0+2i sits at bits 2i..2i+1 and weight
+ *           k0+2i+1 at bits 16+2i..17+2i (i in 0..7).
  *           The stored value is the biased code v = t + 1 in {0,1,2}.
- *   scales: R*G blocks of 32 bytes from byte R*G*512; block (b,g) starts at
- *           R*G*512 + (b*G + g)*32 and holds eight little-endian 32-bit
- *           words; word r8 = fp16(s[16b+r8][g]) | fp16(s[16b+r8+8][g]) << 16.
+ *   scales: R*G units of 256 bytes from byte R*G*4096; unit (b,g) starts
+ *           at R*G*4096 + (b*G + g)*256 and holds the 128 fp16 scales
+ *           s[128b + r][g], r = 0..127, little-endian.
  *
- *   total:  R*G*544 bytes.
+ *   total:  R*G*4352 bytes.
  */
 
 int64_t orc_tiled_bytes(int64_t N, int64_t K) {
-    int64_t R = (N + 15) / 16, G = K / 128;
-    return R * G * 544;
+    int64_t R = (N + 127) / 128, G = K / 128;
+    return R * G * 4352;
 }
 
 static void put_u32(uint8_t* p, uint32_t w) {
@@ -159,19 +157,18 @@ static uint32_t get_u32(const uint8_t* p) {
    position of that weight inside it. */
 static void tiled_code_position(int64_t K, int64_t n, int64_t k, int64_t* word_off, int* bit) {
     int64_t G = K / 128;
-    int64_t b = n / 16, r = n % 16, r8 = r % 8, rhi = r / 8;
+    int64_t b = n / 128, r = n % 128;
     int64_t g = k / 128, kk = k % 128;
-    int64_t h = kk / 64, c = (kk % 64) / 16, j = kk % 16;
-    int64_t lane = 4 * r8 + c, q = 2 * h + rhi;
-    *word_off = (b * G + g) * 512 + 16 * lane + 4 * q;
+    int64_t h = kk / 64, q = (kk % 64) / 16, j = kk % 16;
+    *word_off = (b * G + g) * 4096 + 2048 * h + 16 * r + 4 * q;
     *bit = (int)(16 * (j % 2) + 2 * (j / 2));
 }
 
-static int64_t tiled_scale_position(int64_t N, int64_t K, int64_t n, int64_t g, int* shift) {
-    int64_t R = (N + 15) / 16, G = K / 128;
-    int64_t b = n / 16, r = n % 16;
-    *shift = (int)(16 * (r / 8));
-    return R * G * 512 + (b * G + g) * 32 + 4 * (r % 8);
+/* Byte offset of the fp16 scale of row n, group g. */
+static int64_t tiled_scale_position(int64_t N, int64_t K, int64_t n, int64_t g) {
+    int64_t R = (N + 127) / 128, G = K / 128;
+    int64_t b = n / 128, r = n % 128;
+    return R * G * 4096 + (b * G + g) * 256 + 2 * r;
 }
 
 /* on-disk packed [N,K/4] + fp16 scales [N,K/128] -> tiled.
@@ -179,7 +176,7 @@ static int64_t tiled_scale_position(int64_t N, int64_t K, int64_t n, int64_t g, 
 int64_t orc_repack(const uint8_t* packed, const uint16_t* scales, int64_t N, int64_t K,
                    uint8_t* tiled) {
     int64_t reserved = 0;
-    int64_t Np = (N + 15) / 16 * 16, G = K / 128;
+    int64_t Np = (N + 127) / 128 * 128, G = K / 128;
     memset(tiled, 0, (size_t)orc_tiled_bytes(N, K));
     for (int64_t n = 0; n < Np; ++n) {
         for (int64_t k = 0; k < K; ++k) {
@@ -197,11 +194,9 @@ int64_t orc_repack(const uint8_t* packed, const uint16_t* scales, int64_t N, int
         }
         for (int64_t g = 0; g < G; ++g) {
             uint16_t s = n < N ? scales[n * G + g] : 0;
-            int shift;
-            int64_t off = tiled_scale_position(N, K, n, g, &shift);
-            uint32_t w = get_u32(tiled + off);
-            w |= (uint32_t)s << shift;
-            put_u32(tiled + off, w);
+            int64_t off = tiled_scale_position(N, K, n, g);
+            tiled[off] = (uint8_t)(s & 0xFF);
+            tiled[off + 1] = (uint8_t)(s >> 8);
         }
     }
     return reserved;
@@ -225,9 +220,8 @@ int64_t orc_unrepack(const uint8_t* tiled, int64_t N, int64_t K,
             packed[n * (K / 4) + k / 4] |= (uint8_t)(code << (2 * (k % 4)));
         }
         for (int64_t g = 0; g < G; ++g) {
-            int shift;
-            int64_t off = tiled_scale_position(N, K, n, g, &shift);
-            scales[n * G + g] = (uint16_t)(get_u32(tiled + off) >> shift);
+            int64_t off = tiled_scale_position(N, K, n, g);
+            scales[n * G + g] = (uint16_t)(tiled[off] | (tiled[off + 1] << 8));
         }
     }
     return invalid;

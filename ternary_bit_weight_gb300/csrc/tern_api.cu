@@ -107,7 +107,7 @@ tern_status tern_unpack(const uint8_t* d_packed, int64_t N, int64_t K, int8_t* d
 size_t tern_tiled_bytes(int64_t N, int64_t K) {
     if (!valid_group_shape(N, K)) return 0;
     return (size_t)ceil_div(N, tern::kTileRows) * (size_t)(K / tern::kGroup) *
-           (size_t)(tern::kCodeBlockBytes + tern::kScaleBlockBytes);
+           (size_t)(tern::kUnitCodeBytes + tern::kUnitScaleBytes);
 }
 
 tern_status tern_repack(const uint8_t* d_packed, const uint16_t* d_scales, int64_t N, int64_t K,

@@ -8,10 +8,10 @@
 
 namespace tern {
 
-constexpr int kGroup = 128;           // weights per FP16 scale along K
-constexpr int kTileRows = 16;         // rows per tile (one m16 tensor-core fragment)
-constexpr int kCodeBlockBytes = 512;  // 16 rows x 128 weights x 2 bits
-constexpr int kScaleBlockBytes = 32;  // 16 FP16 scales
+constexpr int kGroup = 128;            // weights per FP16 scale along K
+constexpr int kTileRows = 128;         // rows per tile of the tiled layout
+constexpr int kUnitCodeBytes = 4096;   // 128 rows x 128 weights x 2 bits
+constexpr int kUnitScaleBytes = 256;   // 128 FP16 scales
 
 __host__ __device__ constexpr int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 

@@ -25,15 +25,10 @@
 // 16-weight code word of the tiled layout and its B registers are four
 // consecutive activations.
 //
-// Two kernels share the per-tile work:
-//   stream_kernel  (X fits in shared memory, the decode case): persistent
-//       CTAs, two per SM; warp w owns the contiguous run [T*w/W, T*(w+1)/W)
-//       of the T = tiles x groups blocks, which is one contiguous byte range
-//       of the tiled layout, so every warp streams without ever draining
-//       its prefetch ring.  A tile split between warps is summed by the
-//       last warp to finish it, in warp order (deterministic, no waiting).
-//   split_kernel   (larger M x K): one CTA per (128-row block, K range);
-//       the last CTA of a row block sums the K-range partials in order.
+// Work split: one CTA of 8 warps per (128-row tile, K range); warp w owns
+// rows 16w..16w+15 of the tile.  When N alone does not fill the GPU, K is
+// split into S ranges and the last CTA of a tile to finish sums the S
+// partials in split order (deterministic, no spin-waiting).
 
 #include "tern_common.cuh"
 #include "tern_internal.h"
@@ -44,9 +39,9 @@ namespace {
 constexpr int kWarps = 8;                 // warps per CTA
 constexpr int kThreads = kWarps * 32;
 constexpr int kPrefetch = 8;              // groups in flight per warp
-constexpr int kRowsPerBlock = kWarps * kTileRows;
+constexpr int kRowsPerBlock = kTileRows;   // one 128-row tile per CTA
+constexpr int kSubRows = 16;               // rows per warp (one m16 fragment)
 constexpr size_t kSplitMaxSmem = 200 * 1024;
-constexpr size_t kStreamMaxSmem = 110 * 1024;   // two CTAs per SM
 constexpr int kZeroBytes = 32;
 
 __device__ __forceinline__ void store_y(const OutputSplit& out, int m, int64_t n, float v) {
@@ -119,17 +114,17 @@ __device__ __forceinline__ void group_mac(const uint4 cw, uint32_t sw, const uin
     }
 }
 
-// Write a finished tile's fragments: element e of n-tile mt is row
-// 16*tile + gq + 8*(e/2), token 8*mt + 2*cq + (e%2).
+// Write a finished 16-row sub-tile's fragments: element e of n-tile mt is
+// row row0 + gq + 8*(e/2), token 8*mt + 2*cq + (e%2).
 template <int MT>
-__device__ __forceinline__ void store_tile(const OutputSplit& out, int M, int64_t N, int64_t tile,
+__device__ __forceinline__ void store_tile(const OutputSplit& out, int M, int64_t N, int64_t row0,
                                            const float (&acc)[MT][4], int gq, int cq) {
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const int m = mt * 8 + 2 * cq + (e & 1);
-            const int64_t n = tile * kTileRows + gq + 8 * (e >> 1);
+            const int64_t n = row0 + gq + 8 * (e >> 1);
             if (m < M && n < N) store_y(out, m, n, acc[mt][e]);
         }
 }
@@ -154,140 +149,6 @@ __device__ __forceinline__ uint32_t stage_x(uint8_t* smem, const uint16_t* X, in
     return zero_off;
 }
 
-// ----------------------------------------------------------- stream kernel
-
-struct StreamArgs {
-    const uint16_t* X;
-    int64_t ldx;
-    const uint8_t* codes;    // tiled code region
-    const uint8_t* scales;   // tiled scale region
-    int M;
-    int K;
-    int64_t N;
-    int64_t G;               // groups per row (K / 128)
-    int64_t T;               // tiles x groups
-    int64_t W;               // working warps (<= T)
-    OutputSplit out;
-    int* counters;           // [tiles] arrival counters
-    float* slots;            // [2W][32][MT*4] partial tiles
-};
-
-// Warp that owns block q under the partition [T*w/W, T*(w+1)/W).
-__device__ __forceinline__ int64_t owner_warp(int64_t q, int64_t T, int64_t W) {
-    return ((q + 1) * W - 1) / T;
-}
-
-template <int MT>
-__device__ __noinline__ void flush_partial(const StreamArgs& a, int64_t w, int64_t tile,
-                                           int64_t first_tile, const float (&acc)[MT][4], int lane) {
-    const int gq = lane >> 2, cq = lane & 3;
-    const int64_t slot = 2 * w + (tile == first_tile ? 0 : 1);
-    float4* sp = reinterpret_cast<float4*>(a.slots + (slot * 32 + lane) * (MT * 4));
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) sp[mt] = make_float4(acc[mt][0], acc[mt][1], acc[mt][2], acc[mt][3]);
-    __threadfence();
-    __syncwarp();
-    const int64_t w_first = owner_warp(tile * a.G, a.T, a.W);
-    const int64_t w_last = owner_warp(tile * a.G + a.G - 1, a.T, a.W);
-    int last = 0;
-    if (lane == 0) last = atomicAdd(a.counters + tile, 1) == (int)(w_last - w_first);
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (!last) return;
-    __threadfence();
-    float sum[MT][4];
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sum[mt][e] = 0.f;
-    for (int64_t ww = w_first; ww <= w_last; ++ww) {
-        const int64_t ww_first_tile = (a.T * ww / a.W) / a.G;
-        const int64_t sl = 2 * ww + (tile == ww_first_tile ? 0 : 1);
-        const float4* src = reinterpret_cast<const float4*>(a.slots + (sl * 32 + lane) * (MT * 4));
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-            const float4 v = __ldcg(src + mt);
-            sum[mt][0] += v.x; sum[mt][1] += v.y; sum[mt][2] += v.z; sum[mt][3] += v.w;
-        }
-    }
-    store_tile<MT>(a.out, a.M, a.N, tile, sum, gq, cq);
-    if (lane == 0) a.counters[tile] = 0;   // leave the workspace zeroed
-}
-
-template <int MT>
-__global__ void __launch_bounds__(kThreads, 2) stream_kernel(const StreamArgs a) {
-    extern __shared__ __align__(16) uint8_t smem[];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int gq = lane >> 2, cq = lane & 3;
-    const int64_t w = (int64_t)blockIdx.x * kWarps + warp;
-    const bool live = w < a.W;
-    const int64_t q0 = live ? a.T * w / a.W : 0;
-    const int n = live ? static_cast<int>(a.T * (w + 1) / a.W - q0) : 0;
-
-    // 1. Start streaming: weights do not depend on earlier kernels.
-    const uint8_t* cptr = a.codes + (q0 * 32 + lane) * 16;
-    const uint8_t* sptr = a.scales + (q0 * 8 + gq) * 4;
-    uint4 cbuf[kPrefetch];
-    uint32_t sbuf[kPrefetch];
-#pragma unroll
-    for (int d = 0; d < kPrefetch; ++d) {
-        if (d < n) {
-            cbuf[d] = ldg_stream_v4(cptr + d * kCodeBlockBytes);
-            sbuf[d] = ldg_stream_u32(sptr + d * kScaleBlockBytes);
-        } else {
-            cbuf[d] = make_uint4(0, 0, 0, 0);
-            sbuf[d] = 0;
-        }
-    }
-    grid_launch_dependents();
-    grid_dependency_wait();
-
-    // 2. All of X in shared memory.
-    const uint32_t zero_off = stage_x(smem, a.X, a.ldx, a.M, 0, a.K);
-    __syncthreads();
-    const XLanes<MT> xl = x_lanes<MT>(a.M, (uint32_t)(a.K + 8) * 2u, zero_off, gq, cq);
-
-    // 3. Walk this warp's blocks; flush at tile ends and at the range end.
-    int64_t tile = q0 / a.G;
-    uint32_t g = static_cast<uint32_t>(q0 - tile * a.G);
-    const int64_t first_tile = tile;
-    bool whole = g == 0;
-    float acc[MT][4];
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
-
-    for (int base = 0; base < n; base += kPrefetch) {
-#pragma unroll
-        for (int d = 0; d < kPrefetch; ++d) {
-            const int i = base + d;
-            if (i < n) {
-                const uint4 cw = cbuf[d];
-                const uint32_t sw = sbuf[d];
-                if (i + kPrefetch < n) {
-                    cbuf[d] = ldg_stream_v4(cptr + (int64_t)(i + kPrefetch) * kCodeBlockBytes);
-                    sbuf[d] = ldg_stream_u32(sptr + (int64_t)(i + kPrefetch) * kScaleBlockBytes);
-                }
-                group_mac<MT>(cw, sw, smem, xl, g, acc);
-                ++g;
-                if (g == a.G || i == n - 1) {
-                    if (whole && g == a.G)
-                        store_tile<MT>(a.out, a.M, a.N, tile, acc, gq, cq);
-                    else
-                        flush_partial<MT>(a, w, tile, first_tile, acc, lane);
-#pragma unroll
-                    for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
-                    ++tile;
-                    g = 0;
-                    whole = true;
-                }
-            }
-        }
-    }
-}
-
 // ------------------------------------------------------------ split kernel
 
 struct SplitArgs {
@@ -307,6 +168,23 @@ struct SplitArgs {
     int* counters;           // [n_rb] arrival counters (S > 1)
 };
 
+// Four 32-bit code words of one lane for one group: rows gq and gq + 8 of
+// the warp's 16 rows, halves 0 and 1, word cq (the tiled unit layout).
+__device__ __forceinline__ uint4 load_lane_codes(const uint8_t* p) {
+    uint4 c;
+    c.x = ldg_stream_u32(p);
+    c.y = ldg_stream_u32(p + 128);
+    c.z = ldg_stream_u32(p + 2048);
+    c.w = ldg_stream_u32(p + 2048 + 128);
+    return c;
+}
+
+__device__ __forceinline__ uint32_t load_lane_scales(const uint8_t* p) {
+    const uint32_t lo = __ldcs(reinterpret_cast<const unsigned short*>(p));
+    const uint32_t hi = __ldcs(reinterpret_cast<const unsigned short*>(p + 16));
+    return lo | (hi << 16);
+}
+
 template <int MT>
 __global__ void __launch_bounds__(kThreads, 2) split_kernel(const SplitArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
@@ -318,18 +196,18 @@ __global__ void __launch_bounds__(kThreads, 2) split_kernel(const SplitArgs a) {
     const int s = static_cast<int>(blockIdx.x / a.n_rb);
     const int64_t g0 = (int64_t)s * a.G / a.S, g1 = (int64_t)(s + 1) * a.G / a.S;
     const int ng = static_cast<int>(g1 - g0);
-    const int64_t tile = rb * kWarps + warp;
-    const bool active = tile < a.R;
+    const int64_t row0 = rb * kTileRows + kSubRows * warp;
+    const bool active = row0 < a.N;
 
-    const uint8_t* cptr = a.codes + ((tile * a.G + g0) * 32 + lane) * 16;
-    const uint8_t* sptr = a.scales + ((tile * a.G + g0) * 8 + gq) * 4;
+    const uint8_t* cptr = a.codes + (rb * a.G + g0) * kUnitCodeBytes + 16 * (kSubRows * warp + gq) + 4 * cq;
+    const uint8_t* sptr = a.scales + (rb * a.G + g0) * kUnitScaleBytes + 2 * (kSubRows * warp + gq);
     uint4 cbuf[kPrefetch];
     uint32_t sbuf[kPrefetch];
 #pragma unroll
     for (int d = 0; d < kPrefetch; ++d) {
         if (active && d < ng) {
-            cbuf[d] = ldg_stream_v4(cptr + d * kCodeBlockBytes);
-            sbuf[d] = ldg_stream_u32(sptr + d * kScaleBlockBytes);
+            cbuf[d] = load_lane_codes(cptr + d * kUnitCodeBytes);
+            sbuf[d] = load_lane_scales(sptr + d * kUnitScaleBytes);
         } else {
             cbuf[d] = make_uint4(0, 0, 0, 0);
             sbuf[d] = 0;
@@ -358,8 +236,8 @@ __global__ void __launch_bounds__(kThreads, 2) split_kernel(const SplitArgs a) {
                     const uint4 cw = cbuf[d];
                     const uint32_t sw = sbuf[d];
                     if (gi + kPrefetch < ng) {
-                        cbuf[d] = ldg_stream_v4(cptr + (int64_t)(gi + kPrefetch) * kCodeBlockBytes);
-                        sbuf[d] = ldg_stream_u32(sptr + (int64_t)(gi + kPrefetch) * kScaleBlockBytes);
+                        cbuf[d] = load_lane_codes(cptr + (int64_t)(gi + kPrefetch) * kUnitCodeBytes);
+                        sbuf[d] = load_lane_scales(sptr + (int64_t)(gi + kPrefetch) * kUnitScaleBytes);
                     }
                     group_mac<MT>(cw, sw, smem, xl, (uint32_t)gi, acc);
                 }
@@ -368,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 2) split_kernel(const SplitArgs a) {
     }
 
     if (a.S == 1) {
-        if (active) store_tile<MT>(a.out, a.M, a.N, tile, acc, gq, cq);
+        if (active) store_tile<MT>(a.out, a.M, a.N, row0, acc, gq, cq);
         return;
     }
 
@@ -378,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 2) split_kernel(const SplitArgs a) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int m = mt * 8 + 2 * cq + (e & 1);
-                const int64_t n = tile * kTileRows + gq + 8 * (e >> 1);
+                const int64_t n = row0 + gq + 8 * (e >> 1);
                 if (m < a.M) a.part[((int64_t)s * a.M + m) * a.Np + n] = acc[mt][e];
             }
     }
@@ -388,12 +266,11 @@ __global__ void __launch_bounds__(kThreads, 2) split_kernel(const SplitArgs a) {
     __syncthreads();
     if (!last_flag) return;
     __threadfence();
-    // Last CTA of this row block: sum the S partials in split order.
-    const int64_t row0 = rb * kRowsPerBlock;
-    const int rows = static_cast<int>((a.Np - row0) < kRowsPerBlock ? (a.Np - row0) : kRowsPerBlock);
-    for (int i = threadIdx.x; i < rows * a.M; i += kThreads) {
-        const int m = i / rows;
-        const int64_t n = row0 + (i - m * rows);
+    // Last CTA of this row tile: sum the S partials in split order.
+    const int64_t t0 = rb * kRowsPerBlock;
+    for (int i = threadIdx.x; i < kRowsPerBlock * a.M; i += kThreads) {
+        const int m = i / kRowsPerBlock;
+        const int64_t n = t0 + (i - m * kRowsPerBlock);
         if (n >= a.N) continue;
         float v = 0.f;
         for (int k = 0; k < a.S; ++k) v += __ldcg(a.part + ((int64_t)k * a.M + m) * a.Np + n);
@@ -420,23 +297,7 @@ DecodePlan plan_decode(int64_t M, int64_t N, int64_t K, int sm_count) {
     const int64_t R = ceil_div(N, kTileRows);
     const int64_t Np = R * kTileRows;
     p.groups = K / kGroup;
-    p.n_rb = ceil_div(R, kWarps);
-
-    const size_t stream_smem = (size_t)M * (size_t)(K + 8) * 2 + kZeroBytes;
-    if (stream_smem <= kStreamMaxSmem) {
-        // persistent: two CTAs per SM, every warp owns at least one block
-        const int64_t T = R * p.groups;
-        int64_t warps = (int64_t)sm_count * 2 * kWarps;
-        if (warps > T) warps = T;
-        p.kind = DecodePlan::kStream;
-        p.warps = warps;
-        p.grid = ceil_div(warps, kWarps);
-        p.smem = stream_smem;
-        p.splits = 1;
-        p.max_gps = p.groups;
-        p.ws_bytes = align256((size_t)R * 4) + (size_t)2 * warps * 32 * p.mt * 4 * sizeof(float);
-        return p;
-    }
+    p.n_rb = R;
 
     p.kind = DecodePlan::kSplit;
     const int64_t slots = (int64_t)sm_count * 2;   // two 256-thread CTAs per SM
@@ -493,27 +354,7 @@ cudaError_t launch_decode(const uint16_t* X, int64_t ldx, const uint8_t* tiled, 
                           const DecodePlan& plan, cudaStream_t stream) {
     const int64_t R = ceil_div(N, kTileRows), G = K / kGroup;
     const uint8_t* codes = tiled;
-    const uint8_t* scales = tiled + R * G * kCodeBlockBytes;
-
-    if (plan.kind == DecodePlan::kStream) {
-        StreamArgs a = {};
-        a.X = X;
-        a.ldx = ldx;
-        a.codes = codes;
-        a.scales = scales;
-        a.M = static_cast<int>(M);
-        a.K = static_cast<int>(K);
-        a.N = N;
-        a.G = G;
-        a.T = R * G;
-        a.W = plan.warps;
-        a.out = out;
-        a.counters = static_cast<int*>(ws);
-        a.slots = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + align256((size_t)R * 4));
-        if (plan.mt == 1)
-            return launch_pdl(stream_kernel<1>, a, plan.grid, plan.smem, kStreamMaxSmem, stream);
-        return launch_pdl(stream_kernel<2>, a, plan.grid, plan.smem, kStreamMaxSmem, stream);
-    }
+    const uint8_t* scales = tiled + R * G * kUnitCodeBytes;
 
     SplitArgs a = {};
     a.X = X;

@@ -137,13 +137,21 @@ __device__ __forceinline__ uint32_t tiled_to_disk_word(uint32_t w, int& bad) {
 
 // Position of tiled code word `idx`: row n and first weight k0.
 __device__ __forceinline__ void tiled_word_coords(int64_t idx, int64_t G, int64_t& n, int64_t& k0) {
-    const int64_t blk = idx >> 7;              // 128 words per (b, g) block
-    const int within = static_cast<int>(idx & 127);
-    const int lane = within >> 2, q = within & 3;
-    const int r8 = lane >> 2, c = lane & 3;
-    const int64_t b = blk / G, g = blk - b * G;
-    n = 16 * b + r8 + 8 * (q & 1);
-    k0 = 128 * g + 64 * (q >> 1) + 16 * c;
+    const int64_t unit = idx >> 10;            // 1024 words per 128x128 unit
+    const int within = static_cast<int>(idx & 1023);
+    const int h = within >> 9, r = (within >> 2) & 127, q = within & 3;
+    const int64_t b = unit / G, g = unit - b * G;
+    n = kTileRows * b + r;
+    k0 = kGroup * g + 64 * h + 16 * q;
+}
+
+// Scale word `j` (two fp16 scales): rows n_lo, n_lo + 1 of group g.
+__device__ __forceinline__ void tiled_scale_coords(int64_t j, int64_t G, int64_t& n_lo, int64_t& g) {
+    const int64_t unit = j >> 6;               // 64 words per unit
+    const int r2 = static_cast<int>(j & 63);
+    const int64_t b = unit / G;
+    g = unit - b * G;
+    n_lo = kTileRows * b + 2 * r2;
 }
 
 __global__ void __launch_bounds__(kThreads)
@@ -161,13 +169,10 @@ repack_kernel(const uint8_t* __restrict__ packed, const uint16_t* __restrict__ s
             if (n < N) src = *reinterpret_cast<const uint32_t*>(packed + n * (K / 4) + k0 / 4);
             tiled[i] = disk_to_tiled_word(src, bad);
         } else {
-            const int64_t j = i - code_words;
-            const int64_t blk = j >> 3;
-            const int r8 = static_cast<int>(j & 7);
-            const int64_t b = blk / G, g = blk - b * G;
-            const int64_t n_lo = 16 * b + r8, n_hi = n_lo + 8;
+            int64_t n_lo, g;
+            tiled_scale_coords(i - code_words, G, n_lo, g);
             const uint32_t s_lo = n_lo < N ? scales[n_lo * G + g] : 0u;
-            const uint32_t s_hi = n_hi < N ? scales[n_hi * G + g] : 0u;
+            const uint32_t s_hi = n_lo + 1 < N ? scales[(n_lo + 1) * G + g] : 0u;
             tiled[i] = s_lo | (s_hi << 16);
         }
     }
@@ -190,14 +195,11 @@ unrepack_kernel(const uint32_t* __restrict__ tiled, int64_t N, int64_t K, int64_
                 *reinterpret_cast<uint32_t*>(packed + n * (K / 4) + k0 / 4) = tiled_to_disk_word(w, bad);
             }
         } else {
-            const int64_t j = i - code_words;
-            const int64_t blk = j >> 3;
-            const int r8 = static_cast<int>(j & 7);
-            const int64_t b = blk / G, g = blk - b * G;
-            const int64_t n_lo = 16 * b + r8, n_hi = n_lo + 8;
+            int64_t n_lo, g;
+            tiled_scale_coords(i - code_words, G, n_lo, g);
             const uint32_t w = tiled[i];
             if (n_lo < N) scales[n_lo * G + g] = static_cast<uint16_t>(w & 0xFFFFu);
-            if (n_hi < N) scales[n_hi * G + g] = static_cast<uint16_t>(w >> 16);
+            if (n_lo + 1 < N) scales[(n_lo + 1) * G + g] = static_cast<uint16_t>(w >> 16);
         }
     }
     count_errors(err, bad);
@@ -252,8 +254,8 @@ cudaError_t launch_unpack(const uint8_t* packed, int64_t count, int8_t* t, int32
 cudaError_t launch_repack(const uint8_t* packed, const uint16_t* scales, int64_t N, int64_t K,
                           uint8_t* tiled, int32_t* err, cudaStream_t stream) {
     const int64_t R = ceil_div(N, kTileRows), G = K / kGroup;
-    const int64_t code_words = R * G * (kCodeBlockBytes / 4);
-    const int64_t scale_words = R * G * (kScaleBlockBytes / 4);
+    const int64_t code_words = R * G * (kUnitCodeBytes / 4);
+    const int64_t scale_words = R * G * (kUnitScaleBytes / 4);
     return launch_flat(repack_kernel, code_words + scale_words, stream, packed, scales, N, K,
                        code_words, scale_words, reinterpret_cast<uint32_t*>(tiled), err);
 }
@@ -261,8 +263,8 @@ cudaError_t launch_repack(const uint8_t* packed, const uint16_t* scales, int64_t
 cudaError_t launch_unrepack(const uint8_t* tiled, int64_t N, int64_t K, uint8_t* packed,
                             uint16_t* scales, int32_t* err, cudaStream_t stream) {
     const int64_t R = ceil_div(N, kTileRows), G = K / kGroup;
-    const int64_t code_words = R * G * (kCodeBlockBytes / 4);
-    const int64_t scale_words = R * G * (kScaleBlockBytes / 4);
+    const int64_t code_words = R * G * (kUnitCodeBytes / 4);
+    const int64_t scale_words = R * G * (kUnitScaleBytes / 4);
     return launch_flat(unrepack_kernel, code_words + scale_words, stream,
                        reinterpret_cast<const uint32_t*>(tiled), N, K, code_words, scale_words,
                        packed, scales, err);

@@ -147,8 +147,8 @@ def test_tiled_hand_worked_code_positions():
         N, K, n, k, t, off, val = [int(v) for v in parts[1:6]] + [int(parts[6]), int(parts[7], 16)]
         packed, scales = _one_weight(N, K, n, k, t)
         tiled, _ = oracle.repack(packed, scales, K)
-        R, G = (N + 15) // 16, K // 128
-        codes = tiled[: R * G * 512]
+        R, G = (N + 127) // 128, K // 128
+        codes = tiled[: R * G * 4096]
         assert codes[off] == val, (parts, hex(codes[off]))
         others = np.delete(codes, off)
         assert np.all(others == 0x55), parts
@@ -165,19 +165,19 @@ def test_tiled_hand_worked_scale_positions():
         scales = np.zeros((N, K // 128), dtype=np.uint16)
         scales[n, g] = 0xABCD
         tiled, _ = oracle.repack(packed, scales, K)
-        R, G = (N + 15) // 16, K // 128
-        sc = tiled[R * G * 512:]
+        R, G = (N + 127) // 128, K // 128
+        sc = tiled[R * G * 4096:]
         assert tiled[off] == 0xCD and tiled[off + 1] == 0xAB, parts
         assert int(np.count_nonzero(sc)) == 2, parts
 
 
-@pytest.mark.parametrize("N,K", [(16, 128), (20, 256), (1, 128), (33, 384), (48, 1024)])
+@pytest.mark.parametrize("N,K", [(16, 128), (20, 256), (1, 128), (33, 384), (130, 1024), (256, 256)])
 def test_repack_round_trip(N, K):
     rng = np.random.default_rng(N * 1000 + K)
     raw = rng.integers(0, 256, size=(N, K // 4), dtype=np.uint8)
     scales = rng.integers(0, 1 << 16, size=(N, K // 128), dtype=np.uint16)
     tiled, reserved = oracle.repack(raw, scales, K)
-    assert tiled.size == oracle.tiled_bytes(N, K) == ((N + 15) // 16) * (K // 128) * 544
+    assert tiled.size == oracle.tiled_bytes(N, K) == ((N + 127) // 128) * (K // 128) * 4352
     codes = np.stack([(raw >> s) & 3 for s in (0, 2, 4, 6)])
     assert reserved == int((codes == 3).sum())
     packed2, scales2, invalid = oracle.unrepack(tiled, N, K)
@@ -188,9 +188,9 @@ def test_repack_round_trip(N, K):
     assert np.array_equal(t_back, t_raw)   # same weights, code 11 canonicalised to 00
     assert np.array_equal(scales2, scales)
     # padding rows of the last tile hold weight 0 (v = 1) and scale 0
-    R, G = (N + 15) // 16, K // 128
-    if N % 16:
-        tt = np.zeros(((N + 15) // 16 * 16, K), dtype=np.int8)
+    R, G = (N + 127) // 128, K // 128
+    if N % 128:
+        tt = np.zeros(((N + 127) // 128 * 128, K), dtype=np.int8)
         tt[:N] = t_raw
         p_full, _ = oracle.pack(tt)
         s_full = np.zeros((tt.shape[0], G), dtype=np.uint16)
