@@ -179,6 +179,27 @@ tern_status tern_linear_multi(const uint16_t* d_X, int64_t ldx, const void* d_ti
                               float* const* d_Ys, const int64_t* ldys,
                               void* d_ws, size_t ws_bytes, void* stream);
 
+/* tern_linear for callers that cannot allocate device memory, e.g. code
+ * running while a CUDA graph is being captured (where cudaMalloc is not
+ * allowed) or a plug-in whose device memory belongs to a host framework's
+ * allocator.  The source pages have no counterpart: this is a library
+ * convenience.  Arguments and results are those of tern_linear; instead of a
+ * caller workspace the call uses a scratch array built into the library
+ * (8 MiB per device, held by every GPU that loads the library until the
+ * process exits).  It allocates nothing.
+ *   - Problems whose tern_workspace_bytes(M, N, K) exceeds 8 MiB return
+ *     TERN_ERR_SIZE before anything is enqueued.
+ *   - The first call on a device (with that device current) looks up the
+ *     array's device address and may load the library's GPU code; make that
+ *     first call before any stream capture.
+ *   - Each call clears the part of the array it uses (an asynchronous
+ *     memset on `stream`) before its kernels run.  All calls share the one
+ *     array, so calls that may overlap in time on the GPU race; serialise
+ *     them (one stream) or use tern_linear with separate workspaces. */
+tern_status tern_linear_noalloc(const uint16_t* d_X, int64_t ldx, const void* d_tiled,
+                                int64_t M, int64_t N, int64_t K, float* d_Y, int64_t ldy,
+                                void* stream);
+
 #ifdef __cplusplus
 }
 #endif

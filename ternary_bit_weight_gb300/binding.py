@@ -21,7 +21,7 @@ STATUS_NAMES = {0: "TERN_OK", 1: "TERN_ERR_NULL", 2: "TERN_ERR_SHAPE", 3: "TERN_
 # Every symbol include/tern.h declares.
 EXPORTED = ("tern_status_string", "tern_version", "tern_pack", "tern_unpack", "tern_tiled_bytes",
             "tern_repack", "tern_unrepack", "tern_workspace_bytes", "tern_linear",
-            "tern_linear_multi")
+            "tern_linear_multi", "tern_linear_noalloc")
 
 
 class TernError(RuntimeError):
@@ -57,6 +57,8 @@ def _load():
     lib.tern_linear_multi.argtypes = [vp, i64, vp, i64, i64, i32, ctypes.POINTER(i64),
                                       ctypes.POINTER(vp), ctypes.POINTER(i64), vp, sz, vp]
     lib.tern_linear_multi.restype = i32
+    lib.tern_linear_noalloc.argtypes = [vp, i64, vp, i64, i64, i64, vp, i64, vp]
+    lib.tern_linear_noalloc.restype = i32
     return lib
 
 
@@ -154,3 +156,9 @@ def tern_linear_multi(X, ldx: int, tiled, M: int, K: int, n_sizes, Ys, ldys, ws=
         ws_bytes = 0 if ws is None or isinstance(ws, int) else ws.numel() * ws.element_size()
     _check(_lib.tern_linear_multi(_p(X), ldx, _p(tiled), M, K, n_out, sizes, ptrs, lds, _p(ws),
                                   ws_bytes, _s(stream)), "tern_linear_multi")
+
+
+def tern_linear_noalloc(X, ldx: int, tiled, M: int, N: int, K: int, Y, ldy: int, stream=None):
+    """tern_linear with the library's built-in scratch instead of a workspace."""
+    _check(_lib.tern_linear_noalloc(_p(X), ldx, _p(tiled), M, N, K, _p(Y), ldy, _s(stream)),
+           "tern_linear_noalloc")
