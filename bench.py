@@ -190,7 +190,7 @@ class Step:
             X = self.x_dev.data_ptr() + 2 * xo
             Yp = self.y_dev.data_ptr() + 4 * yo
             self.calls.append((lin, X, tiled[(layer, lin.name)], Yp))
-        self.launches_per_call = -(-M // 16)
+        self.launches_per_call = 1
 
     def run_call(self, call, stream=None):
         tb, M = self.tb, self.M
@@ -415,7 +415,7 @@ def main():
     achieved = step.bytes / step.launches / avg_launch_s / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                 "frac": achieved / hbm_peak, "traffic": None, "peak_source": peak_src,
-                "kernel": "decode_kernel<1> (tern_linear / tern_linear_multi, M<=8)"}
+                "kernel": "umma_kernel<16> (tern_linear / tern_linear_multi, M<=16)"}
 
     out = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,

@@ -151,11 +151,13 @@ tern_status tern_unrepack(const void* d_tiled, int64_t N, int64_t K, uint8_t* d_
  *   d_tiled  device tiled weights for N x K (tern_repack); 16-byte aligned
  *   d_Y      device fp32 [M, ldy] row-major output, ldy >= N; 4-byte aligned
  *   d_ws     device workspace of ws_bytes >= tern_workspace_bytes(M, N, K),
- *            256-byte aligned; may be NULL when that size is 0.  It must
- *            be zero-filled before its first use; every completed call
- *            leaves it zero-filled again, so one workspace can serve a
- *            sequence of calls on one stream.  Calls that may overlap in
- *            time need separate workspaces.
+ *            256-byte aligned.  It must be zero-filled before its first
+ *            use; every completed call leaves its counters at zero again,
+ *            so one workspace can serve a sequence of calls on one stream.
+ *            Calls that may overlap in time need separate workspaces.  Its
+ *            first 32-bit word is an error word: the kernel sets it non-zero
+ *            (and returns early, leaving Y incomplete) only if a pipeline
+ *            wait timed out, which correct inputs never cause.
  * M == 0 or N == 0 is a no-op.  K must be a positive multiple of 128.
  * X is read after any preceding kernel on the stream completes; kernels
  * launched with programmatic dependent launch may begin streaming weights
@@ -185,9 +187,9 @@ tern_status tern_linear_multi(const uint16_t* d_X, int64_t ldx, const void* d_ti
  * allocator.  The source pages have no counterpart: this is a library
  * convenience.  Arguments and results are those of tern_linear; instead of a
  * caller workspace the call uses a scratch array built into the library
- * (8 MiB per device, held by every GPU that loads the library until the
+ * (16 MiB per device, held by every GPU that loads the library until the
  * process exits).  It allocates nothing.
- *   - Problems whose tern_workspace_bytes(M, N, K) exceeds 8 MiB return
+ *   - Problems whose tern_workspace_bytes(M, N, K) exceeds 16 MiB return
  *     TERN_ERR_SIZE before anything is enqueued.
  *   - The first call on a device (with that device current) looks up the
  *     array's device address and may load the library's GPU code; make that

@@ -18,44 +18,18 @@ inline tern_status from_cuda(cudaError_t e) { return e == cudaSuccess ? TERN_OK 
 
 inline bool valid_group_shape(int64_t N, int64_t K) { return N >= 0 && K > 0 && K % tern::kGroup == 0; }
 
-// Workspace of the decode path for one launch of up to 16 rows of X, and the
-// maximum over the launches a call with M rows makes.
-size_t decode_ws_bytes(int64_t M, int64_t N, int64_t K, int sms) {
-    if (M <= 0 || N <= 0) return 0;
-    size_t need = 0;
-    const int64_t full = M >= tern::kDecodeMaxM ? tern::kDecodeMaxM : M;
-    need = tern::plan_decode(full, N, K, sms).ws_bytes;
-    const int64_t rem = M % tern::kDecodeMaxM;
-    if (M > tern::kDecodeMaxM && rem != 0) {
-        const size_t r = tern::plan_decode(rem, N, K, sms).ws_bytes;
-        if (r > need) need = r;
-    }
-    return need;
-}
-
 tern_status run_linear(const uint16_t* X, int64_t ldx, const void* tiled, int64_t M, int64_t N,
                        int64_t K, const tern::OutputSplit& out, void* ws, size_t ws_bytes,
                        cudaStream_t stream) {
     const int sms = tern::device_sm_count();
     if (sms <= 0) return TERN_ERR_UNSUPPORTED;
-    const size_t need = decode_ws_bytes(M, N, K, sms);
-    if (need > 0) {
-        if (ws == nullptr) return TERN_ERR_NULL;
-        if (ws_bytes < need) return TERN_ERR_SIZE;
-        if (!aligned(ws, 256)) return TERN_ERR_ALIGN;
-    }
-    // Batches of up to 16 rows go through the decode kernel; larger M is
-    // processed 16 rows at a time.
-    for (int64_t m0 = 0; m0 < M; m0 += tern::kDecodeMaxM) {
-        const int64_t mc = (M - m0) < tern::kDecodeMaxM ? (M - m0) : tern::kDecodeMaxM;
-        tern::OutputSplit o = out;
-        for (int j = 0; j < o.n_out; ++j) o.y[j] = out.y[j] + m0 * out.ldy[j];
-        const tern::DecodePlan plan = tern::plan_decode(mc, N, K, sms);
-        const cudaError_t e = tern::launch_decode(X + m0 * ldx, ldx, static_cast<const uint8_t*>(tiled),
-                                                  mc, N, K, o, ws, plan, stream);
-        if (e != cudaSuccess) return TERN_ERR_CUDA;
-    }
-    return TERN_OK;
+    const tern::UmmaPlan plan = tern::plan_umma(M, N, K, sms);
+    if (ws == nullptr) return TERN_ERR_NULL;
+    if (ws_bytes < plan.ws_bytes) return TERN_ERR_SIZE;
+    if (!aligned(ws, 256)) return TERN_ERR_ALIGN;
+    const cudaError_t e = tern::launch_umma(X, ldx, static_cast<const uint8_t*>(tiled), M, N, K, out,
+                                            ws, plan, stream);
+    return e == cudaSuccess ? TERN_OK : TERN_ERR_CUDA;
 }
 
 tern_status check_x_w(const uint16_t* X, int64_t ldx, const void* tiled, int64_t M, int64_t K) {
@@ -135,7 +109,7 @@ tern_status tern_unrepack(const void* d_tiled, int64_t N, int64_t K, uint8_t* d_
 
 size_t tern_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     if (M <= 0 || !valid_group_shape(N, K) || N == 0) return 0;
-    return decode_ws_bytes(M, N, K, tern::device_sm_count());
+    return tern::plan_umma(M, N, K, tern::device_sm_count()).ws_bytes;
 }
 
 tern_status tern_linear(const uint16_t* d_X, int64_t ldx, const void* d_tiled, int64_t M, int64_t N,

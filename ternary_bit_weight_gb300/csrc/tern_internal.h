@@ -55,4 +55,24 @@ cudaError_t launch_decode(const uint16_t* X, int64_t ldx, const uint8_t* tiled, 
                           int64_t N, int64_t K, const OutputSplit& out, void* ws,
                           const DecodePlan& plan, cudaStream_t stream);
 
+// Tensor-core (tcgen05) plan: token tiles of `ntok`, persistent CTAs whose
+// decode warpgroups each stream a contiguous range of 128x128 units.
+struct UmmaPlan {
+    int ntok;              // tokens per tile (UMMA N): 16, 32, 64 or 128
+    int64_t R;             // 128-row tiles
+    int64_t G;             // groups per row
+    int64_t token_tiles;
+    int64_t U;             // units = token_tiles x R x G
+    int64_t V;             // workers
+    int64_t grid;          // CTAs
+    size_t smem;           // dynamic shared memory per CTA
+    size_t ws_bytes;       // workspace: error word, tile counters, partial slots
+};
+
+UmmaPlan plan_umma(int64_t M, int64_t N, int64_t K, int sm_count);
+
+cudaError_t launch_umma(const uint16_t* X, int64_t ldx, const uint8_t* tiled, int64_t M, int64_t N,
+                        int64_t K, const OutputSplit& out, void* ws, const UmmaPlan& plan,
+                        cudaStream_t stream);
+
 }  // namespace tern

@@ -27,7 +27,7 @@
 
 namespace {
 
-constexpr size_t kScratchBytes = size_t(8) << 20;   // 8 MiB per device
+constexpr size_t kScratchBytes = size_t(16) << 20;   // 16 MiB per device
 constexpr int kMaxDevices = 64;
 
 __device__ __align__(256) uint8_t g_scratch[kScratchBytes];
