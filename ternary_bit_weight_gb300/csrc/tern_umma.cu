@@ -46,13 +46,15 @@ constexpr int kDecWarps = 4 * kNWG;
 constexpr int kProducerWarp = kDecWarps;
 constexpr int kMmaWarp = kDecWarps + 1;
 constexpr int kUThreads = (kDecWarps + 2) * 32;
-constexpr int kACols = 64;                       // tensor-memory columns of one unit's A
 constexpr int kWorkspaceErr = 256;               // error word + padding at the workspace start
 
 template <int NTOK>
 struct Cfg {
     static constexpr int kDBuf = NTOK <= 64 ? 2 : 1;
-    static constexpr int kColsUsed = kNWG * kACols + kNWG * kDBuf * NTOK;
+    // decoded A lives in a ring of 32-column half-unit buffers per worker
+    static constexpr int kAHalves = (NTOK == 16 || NTOK >= 64) ? 3 : 2;
+    static constexpr int kAColsW = 32 * kAHalves;
+    static constexpr int kColsUsed = kNWG * kAColsW + kNWG * kDBuf * NTOK;
     static constexpr int kTmemCols = kColsUsed <= 256 ? 256 : 512;
     static constexpr int kCtasPerSm = kTmemCols <= 256 ? 2 : 1;
     static constexpr int kXBox = NTOK * 128;                 // one 64-wide X box
@@ -81,7 +83,7 @@ struct UmmaArgs {
     OutputSplit out;
     int* err;                // workspace error word
     int* counters;           // [token tiles x R][4 row quarters]
-    float* slots;            // [2V][128][NTOK]
+    float* slots;            // [2V][NTOK][128] (column-major per slot)
 };
 
 __device__ __forceinline__ void store_y(const OutputSplit& out, int m, int64_t n, float v) {
@@ -98,8 +100,10 @@ __device__ __forceinline__ int64_t owner_worker(int64_t u, int64_t U, int64_t V)
 // Finish a tile whose group partials this worker holds in acc (thread =
 // row r of the tile, acc[m] = token m of the tile).  `whole`: this worker
 // covered every group of the tile, so it owns the result.  Otherwise each
-// warp (32 rows) publishes its partial and the last contributing worker to
-// arrive for that row quarter sums all partials in worker order.
+// warp (32 rows) publishes the valid token columns of its partial and the
+// last contributing worker to arrive for that row quarter sums all
+// partials in worker order.  Slots are column-major ([slot][token][128
+// rows]) so a warp's column is one contiguous 128-byte run.
 template <int NTOK>
 __device__ __forceinline__ void flush_tile(const UmmaArgs& a, int64_t v, int64_t tile_id,
                                            int64_t first_tile, bool whole, float (&acc)[NTOK],
@@ -116,31 +120,35 @@ __device__ __forceinline__ void flush_tile(const UmmaArgs& a, int64_t v, int64_t
         return;
     }
     const int64_t slot = 2 * v + (tile_id == first_tile ? 0 : 1);
-    float4* sp = reinterpret_cast<float4*>(a.slots + (slot * kTileRows + r) * NTOK);
+    float* sp = a.slots + slot * (kTileRows * NTOK) + r;
 #pragma unroll
-    for (int m = 0; m < NTOK; m += 4) sp[m / 4] = make_float4(acc[m], acc[m + 1], acc[m + 2], acc[m + 3]);
-    __threadfence();
+    for (int m = 0; m < NTOK; ++m)
+        if (m < mvalid) sp[m * kTileRows] = acc[m];
     __syncwarp();
-    const int64_t w_first = owner_worker(tile_id * a.G, a.U, a.V);
-    const int64_t w_last = owner_worker(tile_id * a.G + a.G - 1, a.U, a.V);
+    const int64_t t0 = tile_id * a.G;
+    const int64_t w_first = owner_worker(t0, a.U, a.V);
+    const int64_t w_last = owner_worker(t0 + a.G - 1, a.U, a.V);
     int* counter = a.counters + tile_id * 4 + quad;
     int last = 0;
-    if (lane == 0) last = atomicAdd(counter, 1) == static_cast<int>(w_last - w_first);
+    if (lane == 0) {
+        __threadfence();   // publish the warp's slot writes (ordered by the warp barrier)
+        last = atomicAdd(counter, 1) == static_cast<int>(w_last - w_first);
+        if (last) __threadfence();
+    }
     last = __shfl_sync(0xffffffffu, last, 0);
     if (!last) return;
-    __threadfence();
-    // sum the partials in worker order (this worker's own included)
+    __syncwarp();   // order the lanes' loads after lane 0's acquire
+    // the first contributor's range starts before this tile (its partial
+    // is its "last tile" slot) unless it starts exactly at the tile start
+    const int first_side = (a.U * w_first < t0 * a.V) ? 1 : 0;
 #pragma unroll
     for (int m = 0; m < NTOK; ++m) acc[m] = 0.f;
     for (int64_t ww = w_first; ww <= w_last; ++ww) {
-        const int64_t ww_first_tile = (a.U * ww / a.V) / a.G;
-        const int64_t sl = 2 * ww + (tile_id == ww_first_tile ? 0 : 1);
-        const float4* src = reinterpret_cast<const float4*>(a.slots + (sl * kTileRows + r) * NTOK);
+        const int64_t sl = 2 * ww + (ww == w_first ? first_side : 0);
+        const float* src = a.slots + sl * (kTileRows * NTOK) + r;
 #pragma unroll
-        for (int m = 0; m < NTOK; m += 4) {
-            const float4 q = __ldcg(src + m / 4);
-            acc[m] += q.x; acc[m + 1] += q.y; acc[m + 2] += q.z; acc[m + 3] += q.w;
-        }
+        for (int m = 0; m < NTOK; ++m)
+            if (m < mvalid) acc[m] += __ldcg(src + m * kTileRows);
     }
     if (row < a.N)
 #pragma unroll
@@ -155,10 +163,44 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return __all_sync(0xffffffffu, got);
 }
 
-template <int NTOK>
+// Position of a unit in (token tile, row tile, group) order, advanced by
+// increments so the per-unit loops do no integer division.
+struct UnitCursor {
+    int32_t g;    // group along K
+    int32_t b;    // 128-row tile
+    int32_t tt;   // token tile
+    int32_t cu;   // unit of the tiled weight: b * G + g
+};
+
+__device__ __forceinline__ UnitCursor cursor_at(int64_t u, int64_t R, int64_t G) {
+    const int64_t RG = R * G;
+    UnitCursor c;
+    c.tt = static_cast<int32_t>(u / RG);
+    const int64_t rem = u - (int64_t)c.tt * RG;
+    c.b = static_cast<int32_t>(rem / G);
+    c.g = static_cast<int32_t>(rem - (int64_t)c.b * G);
+    c.cu = static_cast<int32_t>(rem);
+    return c;
+}
+
+__device__ __forceinline__ void cursor_next(UnitCursor& c, int32_t R, int32_t G) {
+    ++c.cu;
+    if (++c.g == G) {
+        c.g = 0;
+        if (++c.b == R) {
+            c.b = 0;
+            ++c.tt;
+            c.cu = 0;
+        }
+    }
+}
+
+template <int NTOK, int MV>
 __global__ void __launch_bounds__(kUThreads, Cfg<NTOK>::kCtasPerSm)
 umma_kernel(const __grid_constant__ CUtensorMap xmap, const UmmaArgs a) {
+    // MV: token columns promoted per unit (1 when M == 1, else NTOK)
     using C = Cfg<NTOK>;
+    constexpr int AH = C::kAHalves;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base (swizzle atoms)
     const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -170,8 +212,9 @@ umma_kernel(const __grid_constant__ CUtensorMap xmap, const UmmaArgs a) {
     const uint32_t cbase = sbase + C::kOffCtrl;
     const uint32_t bar_full = cbase;                                  // [kStages]
     const uint32_t bar_empty = bar_full + 8 * C::kStages;             // [kStages]
-    const uint32_t bar_afull = bar_empty + 8 * C::kStages;            // [kNWG]
-    const uint32_t bar_dfull = bar_afull + 8 * kNWG;                  // [kNWG][kDBuf]
+    const uint32_t bar_afull = bar_empty + 8 * C::kStages;            // [kNWG][AH]
+    const uint32_t bar_aempty = bar_afull + 8 * kNWG * AH;            // [kNWG][AH]
+    const uint32_t bar_dfull = bar_aempty + 8 * kNWG * AH;            // [kNWG][kDBuf]
     const uint32_t bar_dempty = bar_dfull + 8 * kNWG * C::kDBuf;      // [kNWG][kDBuf]
     const uint32_t bar_drain = bar_dempty + 8 * kNWG * C::kDBuf;
     uint32_t* tmem_base_ptr = reinterpret_cast<uint32_t*>(ctrl + 512);
@@ -179,21 +222,18 @@ umma_kernel(const __grid_constant__ CUtensorMap xmap, const UmmaArgs a) {
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // workers of this CTA
-    int64_t w_u0[kNWG], w_n[kNWG];
-    int64_t max_n = 0;
+    // workers of this CTA: contiguous unit ranges
+    int64_t w_u0[kNWG];
+    int32_t w_n[kNWG];
+    int32_t max_n = 0;
 #pragma unroll
     for (int w = 0; w < kNWG; ++w) {
         const int64_t v = (int64_t)blockIdx.x * kNWG + w;
-        if (v < a.V) {
-            w_u0[w] = a.U * v / a.V;
-            w_n[w] = a.U * (v + 1) / a.V - w_u0[w];
-        } else {
-            w_u0[w] = 0;
-            w_n[w] = 0;
-        }
+        w_u0[w] = v < a.V ? a.U * v / a.V : 0;
+        w_n[w] = v < a.V ? static_cast<int32_t>(a.U * (v + 1) / a.V - w_u0[w]) : 0;
         max_n = w_n[w] > max_n ? w_n[w] : max_n;
     }
+    const int32_t R32 = static_cast<int32_t>(a.R), G32 = static_cast<int32_t>(a.G);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
@@ -201,7 +241,10 @@ umma_kernel(const __grid_constant__ CUtensorMap xmap, const UmmaArgs a) {
             mbar_init(bar_empty + 8 * s, 1);
         }
         for (int w = 0; w < kNWG; ++w) {
-            mbar_init(bar_afull + 8 * w, 4);
+            for (int q = 0; q < AH; ++q) {
+                mbar_init(bar_afull + 8 * (AH * w + q), 4);
+                mbar_init(bar_aempty + 8 * (AH * w + q), 1);
+            }
             for (int b = 0; b < C::kDBuf; ++b) {
                 mbar_init(bar_dfull + 8 * (w * C::kDBuf + b), 1);
                 mbar_init(bar_dempty + 8 * (w * C::kDBuf + b), 4);
@@ -225,71 +268,75 @@ umma_kernel(const __grid_constant__ CUtensorMap xmap, const UmmaArgs a) {
     if (warp == kProducerWarp) {
         // ------------------------------------------------------ producer
         if (lane == 0) {
-            const uint32_t xbytes = C::kXUnit;
-            int64_t issued = 0;
+            constexpr uint32_t kUnitBytes = kUnitCodeBytes + kUnitScaleBytes + C::kXUnit;
+            UnitCursor cw[kNWG], cx[kNWG];   // next unit for weights / for X
+#pragma unroll
+            for (int w = 0; w < kNWG; ++w) cw[w] = cx[w] = cursor_at(w_u0[w], a.R, a.G);
             bool ok = true;
-            // weights of the first stages do not depend on earlier kernels
-            const int64_t pre = max_n < C::kStages ? max_n : C::kStages;
-            for (int64_t f = 0; f < pre; ++f) {
-                const int s = static_cast<int>(f);
+            // the weights of the first stages do not depend on earlier kernels
+            const int32_t pre = max_n < C::kStages ? max_n : C::kStages;
+            for (int32_t f = 0; f < pre; ++f) {
+                const uint32_t st = sbase + f * C::kStageBytes;
                 uint32_t bytes = 0;
-                for (int w = 0; w < kNWG; ++w)
-                    if (f < w_n[w]) bytes += kUnitCodeBytes + kUnitScaleBytes + xbytes;
-                mbar_arrive_expect_tx(bar_full + 8 * s, bytes);
+#pragma unroll
+                for (int w = 0; w < kNWG; ++w) bytes += f < w_n[w] ? kUnitBytes : 0u;
+                mbar_arrive_expect_tx(bar_full + 8 * f, bytes);
+#pragma unroll
                 for (int w = 0; w < kNWG; ++w) {
                     if (f >= w_n[w]) continue;
-                    const int64_t u = w_u0[w] + f;
-                    const int64_t cu = u % (a.R * a.G);
-                    const uint32_t st = sbase + s * C::kStageBytes;
-                    bulk_load(st + C::kOffCodes + w * kUnitCodeBytes, a.codes + cu * kUnitCodeBytes,
-                              kUnitCodeBytes, bar_full + 8 * s);
-                    bulk_load(st + C::kOffScales + w * kUnitScaleBytes, a.scales + cu * kUnitScaleBytes,
-                              kUnitScaleBytes, bar_full + 8 * s);
+                    bulk_load(st + C::kOffCodes + w * kUnitCodeBytes,
+                              a.codes + (int64_t)cw[w].cu * kUnitCodeBytes, kUnitCodeBytes, bar_full + 8 * f);
+                    bulk_load(st + C::kOffScales + w * kUnitScaleBytes,
+                              a.scales + (int64_t)cw[w].cu * kUnitScaleBytes, kUnitScaleBytes, bar_full + 8 * f);
+                    cursor_next(cw[w], R32, G32);
                 }
-                issued = f + 1;
             }
             grid_dependency_wait();
-            for (int64_t f = 0; f < max_n && ok; ++f) {
-                const int s = static_cast<int>(f % C::kStages);
+            int s = 0;
+            uint32_t round = 0;   // completed passes over the ring
+            for (int32_t f = 0; f < max_n && ok; ++f) {
                 const uint32_t st = sbase + s * C::kStageBytes;
                 if (f >= pre) {
-                    if (!mbar_wait(bar_empty + 8 * s, static_cast<uint32_t>((f / C::kStages - 1) & 1), abort_flag)) {
+                    if (!mbar_wait(bar_empty + 8 * s, (round - 1) & 1u, abort_flag)) {
                         ok = false;
                         break;
                     }
                     uint32_t bytes = 0;
-                    for (int w = 0; w < kNWG; ++w)
-                        if (f < w_n[w]) bytes += kUnitCodeBytes + kUnitScaleBytes + xbytes;
+#pragma unroll
+                    for (int w = 0; w < kNWG; ++w) bytes += f < w_n[w] ? kUnitBytes : 0u;
                     mbar_arrive_expect_tx(bar_full + 8 * s, bytes);
+#pragma unroll
                     for (int w = 0; w < kNWG; ++w) {
                         if (f >= w_n[w]) continue;
-                        const int64_t u = w_u0[w] + f;
-                        const int64_t cu = u % (a.R * a.G);
-                        bulk_load(st + C::kOffCodes + w * kUnitCodeBytes, a.codes + cu * kUnitCodeBytes,
-                                  kUnitCodeBytes, bar_full + 8 * s);
+                        bulk_load(st + C::kOffCodes + w * kUnitCodeBytes,
+                                  a.codes + (int64_t)cw[w].cu * kUnitCodeBytes, kUnitCodeBytes, bar_full + 8 * s);
                         bulk_load(st + C::kOffScales + w * kUnitScaleBytes,
-                                  a.scales + cu * kUnitScaleBytes, kUnitScaleBytes, bar_full + 8 * s);
+                                  a.scales + (int64_t)cw[w].cu * kUnitScaleBytes, kUnitScaleBytes,
+                                  bar_full + 8 * s);
+                        cursor_next(cw[w], R32, G32);
                     }
-                    issued = f + 1;
                 }
+#pragma unroll
                 for (int w = 0; w < kNWG; ++w) {
                     if (f >= w_n[w]) continue;
-                    const int64_t u = w_u0[w] + f;
-                    const int64_t tt = u / (a.R * a.G);
-                    const int64_t g = u % a.G;
                     const uint32_t xs = st + w * C::kXUnit;
-                    const int32_t row = static_cast<int32_t>(tt * NTOK);
-                    tma_load_2d(xs, &xmap, static_cast<int32_t>(g * kGroup), row, bar_full + 8 * s);
-                    tma_load_2d(xs + C::kXBox, &xmap, static_cast<int32_t>(g * kGroup + 64), row,
-                                bar_full + 8 * s);
+                    const int32_t k0 = cx[w].g * kGroup, row = cx[w].tt * NTOK;
+                    tma_load_2d(xs, &xmap, k0, row, bar_full + 8 * s);
+                    tma_load_2d(xs + C::kXBox, &xmap, k0 + 64, row, bar_full + 8 * s);
+                    cursor_next(cx[w], R32, G32);
+                }
+                if (++s == C::kStages) {
+                    s = 0;
+                    ++round;
                 }
             }
             if (*abort_flag) {
-                // drain the copies this CTA still has in flight (bounded)
+                // drain the copies this CTA may still have in flight (bounded)
                 volatile int no_abort = 0;
-                for (int64_t f = issued - C::kStages < 0 ? 0 : issued - C::kStages; f < issued; ++f)
-                    (void)mbar_wait(bar_full + 8 * static_cast<int>(f % C::kStages),
-                                    static_cast<uint32_t>((f / C::kStages) & 1), &no_abort);
+                for (int t = 0; t < C::kStages; ++t) {
+                    (void)mbar_wait(bar_full + 8 * t, 0, &no_abort);
+                    (void)mbar_wait(bar_full + 8 * t, 1, &no_abort);
+                }
             }
         }
     } else if (warp == kMmaWarp) {
@@ -298,39 +345,57 @@ umma_kernel(const __grid_constant__ CUtensorMap xmap, const UmmaArgs a) {
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(128, NTOK);
             bool ok = true;
-            for (int64_t f = 0; f < max_n && ok; ++f) {
-                const int s = static_cast<int>(f % C::kStages);
+            int s = 0;
+            uint32_t full_ph = 0;
+            int abuf[kNWG];          // next A half-buffer per worker
+            uint32_t around[kNWG];   // its completion parity
+#pragma unroll
+            for (int w = 0; w < kNWG; ++w) { abuf[w] = 0; around[w] = 0; }
+            for (int32_t f = 0; f < max_n && ok; ++f) {
                 const uint32_t st = sbase + s * C::kStageBytes;
-                if (!mbar_wait(bar_full + 8 * s, static_cast<uint32_t>((f / C::kStages) & 1), abort_flag)) {
+                if (!mbar_wait(bar_full + 8 * s, full_ph, abort_flag)) {
                     ok = false;
                     break;
                 }
-                for (int w = 0; w < kNWG && ok; ++w) {
-                    if (f >= w_n[w]) continue;
-                    const int db = static_cast<int>(f % C::kDBuf);
-                    if (!mbar_wait(bar_afull + 8 * w, static_cast<uint32_t>(f & 1), abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    if (f >= C::kDBuf &&
-                        !mbar_wait(bar_dempty + 8 * (w * C::kDBuf + db),
-                                   static_cast<uint32_t>((f / C::kDBuf - 1) & 1), abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after_sync();
-                    const uint32_t a_tm = tmem + w * kACols;
-                    const uint32_t d_tm = tmem + kNWG * kACols + (w * C::kDBuf + db) * NTOK;
-                    const uint32_t xs = st + w * C::kXUnit;
+                const int db = C::kDBuf == 2 ? (f & 1) : 0;
+                const uint32_t dempty_ph = C::kDBuf == 2 ? (((f >> 1) & 1) ^ 1u) : ((f & 1) ^ 1u);
+                // half h of every worker, then the next half: each half's four
+                // MMAs start as soon as its decoded A is in tensor memory
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const uint64_t bdesc =
-                            smem_desc_kmajor_sw128(xs + (j >> 2) * C::kXBox + 32 * (j & 3));
-                        umma_bf16_tmem_a(d_tm, a_tm + 8 * j, bdesc, idesc, j > 0 ? 1u : 0u);
+                for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                    for (int w = 0; w < kNWG; ++w) {
+                        if (!ok || f >= w_n[w]) continue;
+                        const int q = abuf[w];
+                        if (!mbar_wait(bar_afull + 8 * (AH * w + q), around[w], abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        if (h == 0 && f >= C::kDBuf &&
+                            !mbar_wait(bar_dempty + 8 * (w * C::kDBuf + db), dempty_ph, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after_sync();
+                        const uint32_t a_tm = tmem + w * C::kAColsW + 32 * q;
+                        const uint32_t d_tm = tmem + kNWG * C::kAColsW + (w * C::kDBuf + db) * NTOK;
+                        const uint64_t bdesc0 = smem_desc_kmajor_sw128(st + w * C::kXUnit + h * C::kXBox);
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj)   // +32 bytes per K-step = +2 in the address field
+                            umma_bf16_tmem_a(d_tm, a_tm + 8 * jj, bdesc0 + 2 * jj, idesc, (h | jj) != 0 ? 1u : 0u);
+                        umma_commit(bar_aempty + 8 * (AH * w + q));
+                        if (h == 1) umma_commit(bar_dfull + 8 * (w * C::kDBuf + db));
+                        if (++abuf[w] == AH) {
+                            abuf[w] = 0;
+                            around[w] ^= 1u;
+                        }
                     }
-                    umma_commit(bar_dfull + 8 * (w * C::kDBuf + db));
                 }
                 if (ok) umma_commit(bar_empty + 8 * s);
+                if (++s == C::kStages) {
+                    s = 0;
+                    full_ph ^= 1u;
+                }
             }
             // every MMA issued has completed before tensor memory is freed
             umma_commit(bar_drain);
@@ -343,98 +408,120 @@ umma_kernel(const __grid_constant__ CUtensorMap xmap, const UmmaArgs a) {
         const int wg = warp >> 2;
         const int r = threadIdx.x & 127;               // weight row in the tile = TMEM lane
         const int64_t v = (int64_t)blockIdx.x * kNWG + wg;
-        const int64_t u0 = v < a.V ? a.U * v / a.V : 0;
-        const int64_t n = v < a.V ? a.U * (v + 1) / a.V - u0 : 0;
+        const int32_t n = w_n[wg == 0 ? 0 : 1];
+        const int64_t u0 = w_u0[wg == 0 ? 0 : 1];
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t a_tm = tmem + lane_off + wg * kACols;
-        const int64_t RG = a.R * a.G;
+        const uint32_t a_tm0 = tmem + lane_off + wg * C::kAColsW;
+        const uint32_t d_tm0 = tmem + lane_off + kNWG * C::kAColsW + wg * C::kDBuf * NTOK;
+        const uint32_t bar_afull_w = bar_afull + 8 * AH * wg;
+        const uint32_t bar_aempty_w = bar_aempty + 8 * AH * wg;
         if (n > 0) {
-            const int64_t first_tile = u0 / a.G;
-            int64_t tile_cur = first_tile;
-            bool whole = (u0 % a.G) == 0;
+            UnitCursor cur = cursor_at(u0, a.R, a.G);    // unit j
+            UnitCursor prev = cur;                        // unit j - 1
+            const int64_t first_tile = (int64_t)cur.tt * a.R + cur.b;
+            bool whole = cur.g == 0;
             float acc[NTOK];
 #pragma unroll
             for (int m = 0; m < NTOK; ++m) acc[m] = 0.f;
             float s_prev = 0.f;
-            int mvalid = 0;
             bool ok = true;
-            for (int64_t j = 0; j <= n && ok; ++j) {
-                // decode unit j (if any) into A
+            int s = 0;
+            uint32_t full_ph = 0;
+            int q = 0;               // next A half-buffer
+            uint32_t qround = 0;     // completions of that buffer so far (parity)
+            int32_t halves = 0;      // half-units decoded so far
+            const uint8_t* codes_base = smem + C::kOffCodes + wg * kUnitCodeBytes + 16 * r;
+            const uint8_t* scale_base = smem + C::kOffScales + wg * kUnitScaleBytes + 2 * r;
+            for (int32_t j = 0; j <= n && ok; ++j) {
                 float s_cur = 0.f;
                 if (j < n) {
-                    const int s = static_cast<int>(j % C::kStages);
-                    const uint8_t* st = smem + s * C::kStageBytes;
-                    if (!warp_wait(bar_full + 8 * s, static_cast<uint32_t>((j / C::kStages) & 1), abort_flag)) {
+                    // ---- decode unit j into two A half-buffers
+                    if (!warp_wait(bar_full + 8 * s, full_ph, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    const uint4 c0 = lds_v4(st + C::kOffCodes + wg * kUnitCodeBytes + 16 * r);
-                    const uint4 c1 = lds_v4(st + C::kOffCodes + wg * kUnitCodeBytes + 2048 + 16 * r);
-                    s_cur = fp16_bits_to_float(
-                        *reinterpret_cast<const uint16_t*>(st + C::kOffScales + wg * kUnitScaleBytes + 2 * r));
-                    if (j >= 1) {
-                        // MMA of unit j-1 complete: A is free and its partial is ready
-                        const int db = static_cast<int>((j - 1) % C::kDBuf);
-                        if (!warp_wait(bar_dfull + 8 * (wg * C::kDBuf + db),
-                                       static_cast<uint32_t>(((j - 1) / C::kDBuf) & 1), abort_flag)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after_sync();
+                    const uint4 c0 = lds_v4(codes_base + s * C::kStageBytes);
+                    const uint4 c1 = lds_v4(codes_base + s * C::kStageBytes + 2048);
+                    s_cur = fp16_bits_to_float(*reinterpret_cast<const uint16_t*>(scale_base + s * C::kStageBytes));
+                    if (++s == C::kStages) {
+                        s = 0;
+                        full_ph ^= 1u;
                     }
                     const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        uint32_t pairs[8];
-                        decode_word(words[q], pairs);
-                        tmem_st_32x32b_x8(a_tm + 8 * q, pairs);
+                    for (int h = 0; h < 2; ++h) {
+                        if (halves >= AH) {
+                            // the MMAs that last read this buffer have completed
+                            if (!warp_wait(bar_aempty_w + 8 * q, qround ^ 1u, abort_flag)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after_sync();
+                        }
+                        const uint32_t a_tm = a_tm0 + 32 * q;
+#pragma unroll
+                        for (int w4 = 0; w4 < 4; ++w4) {
+                            uint32_t pairs[8];
+                            decode_word(words[4 * h + w4], pairs);
+                            tmem_st_32x32b_x8(a_tm + 8 * w4, pairs);
+                        }
+                        tmem_st_wait();
+                        tc_fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar_afull_w + 8 * q);
+                        ++halves;
+                        if (++q == AH) {
+                            q = 0;
+                            qround ^= 1u;
+                        }
                     }
-                    tmem_st_wait();
-                    tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar_afull + 8 * wg);
-                } else {
-                    // final unit's partial
-                    const int db = static_cast<int>((j - 1) % C::kDBuf);
-                    if (!warp_wait(bar_dfull + 8 * (wg * C::kDBuf + db),
-                                   static_cast<uint32_t>(((j - 1) / C::kDBuf) & 1), abort_flag)) {
+                    if (!ok) break;
+                }
+                if (j >= 1) {
+                    // ---- promote unit j-1: acc += s * group partial
+                    const int jp = j - 1;
+                    const int db = C::kDBuf == 2 ? (jp & 1) : 0;
+                    const uint32_t dfull_ph = C::kDBuf == 2 ? ((jp >> 1) & 1) : (jp & 1);
+                    if (!warp_wait(bar_dfull + 8 * (wg * C::kDBuf + db), dfull_ph, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
-                }
-                if (j >= 1) {
-                    // promote unit j-1: acc += s * partial
-                    const int64_t up = u0 + j - 1;
-                    const int64_t tt = up / RG;
-                    mvalid = static_cast<int>((a.M - tt * NTOK) < NTOK ? (a.M - tt * NTOK) : NTOK);
-                    const int db = static_cast<int>((j - 1) % C::kDBuf);
-                    const uint32_t d_tm = tmem + lane_off + kNWG * kACols + (wg * C::kDBuf + db) * NTOK;
-#pragma unroll
-                    for (int c = 0; c < NTOK; c += 16) {
-                        uint32_t d[16];
-                        tmem_ld_32x32b_x16(d_tm + c, d);
+                    const uint32_t d_tm = d_tm0 + db * NTOK;
+                    if (MV == 1) {
+                        uint32_t d0;
+                        tmem_ld_32x32b_x1(d_tm, d0);
                         tmem_ld_wait();
+                        acc[0] = fmaf(s_prev, __uint_as_float(d0), acc[0]);
+                    } else {
 #pragma unroll
-                        for (int m = 0; m < 16; ++m) acc[c + m] = fmaf(s_prev, __uint_as_float(d[m]), acc[c + m]);
+                        for (int c = 0; c < NTOK; c += 16) {
+                            uint32_t d[16];
+                            tmem_ld_32x32b_x16(d_tm + c, d);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int m = 0; m < 16; ++m) acc[c + m] = fmaf(s_prev, __uint_as_float(d[m]), acc[c + m]);
+                        }
                     }
                     tc_fence_before_sync();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar_dempty + 8 * (wg * C::kDBuf + db));
-                    // tile finished?
-                    const int64_t tile_next = (j < n) ? (u0 + j) / a.G : -1;
-                    if (tile_next != tile_cur) {
-                        const bool whole_tile = whole && ((up % a.G) == a.G - 1);
-                        flush_tile<NTOK>(a, v, tile_cur, first_tile, whole_tile, acc, mvalid, r);
+                    // tile finished (next unit in another tile, or no next unit)?
+                    const bool tile_end = (j == n) || cur.b != prev.b || cur.tt != prev.tt;
+                    if (tile_end) {
+                        const int64_t tile_id = (int64_t)prev.tt * a.R + prev.b;
+                        const int mvalid =
+                            MV == 1 ? 1 : ((a.M - prev.tt * NTOK) < NTOK ? (a.M - prev.tt * NTOK) : NTOK);
+                        flush_tile<NTOK>(a, v, tile_id, first_tile, whole && prev.g == G32 - 1, acc, mvalid, r);
 #pragma unroll
                         for (int m = 0; m < NTOK; ++m) acc[m] = 0.f;
-                        tile_cur = tile_next;
                         whole = true;
                     }
                 }
                 s_prev = s_cur;
+                prev = cur;
+                if (j < n) cursor_next(cur, R32, G32);
             }
-            (void)mvalid;
         }
     }
 
@@ -469,7 +556,7 @@ EncodeTiledFn encode_tiled_fn() {
     return fn;
 }
 
-template <int NTOK>
+template <int NTOK, int MV>
 cudaError_t launch_ntok(const uint16_t* X, int64_t ldx, const UmmaArgs& a, const UmmaPlan& plan,
                         cudaStream_t stream) {
     using C = Cfg<NTOK>;
@@ -486,7 +573,7 @@ cudaError_t launch_ntok(const uint16_t* X, int64_t ldx, const UmmaArgs& a, const
             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
 
-    cudaError_t e = cudaFuncSetAttribute(umma_kernel<NTOK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(umma_kernel<NTOK, MV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -499,7 +586,7 @@ cudaError_t launch_ntok(const uint16_t* X, int64_t ldx, const UmmaArgs& a, const
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, umma_kernel<NTOK>, map, a);
+    return cudaLaunchKernelEx(&cfg, umma_kernel<NTOK, MV>, map, a);
 }
 
 template <int NTOK>
@@ -554,10 +641,12 @@ cudaError_t launch_umma(const uint16_t* X, int64_t ldx, const uint8_t* tiled, in
     a.slots = reinterpret_cast<float*>(w + kWorkspaceErr +
                                        (size_t)ceil_div(plan.token_tiles * plan.R * 4 * 4, 256) * 256);
     switch (plan.ntok) {
-        case 16: return launch_ntok<16>(X, ldx, a, plan, stream);
-        case 32: return launch_ntok<32>(X, ldx, a, plan, stream);
-        case 64: return launch_ntok<64>(X, ldx, a, plan, stream);
-        default: return launch_ntok<128>(X, ldx, a, plan, stream);
+        case 16:
+            return M == 1 ? launch_ntok<16, 1>(X, ldx, a, plan, stream)
+                          : launch_ntok<16, 16>(X, ldx, a, plan, stream);
+        case 32: return launch_ntok<32, 32>(X, ldx, a, plan, stream);
+        case 64: return launch_ntok<64, 64>(X, ldx, a, plan, stream);
+        default: return launch_ntok<128, 128>(X, ldx, a, plan, stream);
     }
 }
 
