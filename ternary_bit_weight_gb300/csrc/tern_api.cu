@@ -23,13 +23,26 @@ tern_status run_linear(const uint16_t* X, int64_t ldx, const void* tiled, int64_
                        cudaStream_t stream) {
     const int sms = tern::device_sm_count();
     if (sms <= 0) return TERN_ERR_UNSUPPORTED;
-    const tern::UmmaPlan plan = tern::plan_umma(M, N, K, sms);
     if (ws == nullptr) return TERN_ERR_NULL;
-    if (ws_bytes < plan.ws_bytes) return TERN_ERR_SIZE;
     if (!aligned(ws, 256)) return TERN_ERR_ALIGN;
-    const cudaError_t e = tern::launch_umma(X, ldx, static_cast<const uint8_t*>(tiled), M, N, K, out,
-                                            ws, plan, stream);
+    const uint8_t* w = static_cast<const uint8_t*>(tiled);
+    cudaError_t e;
+    if (M <= tern::kStreamMaxM) {
+        const tern::StreamPlan plan = tern::plan_stream(M, N, K, sms);
+        if (ws_bytes < plan.ws_bytes) return TERN_ERR_SIZE;
+        e = tern::launch_stream(X, ldx, w, M, N, K, out, ws, plan, stream);
+    } else {
+        const tern::UmmaPlan plan = tern::plan_umma(M, N, K, sms);
+        if (ws_bytes < plan.ws_bytes) return TERN_ERR_SIZE;
+        e = tern::launch_umma(X, ldx, w, M, N, K, out, ws, plan, stream);
+    }
     return e == cudaSuccess ? TERN_OK : TERN_ERR_CUDA;
+}
+
+size_t workspace_bytes(int64_t M, int64_t N, int64_t K) {
+    const int sms = tern::device_sm_count();
+    if (M <= tern::kStreamMaxM) return tern::plan_stream(M, N, K, sms).ws_bytes;
+    return tern::plan_umma(M, N, K, sms).ws_bytes;
 }
 
 tern_status check_x_w(const uint16_t* X, int64_t ldx, const void* tiled, int64_t M, int64_t K) {
@@ -42,6 +55,17 @@ tern_status check_x_w(const uint16_t* X, int64_t ldx, const void* tiled, int64_t
 }
 
 }  // namespace
+
+namespace tern {
+
+int device_sm_count() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return sms;
+}
+
+}  // namespace tern
 
 extern "C" {
 
@@ -109,7 +133,7 @@ tern_status tern_unrepack(const void* d_tiled, int64_t N, int64_t K, uint8_t* d_
 
 size_t tern_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     if (M <= 0 || !valid_group_shape(N, K) || N == 0) return 0;
-    return tern::plan_umma(M, N, K, tern::device_sm_count()).ws_bytes;
+    return workspace_bytes(M, N, K);
 }
 
 tern_status tern_linear(const uint16_t* d_X, int64_t ldx, const void* d_tiled, int64_t M, int64_t N,

@@ -21,42 +21,44 @@ cudaError_t launch_unrepack(const uint8_t* tiled, int64_t N, int64_t K, uint8_t*
 // ---------------------------------------------------------- linear layer
 constexpr int kMaxOutputs = 4;
 
+// Where the rows of the concatenated N go: rows [offset[j], offset[j+1])
+// to output j, element (m, n) at y[j][m * ldy[j] + n - offset[j]], stored as
+// fp32 or (bf16 != 0) as bf16 rounded to nearest even.
 struct OutputSplit {
     int n_out;
-    int64_t offset[kMaxOutputs + 1];  // row offsets into the concatenated N
-    float* y[kMaxOutputs];
+    int bf16;
+    int64_t offset[kMaxOutputs + 1];
+    void* y[kMaxOutputs];
     int64_t ldy[kMaxOutputs];
 };
 
-// Decode (small-M) plan.  kStream: persistent CTAs, X resident in shared
-// memory, each warp streams a contiguous run of 16x128 blocks.  kSplit: one
-// CTA per (128-row block, K range), X slice per CTA.
-struct DecodePlan {
-    enum Kind { kStream = 0, kSplit = 1 };
-    Kind kind;
-    int mt;            // n8 token tiles per MMA row tile (1: M<=8, 2: M<=16)
-    int splits;        // S (kSplit)
-    int64_t n_rb;      // 128-row blocks
-    int64_t groups;    // K / 128
-    int64_t max_gps;   // largest number of groups in one split
-    int64_t grid;      // CTAs
-    int64_t warps;     // working warps
-    size_t smem;       // dynamic shared memory per CTA
-    size_t ws_bytes;   // workspace: counters + partials
+int device_sm_count();
+
+// Largest M served by the streaming (decode) kernel; larger M goes to the
+// tensor-core GEMM kernel.
+constexpr int64_t kStreamMaxM = 16;
+
+// Streaming kernel plan (M <= 16): persistent CTAs, one per SM, whose
+// decode workers each own a contiguous range of 128x128 weight units.
+struct StreamPlan {
+    bool one;              // M == 1: X resident in shared memory
+    int64_t R;             // 128-row tiles
+    int64_t G;             // groups per row (K / 128)
+    int64_t U;             // units = R x G
+    int64_t V;             // workers
+    int64_t grid;          // CTAs
+    int stages;            // shared-memory ring depth
+    size_t smem;           // dynamic shared memory per CTA
+    size_t ws_bytes;       // workspace: error word, tile counters, partial slots
 };
 
-int device_sm_count();
-DecodePlan plan_decode(int64_t M, int64_t N, int64_t K, int sm_count);
+StreamPlan plan_stream(int64_t M, int64_t N, int64_t K, int sm_count);
 
-// Largest M the decode kernel handles in one launch.
-constexpr int64_t kDecodeMaxM = 16;
+cudaError_t launch_stream(const uint16_t* X, int64_t ldx, const uint8_t* tiled, int64_t M, int64_t N,
+                          int64_t K, const OutputSplit& out, void* ws, const StreamPlan& plan,
+                          cudaStream_t stream);
 
-cudaError_t launch_decode(const uint16_t* X, int64_t ldx, const uint8_t* tiled, int64_t M,
-                          int64_t N, int64_t K, const OutputSplit& out, void* ws,
-                          const DecodePlan& plan, cudaStream_t stream);
-
-// Tensor-core (tcgen05) plan: token tiles of `ntok`, persistent CTAs whose
-// decode warpgroups each stream a contiguous range of 128x128 units.
+// Tensor-core (tcgen05) plan for M > kStreamMaxM.
 struct UmmaPlan {
     int ntok;              // tokens per tile (UMMA N): 16, 32, 64 or 128
     int64_t R;             // 128-row tiles
@@ -74,5 +76,8 @@ UmmaPlan plan_umma(int64_t M, int64_t N, int64_t K, int sm_count);
 cudaError_t launch_umma(const uint16_t* X, int64_t ldx, const uint8_t* tiled, int64_t M, int64_t N,
                         int64_t K, const OutputSplit& out, void* ws, const UmmaPlan& plan,
                         cudaStream_t stream);
+
+// Size of the error word + padding at the start of every linear workspace.
+constexpr size_t kWorkspaceErrBytes = 256;
 
 }  // namespace tern

@@ -1,6 +1,9 @@
 // Byte-format kernels of libtern: pack, unpack, repack (disk -> tiled) and
 // unrepack (tiled -> disk).  All are memory-bound single passes, one thread
-// per 32-bit output word, and bit-exact by construction.
+// per 32-bit output word, and bit-exact by construction.  Every thread
+// fences its writes before exiting, so that a following linear-layer kernel
+// that starts early (programmatic dependent launch) and streams weights
+// before its grid dependency resolves sees them.
 //
 // Packing rule ("Ternary embedding model in vLLM", 2kiu.com/news/5082861,
 // §3.1): 2-bit codes 00 -> 0, 01 -> +1, 10 -> -1, 11 -> reserved read as 0;
@@ -43,6 +46,7 @@ pack_words_kernel(const uint4* __restrict__ t, int64_t words, uint32_t* __restri
             out |= code_of(static_cast<int8_t>(part[j >> 2] >> (8 * (j & 3))), bad) << (2 * j);
         packed[i] = out;
     }
+    __threadfence();   // writes visible GPU-wide before exit (early-starting successors)
     count_errors(err, bad);
 }
 
@@ -58,6 +62,7 @@ pack_bytes_kernel(const int8_t* __restrict__ t, int64_t first_byte, int64_t byte
         for (int j = 0; j < 4; ++j) out |= code_of(t[4 * i + j], bad) << (2 * j);
         packed[i] = static_cast<uint8_t>(out);
     }
+    __threadfence();   // writes visible GPU-wide before exit (early-starting successors)
     count_errors(err, bad);
 }
 
@@ -80,6 +85,7 @@ unpack_words_kernel(const uint32_t* __restrict__ packed, int64_t words, uint4* _
             part[j >> 2] |= (uint32_t)(uint8_t)value_of((w >> (2 * j)) & 3u) << (8 * (j & 3));
         t[i] = make_uint4(part[0], part[1], part[2], part[3]);
     }
+    __threadfence();   // writes visible GPU-wide before exit (early-starting successors)
     count_errors(err, bad);
 }
 
@@ -97,6 +103,7 @@ unpack_bytes_kernel(const uint8_t* __restrict__ packed, int64_t first_byte, int6
             t[4 * i + j] = value_of(c);
         }
     }
+    __threadfence();   // writes visible GPU-wide before exit (early-starting successors)
     count_errors(err, bad);
 }
 
@@ -176,6 +183,7 @@ repack_kernel(const uint8_t* __restrict__ packed, const uint16_t* __restrict__ s
             tiled[i] = s_lo | (s_hi << 16);
         }
     }
+    __threadfence();   // writes visible GPU-wide before exit (early-starting successors)
     count_errors(err, bad);
 }
 
@@ -202,6 +210,7 @@ unrepack_kernel(const uint32_t* __restrict__ tiled, int64_t N, int64_t K, int64_
             if (n_lo + 1 < N) scales[(n_lo + 1) * G + g] = static_cast<uint16_t>(w >> 16);
         }
     }
+    __threadfence();   // writes visible GPU-wide before exit (early-starting successors)
     count_errors(err, bad);
 }
 

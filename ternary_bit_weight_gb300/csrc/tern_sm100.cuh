@@ -43,7 +43,7 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 // Test the phase with the given parity; if it is not complete the thread
 // is suspended until it completes or about kSuspendHintNs elapse (it does
 // not spin, so waiting warps leave the issue slots to working warps).
-constexpr uint32_t kSuspendHintNs = 200000;
+constexpr uint32_t kSuspendHintNs = 100000;
 
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t done;
@@ -72,18 +72,25 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 
 // Wait for the phase with the given parity to complete.  Gives up (returns
 // false) when *abort becomes non-zero or after kWaitTimeoutNs of waiting, in
-// which case it sets *abort so that every other waiter gives up too.
+// which case it sets *abort so that every other waiter gives up too.  The
+// flag and the clock are read only every 16 suspended tries, so a wait that
+// completes quickly costs a test and a few tries.
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;   // 2 s
 
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
     if (mbar_test_wait(bar, parity)) return true;   // common case: already complete
-    const uint64_t t0 = global_timer_ns();
-    for (;;) {
+    uint64_t t0 = 0;
+    for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (*abort) return false;
-        if (global_timer_ns() - t0 > kWaitTimeoutNs) {
-            *abort = 1;
-            return false;
+        if ((i & 15u) == 0) {
+            if (*abort) return false;
+            const uint64_t t = global_timer_ns();
+            if (t0 == 0) {
+                t0 = t;
+            } else if (t - t0 > kWaitTimeoutNs) {
+                *abort = 1;
+                return false;
+            }
         }
     }
 }
@@ -158,6 +165,19 @@ __device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t
         : "memory");
 }
 
+// Each thread of the warp writes 32 consecutive 32-bit columns of its lane.
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t* v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),
+        "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),
+        "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -165,6 +185,14 @@ __device__ __forceinline__ void tmem_st_wait() {
 // Each thread of the warp reads one 32-bit column of its lane.
 __device__ __forceinline__ void tmem_ld_32x32b_x1(uint32_t taddr, uint32_t& v) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(v) : "r"(taddr) : "memory");
+}
+
+// Each thread of the warp reads 4 consecutive 32-bit columns of its lane.
+__device__ __forceinline__ void tmem_ld_32x32b_x4(uint32_t taddr, uint32_t (&v)[4]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+                 : "r"(taddr)
+                 : "memory");
 }
 
 // Each thread of the warp reads 16 consecutive 32-bit columns of its lane.
@@ -201,14 +229,31 @@ __device__ __forceinline__ uint64_t smem_desc_kmajor_sw128(uint32_t saddr) {
     return d;
 }
 
-// Instruction descriptor for kind::f16: fp32 D (bits 4-5 = 1), bf16 A
-// (bits 7-9 = 1) and B (bits 10-12 = 1), both K-major (bits 15, 16 = 0),
-// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+// Shared-memory matrix descriptor without swizzle (K-major "interleaved"
+// layout): core matrices of 8 rows x 16 bytes, each row 16 bytes after the
+// previous one; lbo = byte distance between core matrices adjacent along K,
+// sbo = between core matrices adjacent along M/N.  16-byte aligned start.
+__device__ __forceinline__ uint64_t smem_desc_kmajor_noswz(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    return d;
+}
+
+// Instruction descriptor for kind::f16: fp32 D (bits 4-5 = 1), A and B
+// types in bits 7-9 and 10-12 (0 = fp16, 1 = bf16), both K-major (bits 15,
+// 16 = 0), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
-// D[tmem] (+)= A[tmem] . B[smem]^T, one CTA, kind::f16 (bf16 inputs).
+__host__ __device__ constexpr uint32_t idesc_fp16_f32(uint32_t M, uint32_t N) {
+    return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[tmem] . B[smem]^T, one CTA, kind::f16 (fp16 or bf16 inputs).
 __device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                                  uint32_t idesc, uint32_t accumulate) {
     asm volatile(

@@ -46,7 +46,6 @@ constexpr int kDecWarps = 4 * kNWG;
 constexpr int kProducerWarp = kDecWarps;
 constexpr int kMmaWarp = kDecWarps + 1;
 constexpr int kUThreads = (kDecWarps + 2) * 32;
-constexpr int kWorkspaceErr = 256;               // error word + padding at the workspace start
 
 template <int NTOK>
 struct Cfg {
@@ -85,13 +84,6 @@ struct UmmaArgs {
     int* counters;           // [token tiles x R][4 row quarters]
     float* slots;            // [2V][NTOK][128] (column-major per slot)
 };
-
-__device__ __forceinline__ void store_y(const OutputSplit& out, int m, int64_t n, float v) {
-    int j = 0;
-#pragma unroll
-    for (int i = 1; i < kMaxOutputs; ++i) j += (i < out.n_out && n >= out.offset[i]);
-    out.y[j][(int64_t)m * out.ldy[j] + (n - out.offset[j])] = v;
-}
 
 __device__ __forceinline__ int64_t owner_worker(int64_t u, int64_t U, int64_t V) {
     return ((u + 1) * V - 1) / U;
@@ -462,7 +454,7 @@ umma_kernel(const __grid_constant__ CUtensorMap xmap, const UmmaArgs a) {
 #pragma unroll
                         for (int w4 = 0; w4 < 4; ++w4) {
                             uint32_t pairs[8];
-                            decode_word(words[4 * h + w4], pairs);
+                            decode_word_bf16(words[4 * h + w4], pairs);
                             tmem_st_32x32b_x8(a_tm + 8 * w4, pairs);
                         }
                         tmem_st_wait();
@@ -603,7 +595,7 @@ void fill_plan(UmmaPlan& p, int64_t M, int64_t N, int64_t K, int sms) {
     p.grid = ceil_div(workers, kNWG);
     p.smem = C::kSmemBytes;
     const size_t counters = (size_t)ceil_div(p.token_tiles * p.R * 4 * 4, 256) * 256;
-    p.ws_bytes = kWorkspaceErr + counters + (size_t)2 * p.V * kTileRows * NTOK * sizeof(float);
+    p.ws_bytes = kWorkspaceErrBytes + counters + (size_t)2 * p.V * kTileRows * NTOK * sizeof(float);
 }
 
 }  // namespace
@@ -637,8 +629,8 @@ cudaError_t launch_umma(const uint16_t* X, int64_t ldx, const uint8_t* tiled, in
     a.out = out;
     uint8_t* w = static_cast<uint8_t*>(ws);
     a.err = reinterpret_cast<int*>(w);
-    a.counters = reinterpret_cast<int*>(w + kWorkspaceErr);
-    a.slots = reinterpret_cast<float*>(w + kWorkspaceErr +
+    a.counters = reinterpret_cast<int*>(w + kWorkspaceErrBytes);
+    a.slots = reinterpret_cast<float*>(w + kWorkspaceErrBytes +
                                        (size_t)ceil_div(plan.token_tiles * plan.R * 4 * 4, 256) * 256);
     switch (plan.ntok) {
         case 16:

@@ -44,14 +44,32 @@ def workspace(M: int, N: int, K: int) -> torch.Tensor | None:
     return torch.zeros(nbytes, dtype=torch.uint8, device=DEV)
 
 
-def gpu_linear(x_np: np.ndarray, tiled: torch.Tensor, N: int, K: int, ws=None) -> torch.Tensor:
+def gpu_linear(x_np: np.ndarray, tiled: torch.Tensor, N: int, K: int, ws=None, ldx: int | None = None) -> torch.Tensor:
+    """tern_linear on host activations; with ldx > K the rows of X are laid
+    out with that stride (the extra columns hold NaN, which must never be read)."""
     M = x_np.shape[0]
-    X = dev(x_np.view(np.int16))
+    if ldx is None or ldx == K:
+        X = dev(x_np.view(np.int16))
+        ldx = K
+    else:
+        X = torch.full((M, ldx), 0x7FC0, dtype=torch.int16, device=DEV)   # bf16 NaN
+        X[:, :K] = dev(x_np.view(np.int16))
     Y = torch.full((M, N), float("nan"), dtype=torch.float32, device=DEV)
     if ws is None:
         ws = workspace(M, N, K)
-    tb.tern_linear(X, K, tiled, M, N, K, Y, N, ws)
+    tb.tern_linear(X, ldx, tiled, M, N, K, Y, N, ws)
     return Y
+
+
+def gpu_linear_multi(x_np: np.ndarray, tiled: torch.Tensor, splits, K: int, pad: int = 3):
+    """tern_linear_multi with one fp32 output per split (row stride n + pad,
+    padding columns NaN); returns the outputs as host arrays [M, n + pad]."""
+    M = x_np.shape[0]
+    N = int(sum(splits))
+    Ys = [torch.full((M, n + pad), float("nan"), device=DEV) for n in splits]
+    tb.tern_linear_multi(dev(x_np.view(np.int16)), K, tiled, M, K, list(splits), Ys,
+                         [n + pad for n in splits], workspace(M, N, K))
+    return [host(Y) for Y in Ys]
 
 
 def assert_within_bound(y_gpu: np.ndarray, y_ref: np.ndarray, bound: np.ndarray, what=""):

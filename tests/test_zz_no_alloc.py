@@ -39,12 +39,13 @@ def test_noalloc_matches_workspace_entry_point_twice(name, M):
     tiled = tiled_from_ternary(t, s)
     X = dev(x.view(np.int16))
     # the existing entry point with a caller-owned workspace
-    Y_ref = torch.full((M, N), float("nan"), device=DEV)
-    tb.tern_linear(X, K, tiled, M, N, K, Y_ref, N, workspace(M, N, K))
-    # the tests' tolerance: |y - y_ref| <= 1e-4 * sum_k |x w| (bound from the oracle)
+    Y_ws = torch.full((M, N), float("nan"), device=DEV)
+    tb.tern_linear(X, K, tiled, M, N, K, Y_ws, N, workspace(M, N, K))
+    # both are held to the tests' tolerance against the fp64 oracle:
+    # |y - y_ref| <= 1e-4 * sum_k |x w| per output
     packed, _ = oracle.pack(t)
-    _, bound = oracle.linear(x, packed, s, K)
-    y_ref = host(Y_ref).astype(np.float64)
+    y_ref, bound = oracle.linear(x, packed, s, K)
+    assert_within_bound(host(Y_ws), y_ref, bound, f"tern_linear {name} M={M}")
     for call in range(2):   # two calls in a row share the same scratch
         Y = torch.full((M, N), float("nan"), device=DEV)
         tb.tern_linear_noalloc(X, K, tiled, M, N, K, Y, N)
@@ -52,6 +53,8 @@ def test_noalloc_matches_workspace_entry_point_twice(name, M):
         y = host(Y).astype(np.float64)
         assert np.all(np.isfinite(y)), call
         assert_within_bound(y, y_ref, bound, f"noalloc {name} M={M} call {call}")
+        # and it agrees with the workspace entry point within the same tolerance
+        assert_within_bound(y, host(Y_ws).astype(np.float64), bound, f"noalloc vs tern_linear call {call}")
 
 
 def test_noalloc_rejects_problems_beyond_the_scratch():
