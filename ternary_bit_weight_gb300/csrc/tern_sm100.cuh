@@ -20,6 +20,21 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
+// True in exactly one lane of a fully active warp (the same lane every time).
+// Loops that issue asynchronous tensor-core or copy instructions run in the
+// whole warp, with values warp-uniform, and only the issue is elected: this
+// keeps descriptors in uniform registers and issues far faster than a loop
+// inside a single-lane branch.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {

@@ -6,41 +6,46 @@
 // §4.3): the weights stay packed in memory; signs are summed inside each
 // 128-wide scale group and the FP16 scale is applied once per group.  The
 // page's CUDA-core kernel is replaced by tensor cores fed from tensor
-// memory:
+// memory.  One persistent CTA per SM owns a contiguous range of work units
+// (one unit = one 128-row x 128-weight block of the tiled layout: 4 KB of
+// codes + 256 B of scales) and runs a pipeline of warp roles:
 //
-//   * work unit = one 128-row x 128-weight block of the tiled layout (4 KB
-//     of codes + 256 B of scales);
-//   * one persistent CTA per SM; a producer warp fills a ring of shared-
-//     memory stages with bulk copies (one unit per worker per stage);
-//   * two decode workers (warpgroups; one thread per weight row = one
-//     tensor-memory lane) turn each 16-weight code word into eight exact
-//     bf16 pairs t in {-1,0,+1} (one LOP3 + one bf16x2 FMA per pair) and
-//     store the unit's 64 columns of A with tcgen05.st into a 3-deep ring;
-//   * an MMA warp issues eight tcgen05.mma (M = 128, N = 16, K = 16, bf16
-//     -> fp32) per unit, A from tensor memory, B = X from shared memory,
-//     into a per-unit accumulator ("D");
-//   * promotion: the workers read the units' fp32 group partials with
-//     tcgen05.ld one batch behind the decode and add s * partial to register
-//     accumulators -- the FP16 scale is converted exactly to fp32 and never
-//     rounded to bf16.
+//   * producer warp: a ring of shared-memory stages of 8 consecutive units,
+//     filled with two bulk copies per stage (codes, scales) -- few large
+//     copies, since a CTA's copy ring completes only a few copies per
+//     microsecond whatever their size;
+//   * two decode streams (even units / odd units), each two warpgroups
+//     splitting the unit's 128 weights per row into halves (one thread per
+//     weight row = one tensor-memory lane): each 16-weight code word
+//     becomes eight exact bf16 pairs t in {-1,0,+1} (one LOP3 + one bf16x2
+//     FMA per pair, balanced between the integer and FMA pipes) stored with
+//     tcgen05.st into a 6-unit ring of A operands;
+//   * MMA warp: eight tcgen05.mma (M = 128, N = 16, K = 16, bf16 -> fp32)
+//     per unit, A from tensor memory, B = X from shared memory, into one of
+//     8 accumulator slots; the whole warp runs the loop and one elected lane
+//     issues (warp-uniform descriptors issue far faster);
+//   * promotion warpgroup: reads each unit's fp32 group partial with
+//     tcgen05.ld and adds s * partial to register accumulators -- the FP16
+//     scale is converted exactly to fp32 and never rounded to bf16 -- and
+//     finishes tiles.
+// Every hand-off is a per-unit mbarrier, so no role waits for a batch of
+// another's work.
 //
-// M == 1 ("one"): the activation row (2K bytes) is copied once into shared
-// memory and used as B in the no-swizzle layout: row 0 of every core matrix
-// is the real row, rows 1..15 are whatever bytes follow it (they only feed
+// M == 1: the activation row (2K bytes) is copied once into shared memory
+// and used as B in the no-swizzle layout: row 0 of every core matrix is the
+// real row, rows 1..15 are whatever bytes follow it (they only feed
 // accumulator columns 1..15, which nobody reads), and only column 0 of each
 // unit's accumulator is promoted.
+// M in 2..16: each stage also carries its units' 16-row X tiles, copied by
+// TMA (128-byte swizzle, rows >= M zero-filled).
 //
-// M in 2..16: each stage also carries the unit's 16-row X tile, copied by
-// TMA (128-byte swizzle, rows >= M zero-filled); accumulators are 16
-// columns per unit, two units per promotion batch.
-//
-// Work split: worker v owns the contiguous unit range [U*v/V, U*(v+1)/V)
-// in (row tile, group) order.  A tile whose groups span two or more
-// workers is finished by the last of them to arrive (per 32-row quarter),
-// which sums the partials in worker order (deterministic; no waiting on
-// other CTAs).  Every mbarrier wait is bounded; on a timeout the kernel
-// raises the workspace error word, drains its own copies and MMAs, frees
-// its tensor memory and returns.
+// Work split: CTA v owns the contiguous unit range [U*v/V, U*(v+1)/V) in
+// (row tile, group) order.  A tile whose groups span two or more CTAs is
+// finished by the last of them to arrive (per 32-row quarter), which sums
+// the partials in CTA order (deterministic; no waiting on other CTAs).
+// Every mbarrier wait is bounded; on a timeout the kernel raises the
+// workspace error word, drains its own copies and MMAs, frees its tensor
+// memory and returns.
 
 #include <cuda.h>
 
@@ -53,48 +58,52 @@
 namespace tern {
 namespace {
 
-constexpr int kNW = 2;                          // decode workers per CTA
-constexpr int kDecWarps = 4 * kNW;
-constexpr int kProducerWarp = kDecWarps;
-constexpr int kMmaWarp = kDecWarps + 1;
-constexpr int kThreads = (kDecWarps + 2) * 32;
+// warp roles
+constexpr int kDecWarps = 16;                   // 2 streams x 2 warpgroups (halves)
+constexpr int kPromWarp0 = kDecWarps;           // 4 warps
+constexpr int kProducerWarp = kPromWarp0 + 4;
+constexpr int kMmaWarp = kProducerWarp + 1;
+constexpr int kThreads = (kMmaWarp + 1) * 32;
+// tensor memory: the A ring and the accumulators, in pairs of units (one
+// even unit from stream 0, one odd from stream 1); every hand-off is per pair
 constexpr int kTmemCols = 512;
-constexpr int kWorkerCols = kTmemCols / kNW;    // 256 columns per worker
-constexpr int kAU = 3;                          // decoded-A ring depth (units)
-constexpr int kACols = 64;                      // 128 bf16 per row = 64 columns
-constexpr int kDCol0 = kAU * kACols;            // accumulators after the A ring
+constexpr int kAP = 3;                          // decoded-A ring: pairs (6 units)
+constexpr int kACols = 64;                      // 128 bf16 per row = 64 columns per unit
+constexpr int kDCol0 = 2 * kAP * kACols;        // accumulators after the A ring
 constexpr int kNtok = 16;                       // UMMA N
+constexpr int kDP = 4;                          // accumulator ring: pairs of 16-column slots
+static_assert(kDCol0 + 2 * kDP * kNtok <= kTmemCols, "tensor-memory budget");
+// shared memory
+constexpr int kPS = 8;                          // units per stage
 constexpr int kSmemLimit = 232448;              // 227 KB opt-in per CTA
 constexpr int kCtrlBytes = 1024;
 constexpr int kMaxStages = 48;
 
 template <bool ONE>
 struct SCfg {
-    static constexpr int PB = 2;                        // units per promotion batch
-    static constexpr int DS = 2 * PB;                   // 16-column accumulator slots in the ring
-    static constexpr int LAGB = 2;                      // batches between reuses of a slot
     static constexpr int NCOL = ONE ? 1 : kNtok;        // token columns promoted per unit
     static constexpr int XUnit = ONE ? 0 : kNtok * kGroup * 2;   // one unit's X tile
-    static constexpr int StageBytes =
-        ONE ? kNW * kUnitBytes : static_cast<int>(round_up(kNW * (XUnit + kUnitBytes), 1024));
-    static constexpr int OffCodes = kNW * XUnit;
-    static constexpr int OffScales = OffCodes + kNW * kUnitCodeBytes;
+    static constexpr int OffCodes = kPS * XUnit;         // X tiles first (1024-byte aligned)
+    static constexpr int OffScales = OffCodes + kPS * kUnitCodeBytes;
+    static constexpr int StageBytes = static_cast<int>(round_up(OffScales + kPS * kUnitScaleBytes, ONE ? 16 : 1024));
+    // a stage is released by every decode warp, the promotion warps (they
+    // read the scales) and, when X travels in the stage, the MMA commit
+    static constexpr int EmptyCount = kDecWarps + 4 + (ONE ? 0 : 1);
 };
-static_assert(kNW == 2, "stage release count assumes two workers");
-static_assert(kDCol0 + SCfg<true>::DS * kNtok <= kWorkerCols, "tensor-memory budget");
 
 // control block offsets
-constexpr int kBarAFull = 0;                                 // [kNW][kAU]
-constexpr int kBarAEmpty = kBarAFull + 8 * kNW * kAU;        // [kNW][kAU]
-constexpr int kBarDFull = kBarAEmpty + 8 * kNW * kAU;        // [kNW][4]
-constexpr int kBarDEmpty = kBarDFull + 8 * kNW * 4;          // [kNW][4]
-constexpr int kBarX = kBarDEmpty + 8 * kNW * 4;
+constexpr int kBarAFull = 0;                                 // [kAP]
+constexpr int kBarAEmpty = kBarAFull + 8 * kAP;              // [kAP]
+constexpr int kBarDFull = kBarAEmpty + 8 * kAP;              // [kDP]
+constexpr int kBarDEmpty = kBarDFull + 8 * kDP;              // [kDP]
+constexpr int kBarX = kBarDEmpty + 8 * kDP;
 constexpr int kBarDrain = kBarX + 8;
 constexpr int kTmemPtr = kBarDrain + 8;
 constexpr int kAbort = kTmemPtr + 4;
 constexpr int kBarStages = 256;                              // full[S], empty[S]
 static_assert(kAbort + 4 <= kBarStages, "control block");
 static_assert(kBarStages + 16 * kMaxStages <= kCtrlBytes, "control block");
+static_assert(kPS % 2 == 0, "stages hold whole pairs");
 
 struct StreamArgs {
     const uint8_t* codes;
@@ -108,7 +117,7 @@ struct StreamArgs {
     int64_t N;
     int64_t R;
     int64_t U;
-    int64_t V;
+    int64_t V;                 // workers = CTAs
     OutputSplit out;
     int* err;                  // workspace error word
     int* counters;             // [R][4 row quarters]
@@ -119,11 +128,11 @@ __device__ __forceinline__ int64_t owner_worker(int64_t u, int64_t U, int64_t V)
     return ((u + 1) * V - 1) / U;
 }
 
-// Finish tile b whose group partials this worker holds in acc (thread = row
-// r of the tile, acc[m] = token m).  `whole`: this worker covered every
-// group of the tile and owns the result.  Otherwise each warp publishes its
-// 32 rows' partials in the worker's slot, and the last contributing worker
-// to arrive for that row quarter sums all partials in worker order.
+// Finish tile b whose group partials this CTA holds in acc (thread = row r
+// of the tile, acc[m] = token m).  `whole`: this CTA covered every group of
+// the tile and owns the result.  Otherwise each warp publishes its 32 rows'
+// partials in the CTA's slot, and the last contributing CTA to arrive for
+// that row quarter sums all partials in CTA order.
 template <int NCOL>
 __device__ __forceinline__ void flush_tile(const StreamArgs& a, int64_t v, int64_t b, int64_t first_tile,
                                            bool whole, float (&acc)[NCOL], int r) {
@@ -182,11 +191,18 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return __all_sync(0xffffffffu, got);
 }
 
+// Bounded wait by lane 0 alone, its result broadcast to the warp (for warps
+// that only issue asynchronous work after the wait).
+__device__ __forceinline__ bool leader_wait(uint32_t bar, uint32_t parity, volatile int* abort, int lane) {
+    uint32_t got = 1;
+    if (lane == 0) got = mbar_wait(bar, parity, abort) ? 1u : 0u;
+    return __shfl_sync(0xffffffffu, got, 0) != 0;
+}
+
 template <bool ONE>
 __global__ void __launch_bounds__(kThreads, 1)
 stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
     using C = SCfg<ONE>;
-    constexpr int PB = C::PB;
     constexpr int NCOL = C::NCOL;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base (swizzle atoms)
@@ -206,33 +222,24 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = a.G;
 
-    // the workers of this CTA: contiguous unit ranges
-    int64_t w_u0[kNW];
-    int32_t w_n[kNW];
-    int32_t max_n = 0;
-#pragma unroll
-    for (int w = 0; w < kNW; ++w) {
-        const int64_t v = (int64_t)blockIdx.x * kNW + w;
-        w_u0[w] = v < a.V ? a.U * v / a.V : 0;
-        w_n[w] = v < a.V ? static_cast<int32_t>(a.U * (v + 1) / a.V - w_u0[w]) : 0;
-        max_n = w_n[w] > max_n ? w_n[w] : max_n;
-    }
+    // this CTA's worker: a contiguous unit range
+    const int64_t v = blockIdx.x;
+    const int64_t u0 = a.U * v / a.V;
+    const int32_t n = static_cast<int32_t>(a.U * (v + 1) / a.V - u0);
+    const int32_t nst = (n + kPS - 1) / kPS;   // stages of this worker
 
     if (threadIdx.x == 0) {
-        // a stage is released by the four warps of every worker with units
-        // (plus the MMA commit when X travels in the stage)
-        const int active = (w_n[0] > 0) + (w_n[1] > 0);
         for (int s = 0; s < S; ++s) {
             mbar_init(bar_full + 8 * s, 1);
-            mbar_init(bar_empty + 8 * s, 4 * active + (ONE ? 0 : 1));
+            mbar_init(bar_empty + 8 * s, C::EmptyCount);
         }
-        for (int i = 0; i < kNW * kAU; ++i) {
-            mbar_init(cb + kBarAFull + 8 * i, 4);
+        for (int i = 0; i < kAP; ++i) {
+            mbar_init(cb + kBarAFull + 8 * i, kDecWarps);       // both decode streams
             mbar_init(cb + kBarAEmpty + 8 * i, 1);
         }
-        for (int i = 0; i < kNW * 4; ++i) {
+        for (int i = 0; i < kDP; ++i) {
             mbar_init(cb + kBarDFull + 8 * i, 1);
-            mbar_init(cb + kBarDEmpty + 8 * i, 4);
+            mbar_init(cb + kBarDEmpty + 8 * i, 4);               // the promotion warps
         }
         mbar_init(cb + kBarX, 1);
         mbar_init(cb + kBarDrain, 1);
@@ -252,270 +259,250 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
 
     if (warp == kProducerWarp) {
         // ---------------------------------------------------------- producer
-        if (lane == 0) {
-            constexpr uint32_t kPerUnit = kUnitBytes + C::XUnit;
-            int64_t uw[kNW];   // next unit whose weights are loaded
-            int32_t gx[kNW];   // group of the next X tile
-#pragma unroll
-            for (int w = 0; w < kNW; ++w) {
-                uw[w] = w_u0[w];
-                gx[w] = static_cast<int32_t>(w_u0[w] % G);
+        // the whole warp runs the loop; one elected lane issues the copies
+        auto load_weights = [&](int32_t f, uint32_t st, uint32_t bar) {
+            const int64_t uf = u0 + (int64_t)f * kPS;
+            const int32_t cnt = n - f * kPS < kPS ? n - f * kPS : kPS;
+            if (elect_one()) {
+                mbar_arrive_expect_tx(bar, cnt * (kUnitBytes + C::XUnit));
+                bulk_load(st + C::OffCodes, a.codes + uf * kUnitCodeBytes, cnt * kUnitCodeBytes, bar);
+                bulk_load(st + C::OffScales, a.scales + uf * kUnitScaleBytes, cnt * kUnitScaleBytes, bar);
             }
-            auto load_weights = [&](int f, uint32_t st, uint32_t bar) {
-                uint32_t bytes = 0;
-#pragma unroll
-                for (int w = 0; w < kNW; ++w) bytes += f < w_n[w] ? kPerUnit : 0u;
-                mbar_arrive_expect_tx(bar, bytes);
-#pragma unroll
-                for (int w = 0; w < kNW; ++w) {
-                    if (f >= w_n[w]) continue;
-                    bulk_load(st + C::OffCodes + w * kUnitCodeBytes, a.codes + uw[w] * kUnitCodeBytes,
-                              kUnitCodeBytes, bar);
-                    bulk_load(st + C::OffScales + w * kUnitScaleBytes, a.scales + uw[w] * kUnitScaleBytes,
-                              kUnitScaleBytes, bar);
-                    ++uw[w];
-                }
-            };
-            // the weights of the first stages do not depend on earlier kernels
-            const int32_t pre = max_n < S ? max_n : S;
-            for (int32_t f = 0; f < pre; ++f) load_weights(f, ring + f * C::StageBytes, bar_full + 8 * f);
-            grid_dependency_wait();
-            if (ONE) {
+            __syncwarp();
+        };
+        // the weights of the first stages do not depend on earlier kernels
+        const int32_t pre = nst < S ? nst : S;
+        for (int32_t f = 0; f < pre; ++f) load_weights(f, ring + f * C::StageBytes, bar_full + 8 * f);
+        grid_dependency_wait();
+        if (ONE) {
+            if (elect_one()) {
                 mbar_arrive_expect_tx(cb + kBarX, a.x_bytes);
                 bulk_load(sbase, a.x, a.x_bytes, cb + kBarX);
             }
-            int s = 0;
-            uint32_t round = 0;   // completed passes over the ring
-            for (int32_t f = 0; f < max_n; ++f) {
-                const uint32_t st = ring + s * C::StageBytes;
-                if (f >= pre) {
-                    if (!mbar_wait(bar_empty + 8 * s, (round - 1) & 1u, abort_flag)) break;
-                    load_weights(f, st, bar_full + 8 * s);
-                }
-                if (!ONE) {
-#pragma unroll
-                    for (int w = 0; w < kNW; ++w) {
-                        if (f >= w_n[w]) continue;
-                        const int32_t k0 = gx[w] * kGroup;
-                        tma_load_2d(st + w * C::XUnit, &xmap, k0, 0, bar_full + 8 * s);
-                        tma_load_2d(st + w * C::XUnit + kNtok * 128, &xmap, k0 + 64, 0, bar_full + 8 * s);
-                        if (++gx[w] == G) gx[w] = 0;
+            __syncwarp();
+        }
+        int32_t gx = static_cast<int32_t>(u0 % G);           // group of the next X tile
+        int s = 0;
+        uint32_t round = 0;   // completed passes over the ring
+        for (int32_t f = 0; f < nst; ++f) {
+            const uint32_t st = ring + s * C::StageBytes;
+            if (f >= pre) {
+                if (!warp_wait(bar_empty + 8 * s, (round - 1) & 1u, abort_flag)) break;
+                load_weights(f, st, bar_full + 8 * s);
+            }
+            if (!ONE) {
+                const int32_t cnt = n - f * kPS < kPS ? n - f * kPS : kPS;
+                for (int32_t i = 0; i < cnt; ++i) {
+                    const int32_t k0 = gx * kGroup;
+                    if (elect_one()) {
+                        tma_load_2d(st + i * C::XUnit, &xmap, k0, 0, bar_full + 8 * s);
+                        tma_load_2d(st + i * C::XUnit + kNtok * 128, &xmap, k0 + 64, 0, bar_full + 8 * s);
                     }
-                }
-                if (++s == S) {
-                    s = 0;
-                    ++round;
+                    __syncwarp();
+                    if (++gx == G) gx = 0;
                 }
             }
-            if (*abort_flag) {
-                // drain the copies this CTA may still have in flight (bounded)
-                volatile int no_abort = 0;
-                for (int t = 0; t < S; ++t) {
-                    (void)mbar_wait(bar_full + 8 * t, 0, &no_abort);
-                    (void)mbar_wait(bar_full + 8 * t, 1, &no_abort);
-                }
-                (void)mbar_wait(cb + kBarX, 0, &no_abort);
+            if (++s == S) {
+                s = 0;
+                ++round;
             }
+        }
+        if (*abort_flag) {
+            // drain the copies this CTA may still have in flight (bounded)
+            volatile int no_abort = 0;
+            for (int t = 0; t < S; ++t) {
+                (void)mbar_wait(bar_full + 8 * t, 0, &no_abort);
+                (void)mbar_wait(bar_full + 8 * t, 1, &no_abort);
+            }
+            (void)mbar_wait(cb + kBarX, 0, &no_abort);
         }
     } else if (warp == kMmaWarp) {
         // --------------------------------------------------------------- MMA
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(128, kNtok);
-            bool ok = true;
-            if (ONE) ok = mbar_wait(cb + kBarX, 0, abort_flag);
-            int32_t gm[kNW];   // group of the next unit (B address when M == 1)
+        // the whole warp runs the loop with warp-uniform descriptors; lane 0
+        // waits, one elected lane (always the same) issues the MMAs of a pair
+        // of units -- their two K-step chains interleaved -- and the commits
+        constexpr uint32_t idesc = idesc_bf16_f32(128, kNtok);
+        bool ok = true;
+        if (ONE) ok = leader_wait(cb + kBarX, 0, abort_flag, lane);
+        int32_t g = static_cast<int32_t>(u0 % G);   // group of the pair's first unit
+        // B descriptors: M == 1 the resident row (+16 per group, +2 per K-step);
+        // else the unit's X tile in the stage
+        const uint64_t bdesc_x = smem_desc_kmajor_noswz(sbase, 16, 16);
+        const uint64_t bdesc_ring = smem_desc_kmajor_sw128(ring);
+        int s = 0, us = 0, ap = 0, dp = 0;   // stage, unit in stage, A pair slot, D pair slot
+        uint32_t full_ph = 0, a_ph = 0, d_ph = 0;
+        for (int32_t f = 0; f < n && ok; f += 2) {
+            const int32_t k = f >> 1;
+            const bool two = f + 1 < n;
+            ok = (k < kDP || leader_wait(cb + kBarDEmpty + 8 * dp, d_ph ^ 1u, abort_flag, lane)) &&
+                 (ONE || us != 0 || leader_wait(bar_full + 8 * s, full_ph, abort_flag, lane)) &&
+                 leader_wait(cb + kBarAFull + 8 * ap, a_ph, abort_flag, lane);
+            if (!ok) break;
+            tc_fence_after_sync();
+            const uint32_t a_tm = tmem + 2 * ap * kACols;
+            const uint32_t d_tm = tmem + kDCol0 + 2 * dp * kNtok;
+            const int32_t g1 = g + 1 == G ? 0 : g + 1;
+            const uint64_t b0 = ONE ? bdesc_x + 16u * (uint32_t)g
+                                    : bdesc_ring + ((uint32_t)(s * C::StageBytes + us * C::XUnit) >> 4);
+            const uint64_t b1 = ONE ? bdesc_x + 16u * (uint32_t)g1
+                                    : bdesc_ring + ((uint32_t)(s * C::StageBytes + (us + 1) * C::XUnit) >> 4);
+            if (elect_one()) {
 #pragma unroll
-            for (int w = 0; w < kNW; ++w) gm[w] = static_cast<int32_t>(w_u0[w] % G);
-            int s = 0, aslot = 0;
-            uint32_t full_ph = 0, around = 0;
-            for (int32_t f = 0; f < max_n && ok; ++f) {
-                const uint32_t st = ring + s * C::StageBytes;
-                if (!ONE && !mbar_wait(bar_full + 8 * s, full_ph, abort_flag)) {
-                    ok = false;
-                    break;
+                for (int kk = 0; kk < 8; ++kk) {
+                    // M == 1: +32 bytes per K-step; else +32 bytes within a
+                    // 64-wide box and +2048 bytes to the second box
+                    const uint32_t step = ONE ? 2 * kk : (kk >> 2) * (kNtok * 128 / 16) + 2 * (kk & 3);
+                    umma_bf16_tmem_a(d_tm, a_tm + 8 * kk, b0 + step, idesc, kk > 0 ? 1u : 0u);
+                    if (two) umma_bf16_tmem_a(d_tm + kNtok, a_tm + kACols + 8 * kk, b1 + step, idesc, kk > 0 ? 1u : 0u);
                 }
-                const int i = f % PB, beta = f / PB;
-#pragma unroll
-                for (int w = 0; w < kNW; ++w) {
-                    if (!ok || f >= w_n[w]) continue;
-                    if (i == 0 && beta >= C::LAGB) {
-                        const int bb = beta - C::LAGB;
-                        if (!mbar_wait(cb + kBarDEmpty + 8 * (w * 4 + (bb & 3)), (bb >> 2) & 1, abort_flag)) {
-                            ok = false;
-                            continue;
-                        }
-                    }
-                    if (!mbar_wait(cb + kBarAFull + 8 * (w * kAU + aslot), around, abort_flag)) {
-                        ok = false;
-                        continue;
-                    }
-                    tc_fence_after_sync();
-                    const uint32_t a_tm = tmem + w * kWorkerCols + aslot * kACols;
-                    const uint32_t d_tm = tmem + w * kWorkerCols + kDCol0 + kNtok * (f & (C::DS - 1));
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        uint64_t bdesc;
-                        if (ONE)
-                            bdesc = smem_desc_kmajor_noswz(sbase + 2u * (uint32_t)(kGroup * gm[w] + 16 * kk), 16, 16);
-                        else   // +32 bytes per K-step = +2 in the address field
-                            bdesc = smem_desc_kmajor_sw128(st + w * C::XUnit + (kk >> 2) * (kNtok * 128)) + 2 * (kk & 3);
-                        umma_bf16_tmem_a(d_tm, a_tm + 8 * kk, bdesc, idesc, kk > 0 ? 1u : 0u);
-                    }
-                    umma_commit(cb + kBarAEmpty + 8 * (w * kAU + aslot));
-                    if (i == PB - 1 || f == w_n[w] - 1) umma_commit(cb + kBarDFull + 8 * (w * 4 + (beta & 3)));
-                    if (++gm[w] == G) gm[w] = 0;
-                }
-                if (!ONE && ok) umma_commit(bar_empty + 8 * s);
-                if (++aslot == kAU) {
-                    aslot = 0;
-                    around ^= 1u;
-                }
+                umma_commit(cb + kBarAEmpty + 8 * ap);
+                umma_commit(cb + kBarDFull + 8 * dp);
+                if (!ONE && (us == kPS - 2 || f + 2 >= n)) umma_commit(bar_empty + 8 * s);
+            }
+            __syncwarp();
+            g = g1 + 1 == G ? 0 : g1 + 1;
+            if (++ap == kAP) {
+                ap = 0;
+                a_ph ^= 1u;
+            }
+            if (++dp == kDP) {
+                dp = 0;
+                d_ph ^= 1u;
+            }
+            us += 2;
+            if (us == kPS) {
+                us = 0;
                 if (++s == S) {
                     s = 0;
                     full_ph ^= 1u;
                 }
             }
-            // every MMA issued has completed before tensor memory is freed
-            umma_commit(cb + kBarDrain);
-            volatile int no_abort = 0;
-            (void)mbar_wait(cb + kBarDrain, 0, &no_abort);
         }
-    } else {
-        // ---------------------------------------------------- decode workers
-        const int wg = warp >> 2;
+        // every MMA issued has completed before tensor memory is freed
+        if (elect_one()) umma_commit(cb + kBarDrain);
+        __syncwarp();
+        volatile int no_abort = 0;
+        (void)mbar_wait(cb + kBarDrain, 0, &no_abort);
+    } else if (warp < kDecWarps) {
+        // ---------------------------------------------------- decode streams
+        // stream q decodes units j = q, q+2, ... (unit q of pair j/2); its
+        // warpgroup h decodes half h (weights 64h..64h+63 of the unit's 128)
+        const int q = warp >> 3, h = (warp >> 2) & 1;
         const int r = threadIdx.x & 127;   // weight row in the tile = tensor-memory lane
-        const int64_t v = (int64_t)blockIdx.x * kNW + wg;
-        const int32_t n = w_n[wg == 0 ? 0 : 1];
-        const int64_t u0 = w_u0[wg == 0 ? 0 : 1];
-        const uint32_t tm = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + wg * kWorkerCols;
-        const uint32_t bar_afull = cb + kBarAFull + 8 * kAU * wg;
-        const uint32_t bar_aempty = cb + kBarAEmpty + 8 * kAU * wg;
-        const uint32_t bar_dfull = cb + kBarDFull + 8 * 4 * wg;
-        const uint32_t bar_dempty = cb + kBarDEmpty + 8 * 4 * wg;
-        if (n > 0) {
-            const int codes_off = C::OffCodes + wg * kUnitCodeBytes + 16 * r;
-            const int scale_off = C::OffScales + wg * kUnitScaleBytes + 2 * r;
-            // promotion cursor (tile, group) of the next unit to promote
-            const int64_t first_tile = u0 / G;
-            const int32_t first_g = static_cast<int32_t>(u0 - first_tile * G);
-            int64_t pb = first_tile;
-            int32_t pg = first_g;
-            float acc[NCOL];
-#pragma unroll
-            for (int m = 0; m < NCOL; ++m) acc[m] = 0.f;
-            float s_cur[PB], s_prev[PB];
-#pragma unroll
-            for (int i = 0; i < PB; ++i) s_cur[i] = s_prev[i] = 0.f;
-            bool ok = true, waited = false;
-            int s = 0, aslot = 0;
-            uint32_t full_ph = 0, around = 0;
-
-            // acc += s * partial for the units of batch b, finishing tiles
-            auto promote = [&](int32_t b) {
-                if (!waited) {
-                    grid_dependency_wait();   // outputs and workspace belong to earlier kernels until now
-                    waited = true;
-                }
-                if (!warp_wait(bar_dfull + 8 * (b & 3), (b >> 2) & 1, abort_flag)) {
-                    ok = false;
-                    return;
-                }
-                tc_fence_after_sync();
-                const int32_t cnt = (n - b * PB) < PB ? (n - b * PB) : PB;
-                uint32_t d[PB * NCOL];
-#pragma unroll
-                for (int i = 0; i < PB; ++i) {
-                    const uint32_t col = tm + kDCol0 + kNtok * ((b * PB + i) & (C::DS - 1));
-                    // straight into d: the registers are valid only after the wait
-                    if (ONE)
-                        tmem_ld_32x32b_x1(col, d[i]);
-                    else
-                        tmem_ld_32x32b_x16(col, *reinterpret_cast<uint32_t(*)[16]>(d + i * NCOL));
-                }
-                tmem_ld_wait();
-                tc_fence_before_sync();
+        const uint32_t tm = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + q * kACols + 32 * h;
+        const int codes_off = C::OffCodes + 2048 * h + 16 * r;   // + unit in stage * 4096
+        int s = 0, ap = 0;
+        uint32_t full_ph = 0, a_ph = 0;
+        int32_t j = q;
+        for (; j < n; j += 2) {
+            const int32_t k = j >> 1;
+            const int us = j % kPS;
+            if (us < 2 && !warp_wait(bar_full + 8 * s, full_ph, abort_flag)) break;   // first unit of the stage
+            const uint4 c = lds_v4(ring_ptr + s * C::StageBytes + codes_off + us * kUnitCodeBytes);
+            if (us >= kPS - 2 || j + 2 >= n) {   // this stream's last unit of the stage
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar_dempty + 8 * (b & 3));
-#pragma unroll
-                for (int i = 0; i < PB; ++i) {
-                    if (i >= cnt) continue;
-#pragma unroll
-                    for (int m = 0; m < NCOL; ++m) acc[m] = fmaf(s_prev[i], __uint_as_float(d[i * NCOL + m]), acc[m]);
-                    const int32_t u = b * PB + i;
-                    if (pg == G - 1 || u == n - 1) {
-                        const bool whole = (pb != first_tile || first_g == 0) && pg == G - 1;
-                        flush_tile<NCOL>(a, v, pb, first_tile, whole, acc, r);
-#pragma unroll
-                        for (int m = 0; m < NCOL; ++m) acc[m] = 0.f;
-                    }
-                    if (++pg == G) {
-                        pg = 0;
-                        ++pb;
-                    }
+                if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+                if (++s == S) {
+                    s = 0;
+                    full_ph ^= 1u;
                 }
-            };
-
-            int32_t beta = 0;
-            for (; beta * PB < n && ok; ++beta) {
-#pragma unroll
-                for (int i = 0; i < PB; ++i) {
-                    const int32_t j = beta * PB + i;
-                    if (j >= n || !ok) continue;
-                    // ---- unit j: codes and scale from the stage, then release it
-                    if (!warp_wait(bar_full + 8 * s, full_ph, abort_flag)) {
-                        ok = false;
-                        continue;
-                    }
-                    const uint8_t* stp = ring_ptr + s * C::StageBytes;
-                    const uint4 c0 = lds_v4(stp + codes_off);
-                    const uint4 c1 = lds_v4(stp + codes_off + 2048);
-                    const uint32_t sc = *reinterpret_cast<const uint16_t*>(stp + scale_off);
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar_empty + 8 * s);
-                    if (++s == S) {
-                        s = 0;
-                        full_ph ^= 1u;
-                    }
-                    // ---- decode into the A ring slot
-                    if (j >= kAU) {
-                        if (!warp_wait(bar_aempty + 8 * aslot, around ^ 1u, abort_flag)) {
-                            ok = false;
-                            continue;
-                        }
-                        tc_fence_after_sync();
-                    }
-                    const uint32_t a_tm = tm + aslot * kACols;
-                    {
-                        uint32_t p[32];
-                        decode_word_bf16(c0.x, p);
-                        decode_word_bf16(c0.y, p + 8);
-                        decode_word_bf16(c0.z, p + 16);
-                        decode_word_bf16(c0.w, p + 24);
-                        tmem_st_32x32b_x32(a_tm, p);
-                    }
-                    {
-                        uint32_t p[32];
-                        decode_word_bf16(c1.x, p);
-                        decode_word_bf16(c1.y, p + 8);
-                        decode_word_bf16(c1.z, p + 16);
-                        decode_word_bf16(c1.w, p + 24);
-                        tmem_st_32x32b_x32(a_tm + 32, p);
-                    }
-                    tmem_st_wait();
-                    tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar_afull + 8 * aslot);
-                    if (++aslot == kAU) {
-                        aslot = 0;
-                        around ^= 1u;
-                    }
-                    s_cur[i] = fp16_bits_to_float(sc);
-                }
-                if (ok && beta >= 1) promote(beta - 1);
-#pragma unroll
-                for (int i = 0; i < PB; ++i) s_prev[i] = s_cur[i];
             }
-            if (ok && beta >= 1) promote(beta - 1);
+            if (k >= kAP) {
+                if (!warp_wait(cb + kBarAEmpty + 8 * ap, a_ph ^ 1u, abort_flag)) break;
+                tc_fence_after_sync();
+            }
+            uint32_t p[32];
+            decode_word_bf16(c.x, p);
+            decode_word_bf16(c.y, p + 8);
+            decode_word_bf16(c.z, p + 16);
+            decode_word_bf16(c.w, p + 24);
+            tmem_st_32x32b_x32(tm + 2 * ap * kACols, p);
+            tmem_st_wait();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(cb + kBarAFull + 8 * ap);
+            if (++ap == kAP) {
+                ap = 0;
+                a_ph ^= 1u;
+            }
+        }
+        // odd n: the last pair has no unit for stream 1, which still signals
+        // it -- after the slot's previous pair has been consumed, so that the
+        // arrival cannot count towards that pair's phase
+        if (j == n && q == 1 && (n & 1)) {
+            if ((j >> 1) < kAP || warp_wait(cb + kBarAEmpty + 8 * ap, a_ph ^ 1u, abort_flag)) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(cb + kBarAFull + 8 * ap);
+            }
+        }
+    } else if (warp < kPromWarp0 + 4) {
+        // ------------------------------------------------------- promotion
+        const int r = threadIdx.x & 127;   // weight row in the tile = tensor-memory lane
+        const uint32_t tm = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + kDCol0;
+        const int scale_off = C::OffScales + 2 * r;   // + unit in stage * 256
+        const int64_t first_tile = u0 / G;
+        const int32_t first_g = static_cast<int32_t>(u0 - first_tile * G);
+        int64_t pb = first_tile;
+        int32_t pg = first_g;
+        float acc[NCOL];
+#pragma unroll
+        for (int m = 0; m < NCOL; ++m) acc[m] = 0.f;
+        grid_dependency_wait();   // outputs and workspace belong to earlier kernels until now
+        int s = 0, us = 0, dp = 0;
+        uint32_t full_ph = 0, d_ph = 0;
+        for (int32_t f = 0; f < n; f += 2) {
+            const bool two = f + 1 < n;
+            // the stage's copies completed long ago (its units were decoded);
+            // observing its barrier makes the scales visible to these threads
+            if (us == 0 && !warp_wait(bar_full + 8 * s, full_ph, abort_flag)) break;
+            if (!warp_wait(cb + kBarDFull + 8 * dp, d_ph, abort_flag)) break;
+            tc_fence_after_sync();
+            uint32_t d[2 * NCOL];
+            if (ONE) {
+                tmem_ld_32x32b_x1(tm + 2 * dp * kNtok, d[0]);
+                tmem_ld_32x32b_x1(tm + (2 * dp + 1) * kNtok, d[1]);
+            } else {
+                tmem_ld_32x32b_x16(tm + 2 * dp * kNtok, *reinterpret_cast<uint32_t(*)[16]>(d));
+                tmem_ld_32x32b_x16(tm + (2 * dp + 1) * kNtok, *reinterpret_cast<uint32_t(*)[16]>(d + NCOL));
+            }
+            const uint8_t* sp = ring_ptr + s * C::StageBytes + scale_off + us * kUnitScaleBytes;
+            const float sc0 = fp16_bits_to_float(*reinterpret_cast<const uint16_t*>(sp));
+            const float sc1 = two ? fp16_bits_to_float(*reinterpret_cast<const uint16_t*>(sp + kUnitScaleBytes)) : 0.f;
+            tmem_ld_wait();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(cb + kBarDEmpty + 8 * dp);
+            us += 2;
+            if (us == kPS || f + 2 >= n) {   // done with this stage's scales
+                if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+                us = 0;
+                if (++s == S) {
+                    s = 0;
+                    full_ph ^= 1u;
+                }
+            }
+            if (++dp == kDP) {
+                dp = 0;
+                d_ph ^= 1u;
+            }
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                if (i == 1 && !two) break;
+                const float sc = i == 0 ? sc0 : sc1;
+#pragma unroll
+                for (int m = 0; m < NCOL; ++m) acc[m] = fmaf(sc, __uint_as_float(d[i * NCOL + m]), acc[m]);
+                const int32_t u = f + i;
+                if (pg == G - 1 || u == n - 1) {
+                    const bool whole = (pb != first_tile || first_g == 0) && pg == G - 1;
+                    flush_tile<NCOL>(a, v, pb, first_tile, whole, acc, r);
+#pragma unroll
+                    for (int m = 0; m < NCOL; ++m) acc[m] = 0.f;
+                }
+                if (++pg == G) {
+                    pg = 0;
+                    ++pb;
+                }
+            }
         }
     }
 
@@ -601,15 +588,13 @@ StreamPlan plan_stream(int64_t M, int64_t N, int64_t K, int sm_count) {
     p.R = ceil_div(N, kTileRows);
     p.G = K / kGroup;
     p.U = p.R * p.G;
-    int64_t workers = (int64_t)sm_count * kNW;
-    if (workers > p.U) workers = p.U;
-    p.V = workers;
-    p.grid = ceil_div(workers, kNW);
-    // M == 1 keeps the activation row in shared memory when at least four
+    p.V = p.U < sm_count ? p.U : sm_count;   // one worker per CTA, one CTA per SM
+    p.grid = p.V;
+    // M == 1 keeps the activation row in shared memory when at least three
     // stages still fit beside it
     const int64_t x_smem = round_up(2 * K + 256, 1024);
     const int64_t avail_one = kSmemLimit - 1024 - kCtrlBytes - x_smem;
-    p.one = (M == 1) && avail_one >= 4 * SCfg<true>::StageBytes;
+    p.one = (M == 1) && avail_one >= 3 * SCfg<true>::StageBytes;
     const int64_t stage_bytes = p.one ? SCfg<true>::StageBytes : SCfg<false>::StageBytes;
     const int64_t avail = p.one ? avail_one : kSmemLimit - 1024 - kCtrlBytes;
     int64_t stages = avail / stage_bytes;
