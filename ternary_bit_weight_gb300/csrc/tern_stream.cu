@@ -14,22 +14,22 @@
 //     filled with two bulk copies per stage (codes, scales) -- few large
 //     copies, since a CTA's copy ring completes only a few copies per
 //     microsecond whatever their size;
-//   * two decode streams (even units / odd units), each two warpgroups
-//     splitting the unit's 128 weights per row into halves (one thread per
-//     weight row = one tensor-memory lane): each 16-weight code word
-//     becomes eight exact bf16 pairs t in {-1,0,+1} (one LOP3 + one bf16x2
-//     FMA per pair, balanced between the integer and FMA pipes) stored with
-//     tcgen05.st into a 6-unit ring of A operands;
-//   * MMA warp: eight tcgen05.mma (M = 128, N = 16, K = 16, bf16 -> fp32)
-//     per unit, A from tensor memory, B = X from shared memory, into one of
-//     8 accumulator slots; the whole warp runs the loop and one elected lane
-//     issues (warp-uniform descriptors issue far faster);
+//   * two decode streams (even units / odd units), one warpgroup each (one
+//     thread per weight row = one tensor-memory lane): each 16-weight code
+//     word becomes eight exact bf16 pairs t in {-1,0,+1} (one LOP3 + one
+//     bf16x2 FMA per pair, balanced between the integer and FMA pipes)
+//     stored with tcgen05.st into the stream's 3-unit ring of A operands;
+//   * two MMA warps, one per stream: eight tcgen05.mma (M = 128, N = 16,
+//     K = 16, bf16 -> fp32) per unit, A from tensor memory, B = X from
+//     shared memory, into one of 8 accumulator slots; the whole warp runs
+//     the loop and one elected lane issues (warp-uniform descriptors issue
+//     far faster than a loop inside a single-lane branch);
 //   * promotion warpgroup: reads each unit's fp32 group partial with
 //     tcgen05.ld and adds s * partial to register accumulators -- the FP16
 //     scale is converted exactly to fp32 and never rounded to bf16 -- and
 //     finishes tiles.
-// Every hand-off is a per-unit mbarrier, so no role waits for a batch of
-// another's work.
+// Every hand-off is an mbarrier per unit (A operands) or per pair of units
+// (accumulators), so no role waits for a batch of another's work.
 //
 // M == 1: the activation row (2K bytes) is copied once into shared memory
 // and used as B in the no-swizzle layout: row 0 of every core matrix is the
@@ -59,17 +59,17 @@ namespace tern {
 namespace {
 
 // warp roles
-constexpr int kDecWarps = 16;                   // 2 streams x 2 warpgroups (halves)
+constexpr int kDecWarps = 8;                    // 2 streams x 1 warpgroup (whole units)
 constexpr int kPromWarp0 = kDecWarps;           // 4 warps
-constexpr int kProducerWarp = kPromWarp0 + 4;
-constexpr int kMmaWarp = kProducerWarp + 1;
-constexpr int kThreads = (kMmaWarp + 1) * 32;
-// tensor memory: the A ring and the accumulators, in pairs of units (one
-// even unit from stream 0, one odd from stream 1); every hand-off is per pair
+constexpr int kProducerWarp = kPromWarp0 + 4;   // on SMSP 0
+constexpr int kMmaWarp0 = kProducerWarp + 1;    // one MMA warp per decode stream, SMSPs 1 and 2
+constexpr int kThreads = (kMmaWarp0 + 2) * 32;
+// tensor memory: each decode stream has its own A ring; accumulators come
+// in pairs of 16-column slots (one even unit, one odd unit)
 constexpr int kTmemCols = 512;
-constexpr int kAP = 3;                          // decoded-A ring: pairs (6 units)
+constexpr int kAQ = 3;                          // A ring per stream (units)
 constexpr int kACols = 64;                      // 128 bf16 per row = 64 columns per unit
-constexpr int kDCol0 = 2 * kAP * kACols;        // accumulators after the A ring
+constexpr int kDCol0 = 2 * kAQ * kACols;        // accumulators after the A rings
 constexpr int kNtok = 16;                       // UMMA N
 constexpr int kDP = 4;                          // accumulator ring: pairs of 16-column slots
 static_assert(kDCol0 + 2 * kDP * kNtok <= kTmemCols, "tensor-memory budget");
@@ -87,23 +87,28 @@ struct SCfg {
     static constexpr int OffScales = OffCodes + kPS * kUnitCodeBytes;
     static constexpr int StageBytes = static_cast<int>(round_up(OffScales + kPS * kUnitScaleBytes, ONE ? 16 : 1024));
     // a stage is released by every decode warp, the promotion warps (they
-    // read the scales) and, when X travels in the stage, the MMA commit
-    static constexpr int EmptyCount = kDecWarps + 4 + (ONE ? 0 : 1);
+    // read the scales) and, when X travels in the stage, both MMA
+    // warps
+    static constexpr int EmptyCount = kDecWarps + 4 + (ONE ? 0 : 2);
 };
 
 // control block offsets
-constexpr int kBarAFull = 0;                                 // [kAP]
-constexpr int kBarAEmpty = kBarAFull + 8 * kAP;              // [kAP]
-constexpr int kBarDFull = kBarAEmpty + 8 * kAP;              // [kDP]
+constexpr int kBarAFull = 0;                                 // [2][kAQ]
+constexpr int kBarAEmpty = kBarAFull + 8 * 2 * kAQ;          // [2][kAQ]
+constexpr int kBarDFull = kBarAEmpty + 8 * 2 * kAQ;          // [kDP]
 constexpr int kBarDEmpty = kBarDFull + 8 * kDP;              // [kDP]
-constexpr int kBarX = kBarDEmpty + 8 * kDP;
-constexpr int kBarDrain = kBarX + 8;
-constexpr int kTmemPtr = kBarDrain + 8;
+constexpr int kBarX = kBarDEmpty + 8 * kDP;                  // activation row copied (M == 1)
+constexpr int kBarDrain = kBarX + 8;                         // [2]
+constexpr int kTmemPtr = kBarDrain + 16;
 constexpr int kAbort = kTmemPtr + 4;
 constexpr int kBarStages = 256;                              // full[S], empty[S]
 static_assert(kAbort + 4 <= kBarStages, "control block");
 static_assert(kBarStages + 16 * kMaxStages <= kCtrlBytes, "control block");
 static_assert(kPS % 2 == 0, "stages hold whole pairs");
+
+// M == 1 shared-memory layout before the stages: the activation row (2K
+// bytes) and 256 bytes the tensor cores may read past its end.
+__host__ __device__ constexpr int64_t x_smem_bytes(int64_t K) { return round_up(2 * K + 256, 1024); }
 
 struct StreamArgs {
     const uint8_t* codes;
@@ -233,16 +238,17 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, C::EmptyCount);
         }
-        for (int i = 0; i < kAP; ++i) {
-            mbar_init(cb + kBarAFull + 8 * i, kDecWarps);       // both decode streams
+        for (int i = 0; i < 2 * kAQ; ++i) {
+            mbar_init(cb + kBarAFull + 8 * i, kDecWarps / 2);   // the stream's 4 warps
             mbar_init(cb + kBarAEmpty + 8 * i, 1);
         }
         for (int i = 0; i < kDP; ++i) {
-            mbar_init(cb + kBarDFull + 8 * i, 1);
+            mbar_init(cb + kBarDFull + 8 * i, 2);                // both MMA warps
             mbar_init(cb + kBarDEmpty + 8 * i, 4);               // the promotion warps
         }
         mbar_init(cb + kBarX, 1);
         mbar_init(cb + kBarDrain, 1);
+        mbar_init(cb + kBarDrain + 8, 1);
         *abort_flag = 0;
         mbar_fence_init();
     }
@@ -316,36 +322,39 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
             }
             (void)mbar_wait(cb + kBarX, 0, &no_abort);
         }
-    } else if (warp == kMmaWarp) {
+    } else if (warp >= kMmaWarp0) {
         // --------------------------------------------------------------- MMA
-        // the whole warp runs the loop with warp-uniform descriptors; lane 0
-        // waits, one elected lane (always the same) issues the MMAs of a pair
-        // of units -- their two K-step chains interleaved -- and the commits
+        // MMA warp q serves decode stream q (units q, q+2, ...).  The whole
+        // warp runs the loop with warp-uniform descriptors; lane 0 waits and
+        // one elected lane (always the same) issues the MMAs and commits.
+        const int q = warp - kMmaWarp0;
         constexpr uint32_t idesc = idesc_bf16_f32(128, kNtok);
         bool ok = true;
         if (ONE) ok = leader_wait(cb + kBarX, 0, abort_flag, lane);
-        int32_t g = static_cast<int32_t>(u0 % G);   // group of the pair's first unit
+        int32_t g = static_cast<int32_t>((u0 + q) % G);   // group of unit j
+        const int32_t g_step = 2 % G;
         // B descriptors: M == 1 the resident row (+16 per group, +2 per K-step);
         // else the unit's X tile in the stage
         const uint64_t bdesc_x = smem_desc_kmajor_noswz(sbase, 16, 16);
         const uint64_t bdesc_ring = smem_desc_kmajor_sw128(ring);
-        int s = 0, us = 0, ap = 0, dp = 0;   // stage, unit in stage, A pair slot, D pair slot
+        const uint32_t bar_afull = cb + kBarAFull + 8 * kAQ * q;
+        const uint32_t bar_aempty = cb + kBarAEmpty + 8 * kAQ * q;
+        const uint32_t a_tm0 = tmem + q * kAQ * kACols;
+        const uint32_t d_tm0 = tmem + kDCol0 + q * kNtok;
+        int s = 0, al = 0, dp = 0;   // stage, A slot, D pair slot
         uint32_t full_ph = 0, a_ph = 0, d_ph = 0;
-        for (int32_t f = 0; f < n && ok; f += 2) {
-            const int32_t k = f >> 1;
-            const bool two = f + 1 < n;
+        for (int32_t j = q; j < n && ok; j += 2) {
+            const int32_t k = j >> 1;
+            const int us = j % kPS;
             ok = (k < kDP || leader_wait(cb + kBarDEmpty + 8 * dp, d_ph ^ 1u, abort_flag, lane)) &&
-                 (ONE || us != 0 || leader_wait(bar_full + 8 * s, full_ph, abort_flag, lane)) &&
-                 leader_wait(cb + kBarAFull + 8 * ap, a_ph, abort_flag, lane);
+                 (ONE || us >= 2 || leader_wait(bar_full + 8 * s, full_ph, abort_flag, lane)) &&
+                 leader_wait(bar_afull + 8 * al, a_ph, abort_flag, lane);
             if (!ok) break;
             tc_fence_after_sync();
-            const uint32_t a_tm = tmem + 2 * ap * kACols;
-            const uint32_t d_tm = tmem + kDCol0 + 2 * dp * kNtok;
-            const int32_t g1 = g + 1 == G ? 0 : g + 1;
+            const uint32_t a_tm = a_tm0 + al * kACols;
+            const uint32_t d_tm = d_tm0 + 2 * dp * kNtok;
             const uint64_t b0 = ONE ? bdesc_x + 16u * (uint32_t)g
                                     : bdesc_ring + ((uint32_t)(s * C::StageBytes + us * C::XUnit) >> 4);
-            const uint64_t b1 = ONE ? bdesc_x + 16u * (uint32_t)g1
-                                    : bdesc_ring + ((uint32_t)(s * C::StageBytes + (us + 1) * C::XUnit) >> 4);
             if (elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
@@ -353,52 +362,60 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
                     // 64-wide box and +2048 bytes to the second box
                     const uint32_t step = ONE ? 2 * kk : (kk >> 2) * (kNtok * 128 / 16) + 2 * (kk & 3);
                     umma_bf16_tmem_a(d_tm, a_tm + 8 * kk, b0 + step, idesc, kk > 0 ? 1u : 0u);
-                    if (two) umma_bf16_tmem_a(d_tm + kNtok, a_tm + kACols + 8 * kk, b1 + step, idesc, kk > 0 ? 1u : 0u);
                 }
-                umma_commit(cb + kBarAEmpty + 8 * ap);
+                umma_commit(bar_aempty + 8 * al);
                 umma_commit(cb + kBarDFull + 8 * dp);
-                if (!ONE && (us == kPS - 2 || f + 2 >= n)) umma_commit(bar_empty + 8 * s);
+                if (!ONE && (us >= kPS - 2 || j + 2 >= n)) umma_commit(bar_empty + 8 * s);
             }
             __syncwarp();
-            g = g1 + 1 == G ? 0 : g1 + 1;
-            if (++ap == kAP) {
-                ap = 0;
+            g += g_step;
+            if (g >= G) g -= G;
+            if (++al == kAQ) {
+                al = 0;
                 a_ph ^= 1u;
             }
             if (++dp == kDP) {
                 dp = 0;
                 d_ph ^= 1u;
             }
-            us += 2;
-            if (us == kPS) {
-                us = 0;
-                if (++s == S) {
-                    s = 0;
-                    full_ph ^= 1u;
-                }
+            if (us >= kPS - 2 && ++s == S) {
+                s = 0;
+                full_ph ^= 1u;
             }
         }
-        // every MMA issued has completed before tensor memory is freed
-        if (elect_one()) umma_commit(cb + kBarDrain);
+        // odd n: the last pair has no unit for MMA warp 1, which still
+        // signals its accumulator pair -- after the slot's previous pair has
+        // been consumed, so the arrival cannot count towards that phase
+        if (ok && q == 1 && (n & 1)) {
+            const int32_t k = n >> 1;
+            if (k < kDP || leader_wait(cb + kBarDEmpty + 8 * dp, d_ph ^ 1u, abort_flag, lane)) {
+                if (elect_one()) umma_commit(cb + kBarDFull + 8 * dp);
+                __syncwarp();
+            }
+        }
+        // every MMA this warp issued has completed before tensor memory is freed
+        if (elect_one()) umma_commit(cb + kBarDrain + 8 * q);
         __syncwarp();
         volatile int no_abort = 0;
-        (void)mbar_wait(cb + kBarDrain, 0, &no_abort);
+        (void)mbar_wait(cb + kBarDrain + 8 * q, 0, &no_abort);
     } else if (warp < kDecWarps) {
         // ---------------------------------------------------- decode streams
-        // stream q decodes units j = q, q+2, ... (unit q of pair j/2); its
-        // warpgroup h decodes half h (weights 64h..64h+63 of the unit's 128)
-        const int q = warp >> 3, h = (warp >> 2) & 1;
+        // stream q (one warpgroup) decodes units j = q, q+2, ...: each
+        // thread the 128 weights of its row
+        const int q = warp >> 2;
         const int r = threadIdx.x & 127;   // weight row in the tile = tensor-memory lane
-        const uint32_t tm = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + q * kACols + 32 * h;
-        const int codes_off = C::OffCodes + 2048 * h + 16 * r;   // + unit in stage * 4096
-        int s = 0, ap = 0;
+        const uint32_t tm = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + q * kAQ * kACols;
+        const int codes_off = C::OffCodes + 16 * r;   // + unit in stage * 4096 (+ 2048 second half)
+        const uint32_t bar_afull = cb + kBarAFull + 8 * kAQ * q;
+        const uint32_t bar_aempty = cb + kBarAEmpty + 8 * kAQ * q;
+        int s = 0, al = 0;
         uint32_t full_ph = 0, a_ph = 0;
-        int32_t j = q;
-        for (; j < n; j += 2) {
-            const int32_t k = j >> 1;
+        for (int32_t j = q; j < n; j += 2) {
             const int us = j % kPS;
             if (us < 2 && !warp_wait(bar_full + 8 * s, full_ph, abort_flag)) break;   // first unit of the stage
-            const uint4 c = lds_v4(ring_ptr + s * C::StageBytes + codes_off + us * kUnitCodeBytes);
+            const uint8_t* cp = ring_ptr + s * C::StageBytes + codes_off + us * kUnitCodeBytes;
+            const uint4 c0 = lds_v4(cp);
+            const uint4 c1 = lds_v4(cp + 2048);
             if (us >= kPS - 2 || j + 2 >= n) {   // this stream's last unit of the stage
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_empty + 8 * s);
@@ -407,32 +424,28 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
                     full_ph ^= 1u;
                 }
             }
-            if (k >= kAP) {
-                if (!warp_wait(cb + kBarAEmpty + 8 * ap, a_ph ^ 1u, abort_flag)) break;
+            if (j >= 2 * kAQ) {
+                if (!warp_wait(bar_aempty + 8 * al, a_ph ^ 1u, abort_flag)) break;
                 tc_fence_after_sync();
             }
-            uint32_t p[32];
-            decode_word_bf16(c.x, p);
-            decode_word_bf16(c.y, p + 8);
-            decode_word_bf16(c.z, p + 16);
-            decode_word_bf16(c.w, p + 24);
-            tmem_st_32x32b_x32(tm + 2 * ap * kACols, p);
+            const uint32_t a_tm = tm + al * kACols;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const uint4 c = hh == 0 ? c0 : c1;
+                uint32_t p[32];
+                decode_word_bf16(c.x, p);
+                decode_word_bf16(c.y, p + 8);
+                decode_word_bf16(c.z, p + 16);
+                decode_word_bf16(c.w, p + 24);
+                tmem_st_32x32b_x32(a_tm + 32 * hh, p);
+            }
             tmem_st_wait();
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(cb + kBarAFull + 8 * ap);
-            if (++ap == kAP) {
-                ap = 0;
+            if (lane == 0) mbar_arrive(bar_afull + 8 * al);
+            if (++al == kAQ) {
+                al = 0;
                 a_ph ^= 1u;
-            }
-        }
-        // odd n: the last pair has no unit for stream 1, which still signals
-        // it -- after the slot's previous pair has been consumed, so that the
-        // arrival cannot count towards that pair's phase
-        if (j == n && q == 1 && (n & 1)) {
-            if ((j >> 1) < kAP || warp_wait(cb + kBarAEmpty + 8 * ap, a_ph ^ 1u, abort_flag)) {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(cb + kBarAFull + 8 * ap);
             }
         }
     } else if (warp < kPromWarp0 + 4) {
@@ -592,7 +605,7 @@ StreamPlan plan_stream(int64_t M, int64_t N, int64_t K, int sm_count) {
     p.grid = p.V;
     // M == 1 keeps the activation row in shared memory when at least three
     // stages still fit beside it
-    const int64_t x_smem = round_up(2 * K + 256, 1024);
+    const int64_t x_smem = x_smem_bytes(K);
     const int64_t avail_one = kSmemLimit - 1024 - kCtrlBytes - x_smem;
     p.one = (M == 1) && avail_one >= 3 * SCfg<true>::StageBytes;
     const int64_t stage_bytes = p.one ? SCfg<true>::StageBytes : SCfg<false>::StageBytes;
@@ -618,7 +631,7 @@ cudaError_t launch_stream(const uint16_t* X, int64_t ldx, const uint8_t* tiled, 
     a.G = static_cast<int>(plan.G);
     a.stages = plan.stages;
     a.x_bytes = static_cast<uint32_t>(2 * K);
-    a.x_smem = plan.one ? static_cast<uint32_t>(round_up(2 * K + 256, 1024)) : 0u;
+    a.x_smem = plan.one ? static_cast<uint32_t>(x_smem_bytes(K)) : 0u;
     a.N = N;
     a.R = plan.R;
     a.U = plan.U;
