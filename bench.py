@@ -12,11 +12,19 @@ Reported (one JSON line on rank 0):
   value      effective weight GB/s = algorithmic bytes / step time, where a
              linear moves N*K/4 (codes) + 2*N*K/128 (FP16 scales) +
              2*M*K (bf16 X) + 4*M*N (fp32 Y) bytes
-  roofline   the decode kernel against the measured HBM copy bandwidth
-  prefill    TFLOP/s = 2*M*N*K / time at M = 4096 on one layer's linears
-  repack     GB/s of tern_repack over all 48 layers (disk -> tiled)
+  roofline   the dominant kernel (the streaming kernel at the gate+up shape,
+             launched once per layer back to back): algorithmic bytes per
+             launch / average launch duration, against the measured copy
+             bandwidth; `traffic` is the DRAM bytes per launch from the
+             committed ncu summary while the kernel sources are unchanged
   e2e        the same metric with the step's X copied in from pinned host
              memory and all Y copied back, inside the timed region
+  legs       the other listed configurations, each with its own clock record:
+             27B-class linears one by one at M = 2..16 (GB/s), the stack at
+             M = 32..256 (tokens/s), prefill M = 1024..4096 (TFLOP/s), the
+             0.6B embedding-model layers at M = 1, 32, 512 and the single
+             1024x1024 linear at M = 1, 8
+  repack     GB/s of tern_repack over all 48 layers (disk -> tiled)
   cpu_baseline  the fp64 CPU oracle timed on a bounded sample
 
 `--impl reference` times the CPU oracle alone (the reference arm).
@@ -159,7 +167,7 @@ def build_stack(wl, layers, dev, tb, torch):
 class Step:
     """All linears of the stack at batch M, with X/Y arenas on the device."""
 
-    def __init__(self, wl, layers, M, tiled, dev, tb, torch):
+    def __init__(self, wl, layers, M, tiled, dev, tb, torch, host_copies=True):
         import synth
         self.tb, self.torch = tb, torch
         self.M = M
@@ -173,10 +181,11 @@ class Step:
                 plan.append((layer, lin, x_off, y_off))
                 x_off += x.size
                 y_off += M * lin.N
-        self.x_host = torch.from_numpy(np.concatenate(xs).view(np.int16)).pin_memory()
-        self.x_dev = self.x_host.to(dev)
+        x_host = torch.from_numpy(np.concatenate(xs).view(np.int16))
+        self.x_host = x_host.pin_memory() if host_copies else None
+        self.x_dev = x_host.to(dev)
         self.y_dev = torch.zeros(y_off, dtype=torch.float32, device=dev)
-        self.y_host = torch.empty(y_off, dtype=torch.float32).pin_memory()
+        self.y_host = torch.empty(y_off, dtype=torch.float32).pin_memory() if host_copies else None
         ws_need = 0
         self.bytes = 0
         self.flops = 0
@@ -331,6 +340,143 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ legs
+
+def traffic_from_profile(kernel_files):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, or None if the kernel's sources changed since the capture."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "stream_gate_up_m1.txt")
+    try:
+        lines = open(path).read().splitlines()
+    except OSError:
+        return None, "no profile"
+    kv = {}
+    for ln in lines:
+        if ":" in ln:
+            k, v = ln.split(":", 1)
+            kv[k.strip()] = v.strip()
+    h = hashlib.sha256()
+    for f in kernel_files:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    if kv.get("kernel_sources_sha256") != h.hexdigest():
+        return None, "kernel changed since the capture"
+    try:
+        return int(kv["dram_bytes_per_launch"]), "profiles/stream_gate_up_m1.txt"
+    except (KeyError, ValueError):
+        return None, "no traffic line"
+
+
+KERNEL_FILES = ["ternary_bit_weight_gb300/csrc/tern_stream.cu", "ternary_bit_weight_gb300/csrc/tern_common.cuh",
+                "ternary_bit_weight_gb300/csrc/tern_sm100.cuh"]
+
+
+def timed_region(torch, fn, reps, local, min_ms=300.0):
+    """Run fn() reps times between CUDA events on the current stream (repeating
+    the batch until at least min_ms have elapsed) while sampling clocks;
+    returns (ms per fn call, clocks)."""
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    total_ms, calls = 0.0, 0
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    while total_ms < min_ms or calls == 0:
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        total_ms += e0.elapsed_time(e1)
+        calls += reps
+    clocks = sampler.stop()
+    return total_ms / calls, clocks
+
+
+def leg_stack_batched(wl, layers, tiled, dev, tb, torch, Ms, local):
+    """27B-class stack at continuous-batching sizes: tokens/s per step."""
+    out = {}
+    for M in Ms:
+        st = Step(wl, layers, M, tiled, dev, tb, torch, host_copies=False)
+        g = capture(torch, st.run)
+        for _ in range(2):
+            g.replay()
+        ms, clocks = timed_region(torch, g.replay, 2, local, min_ms=200.0)
+        out[str(M)] = {"ms_per_step": ms, "tokens_per_s": M / (ms / 1e3),
+                       "weight_gbs": st.bytes / (ms / 1e3) / 1e9, "tflops": st.flops / (ms / 1e3) / 1e12,
+                       "clocks": clocks}
+        del g, st
+        torch.cuda.empty_cache()
+    return out
+
+
+def leg_per_linear(wl, layers, tiled, dev, tb, torch, Ms, local):
+    """Each 27B-class linear at batch M, launched once per layer back to back
+    (distinct weights: every launch streams from HBM); average per launch."""
+    import synth
+    out = {}
+    for M in Ms:
+        row = {}
+        for lin in wl.linears:
+            xs = [torch.from_numpy(synth.activations(wl, l, lin, M).view(np.int16)).to(dev) for l in range(layers)]
+            Y = torch.empty((M, lin.N), dtype=torch.float32, device=dev)
+            ws = torch.zeros(max(tb.tern_workspace_bytes(M, lin.N, lin.K), 256), dtype=torch.uint8, device=dev)
+            outs = []
+            off = 0
+            for n in lin.splits:
+                outs.append(Y.data_ptr() + 4 * M * off)
+                off += n
+
+            def one_pass():
+                for l in range(layers):
+                    if len(lin.splits) == 1:
+                        tb.tern_linear(xs[l], lin.K, tiled[(l, lin.name)], M, lin.N, lin.K, Y, lin.N, ws)
+                    else:
+                        tb.tern_linear_multi(xs[l], lin.K, tiled[(l, lin.name)], M, lin.K, list(lin.splits), outs,
+                                             list(lin.splits), ws)
+            one_pass()
+            ms, clocks = timed_region(torch, one_pass, 1, local, min_ms=100.0)
+            us = ms * 1e3 / layers
+            row[lin.name] = {"us": us, "gbs": linear_bytes(M, lin.N, lin.K) / (us * 1e-6) / 1e9,
+                             "tflops": 2 * M * lin.N * lin.K / (us * 1e-6) / 1e12, "clocks": clocks}
+            del xs, Y, ws
+        out[str(M)] = row
+    return out
+
+
+def leg_prefill(wl, tiled, dev, tb, torch, Ms, local):
+    """One layer's four linears at prefill batch sizes: TFLOP/s."""
+    out = {}
+    for M in Ms:
+        st = Step(wl, 1, M, tiled, dev, tb, torch, host_copies=False)
+        st.run()
+        ms, clocks = timed_region(torch, st.run, 2, local, min_ms=200.0)
+        out[str(M)] = {"ms": ms, "tflops": st.flops / (ms / 1e3) / 1e12, "clocks": clocks}
+        del st
+        torch.cuda.empty_cache()
+    return out
+
+
+def leg_workload(name, Ms, dev, tb, torch, local, reps=20):
+    """A small workload end to end (its own weights): per-step time at each M."""
+    import synth
+    wl = synth.WORKLOADS[name]
+    tiled, disk, _, _ = build_stack(wl, wl.layers, dev, tb, torch)
+    del disk
+    out = {}
+    for M in Ms:
+        st = Step(wl, wl.layers, M, tiled, dev, tb, torch, host_copies=False)
+        g = capture(torch, st.run)
+        for _ in range(3):
+            g.replay()
+        ms, clocks = timed_region(torch, g.replay, reps, local, min_ms=100.0)
+        out[str(M)] = {"ms_per_step": ms, "tokens_per_s": M / (ms / 1e3),
+                       "weight_gbs": st.bytes / (ms / 1e3) / 1e9, "clocks": clocks}
+        del g, st
+    del tiled
+    torch.cuda.empty_cache()
+    return out
+
+
 # ------------------------------------------------------------------ main
 
 def main():
@@ -342,8 +488,7 @@ def main():
     ap.add_argument("--workload", default="stack27b")
     ap.add_argument("--layers", type=int, default=48)
     ap.add_argument("--M", type=int, default=1)
-    ap.add_argument("--prefill-M", type=int, default=4096)
-    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-legs", action="store_true", help="only the headline step")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args()
@@ -371,7 +516,7 @@ def main():
     del disk
     torch.cuda.empty_cache()
 
-    # ---- decode step: all linears at batch M, graph-captured
+    # ---- headline: all linears of the stack at batch M, one CUDA graph per step
     step = Step(wl, layers, args.M, tiled, dev, tb, torch)
     graph = capture(torch, step.run)
     sampler = ClockSampler(local)
@@ -392,30 +537,21 @@ def main():
     ms_e2e = time_graph(torch, graph, args.steps, args.warmup, world, before=h2d, after=d2h, stream=cur)
     e2e = {"value": step.bytes / (ms_e2e / 1e3) / 1e9 * world, "unit": "GB/s",
            "h2d_bytes_per_step": step.x_host.numel() * 2, "d2h_bytes_per_step": step.y_host.numel() * 4}
+    del graph
 
-    # ---- per-linear breakdown (event-timed, not graphed): where the time goes
-    per_linear = {}
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in step.calls]
-    torch.cuda.synchronize()
-    for call, (a, b) in zip(step.calls, ev):
-        a.record()
-        step.run_call(call)
-        b.record()
-    torch.cuda.synchronize()
-    for (lin, *_), (a, b) in zip(step.calls, ev):
-        per_linear.setdefault(lin.name, []).append(a.elapsed_time(b) * 1e3)
-    per_linear_us = {k: statistics.median(v) for k, v in per_linear.items()}
-    per_linear_gbs = {lin.name: linear_bytes(args.M, lin.N, lin.K) / (per_linear_us[lin.name] * 1e-6) / 1e9
-                      for lin in wl.linears}
-
-    # roofline of the dominant kernel: the decode kernel is every launch of the
-    # step, so its average launch duration in the timed region is step/launches
-    avg_launch_s = ms / 1e3 / step.launches
-    achieved = step.bytes / step.launches / avg_launch_s / 1e9
+    # ---- the dominant kernel: the streaming kernel at the gate+up shape,
+    # launched once per layer back to back on the current stream; its
+    # average launch duration from CUDA events over those launches
+    gu = next(l for l in wl.linears if l.name == "gate_up")
+    per_lin = leg_per_linear(wl, layers, tiled, dev, tb, torch, [args.M], local)[str(args.M)]
+    avg_s = per_lin["gate_up"]["us"] * 1e-6
+    achieved = linear_bytes(args.M, gu.N, gu.K) / avg_s / 1e9
+    traffic, traffic_src = traffic_from_profile(KERNEL_FILES)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                "frac": achieved / hbm_peak, "traffic": None, "peak_source": peak_src,
-                "kernel": "umma_kernel<16> (tern_linear / tern_linear_multi, M<=16)"}
+                "frac": achieved / hbm_peak, "traffic": traffic, "traffic_source": traffic_src,
+                "peak_source": peak_src + " (copy bandwidth)",
+                "kernel": f"stream_kernel (tern_linear_multi, gate+up {gu.K}->{gu.N}, M={args.M})",
+                "bytes_per_launch": linear_bytes(args.M, gu.N, gu.K), "avg_launch_us": avg_s * 1e6}
 
     out = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -432,29 +568,29 @@ def main():
         "e2e": e2e,
         "gpu_launches": step.launches * args.steps,
         "clocks": clocks,
-        "per_linear_us": per_linear_us,
-        "per_linear_gbs": per_linear_gbs,
+        "per_linear_M1": {k: {"us": v["us"], "gbs": v["gbs"]} for k, v in per_lin.items()},
         "repack": {"gbs": repack_bytes / repack_s / 1e9, "layers": layers,
                    "bytes": repack_bytes, "ms": repack_s * 1e3},
     }
+    del step
+    torch.cuda.empty_cache()
 
-    # ---- prefill: one layer's linears at M = prefill_M
-    if not args.no_prefill:
-        del graph
-        pstep = Step(wl, 1, args.prefill_M, tiled, dev, tb, torch)
-        pstep.run()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        reps = 3
-        e0.record()
-        for _ in range(reps):
-            pstep.run()
-        e1.record()
-        torch.cuda.synchronize()
-        pms = e0.elapsed_time(e1) / reps
-        tflops = pstep.flops / (pms / 1e3) / 1e12
-        out["prefill"] = {"M": args.prefill_M, "ms": pms, "tflops": tflops,
-                          "frac": tflops / bf16_peak, "peak_tflops": bf16_peak,
+    # ---- the other listed configurations, each with its own clock record
+    if not args.no_legs and world == 1:
+        legs = {}
+        legs["dec27b_per_linear"] = leg_per_linear(wl, layers, tiled, dev, tb, torch, [2, 4, 8, 16], local)
+        legs["stack27b_batched"] = leg_stack_batched(wl, layers, tiled, dev, tb, torch, [32, 64, 128, 256], local)
+        legs["prefill27b"] = leg_prefill(wl, tiled, dev, tb, torch, [1024, 2048, 4096], local)
+        for v in legs["prefill27b"].values():
+            v["frac_of_bf16_peak"] = v["tflops"] / bf16_peak
+        del tiled
+        torch.cuda.empty_cache()
+        legs["embed06b"] = leg_workload("embed06b", [1, 32, 512], dev, tb, torch, local)
+        legs["single"] = leg_workload("single", [1, 8], dev, tb, torch, local, reps=200)
+        legs["single"]["note"] = "one 1024x1024 linear: 0.28 MB of weights, L2-resident and launch-bound"
+        out["legs"] = legs
+        out["prefill"] = {"M": 4096, "tflops": legs["prefill27b"]["4096"]["tflops"],
+                          "frac": legs["prefill27b"]["4096"]["tflops"] / bf16_peak, "peak_tflops": bf16_peak,
                           "peak_source": peak_src, "linears": "layer 0: qkv, o, gate_up, down"}
 
     # ---- CPU baseline: the oracle on a bounded sample (rank 0 only)

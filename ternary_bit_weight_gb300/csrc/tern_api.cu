@@ -32,9 +32,9 @@ tern_status run_linear(const uint16_t* X, int64_t ldx, const void* tiled, int64_
         if (ws_bytes < plan.ws_bytes) return TERN_ERR_SIZE;
         e = tern::launch_stream(X, ldx, w, M, N, K, out, ws, plan, stream);
     } else {
-        const tern::UmmaPlan plan = tern::plan_umma(M, N, K, sms);
+        const tern::GemmPlan plan = tern::plan_gemm(M, N, K, sms);
         if (ws_bytes < plan.ws_bytes) return TERN_ERR_SIZE;
-        e = tern::launch_umma(X, ldx, w, M, N, K, out, ws, plan, stream);
+        e = tern::launch_gemm(X, ldx, w, M, N, K, out, ws, plan, stream);
     }
     return e == cudaSuccess ? TERN_OK : TERN_ERR_CUDA;
 }
@@ -42,7 +42,7 @@ tern_status run_linear(const uint16_t* X, int64_t ldx, const void* tiled, int64_
 size_t workspace_bytes(int64_t M, int64_t N, int64_t K) {
     const int sms = tern::device_sm_count();
     if (M <= tern::kStreamMaxM) return tern::plan_stream(M, N, K, sms).ws_bytes;
-    return tern::plan_umma(M, N, K, sms).ws_bytes;
+    return tern::plan_gemm(M, N, K, sms).ws_bytes;
 }
 
 tern_status check_x_w(const uint16_t* X, int64_t ldx, const void* tiled, int64_t M, int64_t K) {

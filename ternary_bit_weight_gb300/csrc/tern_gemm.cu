@@ -1,0 +1,644 @@
+// Tensor-core GEMM of libtern for M > 16 tokens (batched decode, prefill):
+//   Y[M,N] = X[M,K] . (s (.) T)^T
+//
+// Method ("Ternary embedding model in vLLM", 2kiu.com/news/5082861, §4.2):
+// the packed weights are dequantised tile by tile on chip and fed to the
+// tensor cores (the page's "dequantise, then a dense GEMM" route, with the
+// dequantisation fused into the GEMM instead of materialising W).
+//
+// Exactness: the dequantised weight t * s is exactly representable in fp16
+// (t in {-1,0,+1}, s an FP16 scale).  The activations are converted once by
+// `xprep_kernel` to fp16 after scaling each token row by a power of two
+// 2^c_m chosen so that its largest magnitude lies in [2^14, 2^15): every
+// bf16 value at most 2^-32 of the row's maximum converts exactly.  The
+// products are then exact in fp32 and the whole K range accumulates in fp32
+// in tensor memory; the epilogue multiplies by 2^-c_m (exact).
+//
+// Work item = 256 weight rows (two 128-row tiles) x NT tokens x a range of
+// 128-wide groups along K.  Both row tiles share every activation tile,
+// halving the activation traffic per flop.  Warp roles of the persistent
+// CTA (one per SM):
+//   * producer warp: weights by bulk copy, 4 groups per copy per row tile;
+//     activations by one 3-D TMA copy of 2 groups (4 chunks of 64 along K,
+//     128-byte swizzle) -- a CTA's copy engine completes only a few copies
+//     per microsecond, so copies are few and large;
+//   * two decode warpgroups, one per row tile (one thread per weight row =
+//     one tensor-memory lane): code word -> exact fp16 t (LOP3 + FMA), times
+//     the row's scale (one multiply) -> tcgen05.st into a 2-unit A ring;
+//   * MMA warp (warp-uniform loop, one elected lane issues): per group and
+//     row tile eight tcgen05.mma (M = 128, N = NT, K = 16, f16 -> fp32);
+//   * epilogue warpgroup: tcgen05.ld of both accumulators, times 2^-c_m,
+//     stores (or, when K is split across items, a partial summed in split
+//     order by the last item of the tile to arrive).
+// Every wait is bounded; a timeout raises the workspace error word.
+
+#include <cuda.h>
+
+#include <mutex>
+
+#include "tern_common.cuh"
+#include "tern_internal.h"
+#include "tern_sm100.cuh"
+
+namespace tern {
+namespace {
+
+constexpr int kDecWarps = 8;                    // warpgroup r decodes row tile r of the pair
+constexpr int kEpiWarp0 = kDecWarps;            // 4 warps
+constexpr int kProducerWarp = kEpiWarp0 + 4;
+constexpr int kMmaWarp = kProducerWarp + 1;
+constexpr int kThreads = (kMmaWarp + 1) * 32;
+constexpr int kMaxNT = 128;                     // tokens per tile (UMMA N)
+constexpr int kTmemCols = 512;
+constexpr int kACols = 64;                      // one unit of fp16 A (128 per row)
+constexpr int kAU = 2;                          // A ring per row tile
+constexpr int kDCol0 = 2 * kAU * kACols;        // two accumulators of NT columns
+static_assert(kDCol0 + 2 * kMaxNT <= kTmemCols, "tensor-memory budget");
+constexpr int kWG = 4;                          // groups per weight stage
+constexpr int kWS = 2;                          // weight stages
+constexpr int kXG = 2;                          // groups per activation stage (one TMA copy)
+constexpr int kXS = 2;                          // activation stages
+constexpr int kXStageMax = kXG * 2 * kMaxNT * 128;          // 2 chunks of 64 per group
+constexpr int kWStage = 2 * kWG * kUnitBytes;              // both row tiles
+constexpr int kCtrlBytes = 1024;
+constexpr int kSmemBytes = 1024 + kXS * kXStageMax + kWS * kWStage + kCtrlBytes;
+static_assert(kSmemBytes <= 232448, "shared-memory budget");
+
+// control block offsets
+constexpr int kBarXFull = 0;                                 // [kXS]
+constexpr int kBarXEmpty = kBarXFull + 8 * kXS;              // [kXS]
+constexpr int kBarWFull = kBarXEmpty + 8 * kXS;              // [kWS]
+constexpr int kBarWEmpty = kBarWFull + 8 * kWS;              // [kWS]
+constexpr int kBarAFull = kBarWEmpty + 8 * kWS;              // [2][kAU]
+constexpr int kBarAEmpty = kBarAFull + 8 * 2 * kAU;          // [2][kAU]
+constexpr int kBarDFull = kBarAEmpty + 8 * 2 * kAU;
+constexpr int kBarDEmpty = kBarDFull + 8;
+constexpr int kBarDrain = kBarDEmpty + 8;
+constexpr int kTmemPtr = kBarDrain + 8;
+constexpr int kAbort = kTmemPtr + 4;
+static_assert(kAbort + 4 <= kCtrlBytes, "control block");
+
+struct GemmArgs {
+    const uint8_t* codes;
+    const uint8_t* scales;
+    const float* inv_scale;    // [M]: 2^-c_m
+    int M;
+    int NT;                    // tokens per tile
+    int G;                     // groups along K
+    int R;                     // 128-row tiles
+    int RP;                    // pairs of row tiles
+    int T;                     // token tiles
+    int KS;                    // splits of K
+    int64_t N;
+    int64_t items;             // RP * T * KS
+    OutputSplit out;
+    int* err;
+    int* counters;             // [RP * T]
+    float* partial;            // [RP * T][KS][2][NT][128]
+};
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+    const bool got = mbar_wait(bar, parity, abort);
+    return __all_sync(0xffffffffu, got);
+}
+
+__device__ __forceinline__ bool leader_wait(uint32_t bar, uint32_t parity, volatile int* abort, int lane) {
+    uint32_t got = 1;
+    if (lane == 0) got = mbar_wait(bar, parity, abort) ? 1u : 0u;
+    return __shfl_sync(0xffffffffu, got, 0) != 0;
+}
+
+// 3-D TMA load (coordinates c0 innermost).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int32_t c0, int32_t c1, int32_t c2,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+
+// Item i -> (row-tile pair, token tile, K split), token tile slowest so that
+// the CTAs working at the same time share activation tiles in L2.
+struct Item {
+    int bp, n, ks;
+};
+__device__ __forceinline__ Item item_of(const GemmArgs& a, int64_t i) {
+    Item it;
+    it.ks = static_cast<int>(i % a.KS);
+    const int64_t t = i / a.KS;
+    it.bp = static_cast<int>(t % a.RP);
+    it.n = static_cast<int>(t / a.RP);
+    return it;
+}
+__device__ __forceinline__ void group_range(const GemmArgs& a, int ks, int& g0, int& g1) {
+    g0 = static_cast<int>((int64_t)a.G * ks / a.KS);
+    g1 = static_cast<int>((int64_t)a.G * (ks + 1) / a.KS);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_u32 = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);
+    const uint32_t sbase = smem_u32(smem);
+    const int NT = a.NT;
+    const int x_stage = kXG * 2 * NT * 128;       // bytes of one activation stage
+    const uint32_t xring = sbase;
+    const uint32_t wring = sbase + kXS * kXStageMax;
+    uint8_t* wring_ptr = smem + kXS * kXStageMax;
+    uint8_t* ctrl = smem + kXS * kXStageMax + kWS * kWStage;
+    const uint32_t cb = smem_u32(ctrl);
+    uint32_t* tmem_base_ptr = reinterpret_cast<uint32_t*>(ctrl + kTmemPtr);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(ctrl + kAbort);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kXS; ++i) {
+            mbar_init(cb + kBarXFull + 8 * i, 1);
+            mbar_init(cb + kBarXEmpty + 8 * i, 1);   // MMA commit
+        }
+        for (int i = 0; i < kWS; ++i) {
+            mbar_init(cb + kBarWFull + 8 * i, 1);
+            mbar_init(cb + kBarWEmpty + 8 * i, kDecWarps);
+        }
+        for (int i = 0; i < 2 * kAU; ++i) {
+            mbar_init(cb + kBarAFull + 8 * i, 4);
+            mbar_init(cb + kBarAEmpty + 8 * i, 1);
+        }
+        mbar_init(cb + kBarDFull, 1);
+        mbar_init(cb + kBarDEmpty, 4);
+        mbar_init(cb + kBarDrain, 1);
+        *abort_flag = 0;
+        mbar_fence_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_base_ptr), kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == kProducerWarp && lane == 0) prefetch_tensormap(&xmap);
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_base_ptr;
+    grid_launch_dependents();
+
+    if (warp == kProducerWarp) {
+        // ---------------------------------------------------------- producer
+        grid_dependency_wait();   // the converted activations come from the kernel before
+        int xs = 0, ws = 0;
+        uint32_t x_round = 0, w_round = 0;
+        int64_t xcount = 0, wcount = 0;
+        for (int64_t i = blockIdx.x; i < a.items; i += gridDim.x) {
+            const Item it = item_of(a, i);
+            int g0, g1;
+            group_range(a, it.ks, g0, g1);
+            const bool two = 2 * it.bp + 1 < a.R;
+            bool ok = true;
+            for (int g = g0; g < g1 && ok; ++g) {
+                if ((g - g0) % kWG == 0) {   // weights of up to kWG groups, both row tiles
+                    if (wcount >= kWS && !(ok = warp_wait(cb + kBarWEmpty + 8 * ws, (w_round - 1) & 1u, abort_flag))) break;
+                    const int cnt = g1 - g < kWG ? g1 - g : kWG;
+                    const uint32_t st = wring + ws * kWStage;
+                    if (elect_one()) {
+                        mbar_arrive_expect_tx(cb + kBarWFull + 8 * ws, (two ? 2 : 1) * cnt * kUnitBytes);
+#pragma unroll
+                        for (int rt = 0; rt < 2; ++rt) {
+                            if (rt == 1 && !two) break;
+                            const int64_t u = (int64_t)(2 * it.bp + rt) * a.G + g;
+                            bulk_load(st + rt * kWG * kUnitCodeBytes, a.codes + u * kUnitCodeBytes, cnt * kUnitCodeBytes,
+                                      cb + kBarWFull + 8 * ws);
+                            bulk_load(st + 2 * kWG * kUnitCodeBytes + rt * kWG * kUnitScaleBytes,
+                                      a.scales + u * kUnitScaleBytes, cnt * kUnitScaleBytes, cb + kBarWFull + 8 * ws);
+                        }
+                    }
+                    __syncwarp();
+                    ++wcount;
+                    if (++ws == kWS) {
+                        ws = 0;
+                        ++w_round;
+                    }
+                }
+                if ((g - g0) % kXG == 0) {   // activations of up to kXG groups: 4 chunks of 64 along K
+                    if (xcount >= kXS && !(ok = warp_wait(cb + kBarXEmpty + 8 * xs, (x_round - 1) & 1u, abort_flag))) break;
+                    if (elect_one()) {
+                        mbar_arrive_expect_tx(cb + kBarXFull + 8 * xs, x_stage);
+                        tma_load_3d(xring + xs * kXStageMax, &xmap, 0, it.n * NT, 2 * g, cb + kBarXFull + 8 * xs);
+                    }
+                    __syncwarp();
+                    ++xcount;
+                    if (++xs == kXS) {
+                        xs = 0;
+                        ++x_round;
+                    }
+                }
+            }
+            if (!ok) break;
+        }
+        if (*abort_flag) {
+            volatile int no_abort = 0;
+            for (int t = 0; t < kXS; ++t) {
+                (void)mbar_wait(cb + kBarXFull + 8 * t, 0, &no_abort);
+                (void)mbar_wait(cb + kBarXFull + 8 * t, 1, &no_abort);
+            }
+            for (int t = 0; t < kWS; ++t) {
+                (void)mbar_wait(cb + kBarWFull + 8 * t, 0, &no_abort);
+                (void)mbar_wait(cb + kBarWFull + 8 * t, 1, &no_abort);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // --------------------------------------------------------------- MMA
+        const uint32_t idesc = idesc_fp16_f32(128, static_cast<uint32_t>(NT));
+        const uint64_t bdesc0 = smem_desc_kmajor_sw128(xring);
+        int xs = 0, al0 = 0, al1 = 0;       // A slots of row tile 0 and 1 (tile 1 may be absent)
+        uint32_t x_ph = 0, a_ph0 = 0, a_ph1 = 0;
+        uint32_t d_round = 0;
+        bool ok = true;
+        for (int64_t i = blockIdx.x; i < a.items && ok; i += gridDim.x) {
+            const Item it = item_of(a, i);
+            int g0, g1;
+            group_range(a, it.ks, g0, g1);
+            const bool two = 2 * it.bp + 1 < a.R;
+            // the accumulators are free once the epilogue has read the last item's
+            if (d_round > 0 && !(ok = leader_wait(cb + kBarDEmpty, (d_round - 1) & 1u, abort_flag, lane))) break;
+            for (int g = g0; g < g1; ++g) {
+                const int xg = (g - g0) % kXG;
+                if (xg == 0 && !(ok = leader_wait(cb + kBarXFull + 8 * xs, x_ph, abort_flag, lane))) break;
+                ok = leader_wait(cb + kBarAFull + 8 * al0, a_ph0, abort_flag, lane) &&
+                     (!two || leader_wait(cb + kBarAFull + 8 * (kAU + al1), a_ph1, abort_flag, lane));
+                if (!ok) break;
+                tc_fence_after_sync();
+                // chunk 2*xg (+1) of the stage; +32 bytes per K-step inside a chunk
+                const uint64_t b0 = bdesc0 + ((uint32_t)(xs * kXStageMax + 2 * xg * NT * 128) >> 4);
+                if (elect_one()) {
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint64_t bdesc = b0 + (uint32_t)((kk >> 2) * (NT * 128 / 16)) + 2 * (kk & 3);
+                        const uint32_t acc = (g > g0 || kk > 0) ? 1u : 0u;
+                        umma_bf16_tmem_a(tmem + kDCol0, tmem + al0 * kACols + 8 * kk, bdesc, idesc, acc);
+                        if (two) umma_bf16_tmem_a(tmem + kDCol0 + NT, tmem + (kAU + al1) * kACols + 8 * kk, bdesc, idesc, acc);
+                    }
+                    umma_commit(cb + kBarAEmpty + 8 * al0);
+                    if (two) umma_commit(cb + kBarAEmpty + 8 * (kAU + al1));
+                    if (xg == kXG - 1 || g == g1 - 1) umma_commit(cb + kBarXEmpty + 8 * xs);
+                    if (g == g1 - 1) umma_commit(cb + kBarDFull);
+                }
+                __syncwarp();
+                if (++al0 == kAU) {
+                    al0 = 0;
+                    a_ph0 ^= 1u;
+                }
+                if (two && ++al1 == kAU) {
+                    al1 = 0;
+                    a_ph1 ^= 1u;
+                }
+                if (xg == kXG - 1 || g == g1 - 1) {
+                    if (++xs == kXS) {
+                        xs = 0;
+                        x_ph ^= 1u;
+                    }
+                }
+            }
+            ++d_round;
+        }
+        if (elect_one()) umma_commit(cb + kBarDrain);
+        __syncwarp();
+        volatile int no_abort = 0;
+        (void)mbar_wait(cb + kBarDrain, 0, &no_abort);
+    } else if (warp < kDecWarps) {
+        // ------------------------------------------------------------ decode
+        const int rt = warp >> 2;                       // row tile of the pair
+        const int r = threadIdx.x & 127;                // weight row in the tile = tensor-memory lane
+        const uint32_t tm = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + rt * kAU * kACols;
+        const uint32_t bar_afull = cb + kBarAFull + 8 * rt * kAU;
+        const uint32_t bar_aempty = cb + kBarAEmpty + 8 * rt * kAU;
+        int ws = 0, al = 0;
+        uint32_t w_ph = 0, a_ph = 0;
+        int64_t acount = 0;
+        bool ok = true;
+        for (int64_t i = blockIdx.x; i < a.items && ok; i += gridDim.x) {
+            const Item it = item_of(a, i);
+            int g0, g1;
+            group_range(a, it.ks, g0, g1);
+            const bool mine = rt == 0 || 2 * it.bp + 1 < a.R;
+            for (int g = g0; g < g1; ++g) {
+                const int wg = (g - g0) % kWG;
+                if (wg == 0 && !(ok = warp_wait(cb + kBarWFull + 8 * ws, w_ph, abort_flag))) break;
+                if (mine) {
+                    const uint8_t* st = wring_ptr + ws * kWStage;
+                    const uint4 c0 = lds_v4(st + rt * kWG * kUnitCodeBytes + wg * kUnitCodeBytes + 16 * r);
+                    const uint4 c1 = lds_v4(st + rt * kWG * kUnitCodeBytes + wg * kUnitCodeBytes + 2048 + 16 * r);
+                    const uint32_t sb = *reinterpret_cast<const uint16_t*>(
+                        st + 2 * kWG * kUnitCodeBytes + rt * kWG * kUnitScaleBytes + wg * kUnitScaleBytes + 2 * r);
+                    const uint32_t s2 = sb | (sb << 16);
+                    if (acount >= kAU) {
+                        if (!(ok = warp_wait(bar_aempty + 8 * al, a_ph ^ 1u, abort_flag))) break;
+                        tc_fence_after_sync();
+                    }
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const uint4 c = hh == 0 ? c0 : c1;
+                        uint32_t p[32];
+                        decode_word_fp16_scaled(c.x, s2, p);
+                        decode_word_fp16_scaled(c.y, s2, p + 8);
+                        decode_word_fp16_scaled(c.z, s2, p + 16);
+                        decode_word_fp16_scaled(c.w, s2, p + 24);
+                        tmem_st_32x32b_x32(tm + al * kACols + 32 * hh, p);
+                    }
+                    tmem_st_wait();
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_afull + 8 * al);
+                    ++acount;
+                    if (++al == kAU) {
+                        al = 0;
+                        a_ph ^= 1u;
+                    }
+                }
+                if (wg == kWG - 1 || g == g1 - 1) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(cb + kBarWEmpty + 8 * ws);
+                    if (++ws == kWS) {
+                        ws = 0;
+                        w_ph ^= 1u;
+                    }
+                }
+            }
+        }
+    } else if (warp < kEpiWarp0 + 4) {
+        // ---------------------------------------------------------- epilogue
+        const int r = threadIdx.x & 127;
+        const uint32_t tm = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + kDCol0;
+        grid_dependency_wait();   // outputs and workspace belong to earlier kernels until now
+        uint32_t d_ph = 0;
+        for (int64_t i = blockIdx.x; i < a.items; i += gridDim.x) {
+            const Item it = item_of(a, i);
+            // the four warps decide together (they meet at barrier 1 below)
+            const bool got = warp_wait(cb + kBarDFull, d_ph, abort_flag);
+            if (named_barrier_or(1, 128, !got)) break;
+            d_ph ^= 1u;
+            tc_fence_after_sync();
+            const int m0 = it.n * NT;
+            const int mvalid = a.M - m0 < NT ? a.M - m0 : NT;
+            const bool two = 2 * it.bp + 1 < a.R;
+            const int64_t tile = (int64_t)it.n * a.RP + it.bp;
+            if (a.KS == 1) {
+                // final values straight from tensor memory
+                for (int rt = 0; rt < 2; ++rt) {
+                    if (rt == 1 && !two) break;
+                    const int64_t row = (int64_t)(2 * it.bp + rt) * kTileRows + r;
+                    for (int c = 0; c < NT; c += 16) {
+                        uint32_t d[16];
+                        tmem_ld_32x32b_x16(tm + rt * NT + c, d);
+                        tmem_ld_wait();
+                        if (row < a.N)
+#pragma unroll
+                            for (int m = 0; m < 16; ++m)
+                                if (c + m < mvalid) store_y(a.out, m0 + c + m, row, __uint_as_float(d[m]) * __ldg(a.inv_scale + m0 + c + m));
+                    }
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(cb + kBarDEmpty);
+            } else {
+                // publish this split's partial; the last split of the tile sums
+                // all partials in split order
+                float* base = a.partial + (tile * a.KS + it.ks) * (2 * (int64_t)NT * kTileRows);
+                for (int rt = 0; rt < 2; ++rt) {
+                    if (rt == 1 && !two) break;
+                    for (int c = 0; c < NT; c += 16) {
+                        uint32_t d[16];
+                        tmem_ld_32x32b_x16(tm + rt * NT + c, d);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int m = 0; m < 16; ++m) base[((int64_t)rt * NT + c + m) * kTileRows + r] = __uint_as_float(d[m]);
+                    }
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(cb + kBarDEmpty);
+                // every epilogue thread's partial is visible GPU-wide before the count
+                __threadfence();
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+                __shared__ int last_flag;
+                if (r == 0) {
+                    __threadfence();
+                    last_flag = atomicAdd(a.counters + tile, 1) == a.KS - 1;
+                    if (last_flag) __threadfence();
+                }
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+                if (last_flag) {
+                    // 16 columns at a time: the loads of a split are independent
+                    const float* tb = a.partial + tile * a.KS * (2 * (int64_t)NT * kTileRows);
+                    for (int rt = 0; rt < 2; ++rt) {
+                        if (rt == 1 && !two) break;
+                        const int64_t row = (int64_t)(2 * it.bp + rt) * kTileRows + r;
+                        for (int c = 0; c < mvalid; c += 16) {
+                            float v[16];
+#pragma unroll
+                            for (int m = 0; m < 16; ++m) v[m] = 0.f;
+                            for (int k = 0; k < a.KS; ++k) {
+                                const float* src = tb + ((int64_t)k * 2 * NT + rt * NT + c) * kTileRows + r;
+#pragma unroll
+                                for (int m = 0; m < 16; ++m) v[m] += __ldcg(src + m * kTileRows);
+                            }
+                            if (row < a.N)
+#pragma unroll
+                                for (int m = 0; m < 16; ++m)
+                                    if (c + m < mvalid) store_y(a.out, m0 + c + m, row, v[m] * __ldg(a.inv_scale + m0 + c + m));
+                        }
+                    }
+                    if (r == 0) a.counters[tile] = 0;   // leave the workspace zeroed
+                }
+            }
+        }
+    }
+
+    // ------------------------------------------------------------ teardown
+    tc_fence_before_sync();
+    __syncthreads();
+    if (*abort_flag && threadIdx.x == 0) atomicOr(a.err, 1);
+    if (warp == 0) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// Activation rows -> fp16 scaled by 2^c_m (largest magnitude in [2^14,
+// 2^15)), and 2^-c_m per row.  One CTA per row.
+__global__ void __launch_bounds__(256) xprep_kernel(const uint16_t* __restrict__ X, int64_t ldx, int K,
+                                                     __half* __restrict__ X16, float* __restrict__ inv_scale) {
+    const int m = blockIdx.x;
+    const uint16_t* xr = X + (int64_t)m * ldx;
+    __half* yr = X16 + (int64_t)m * K;
+    grid_dependency_wait();
+    float mx = 0.f;
+    for (int k = threadIdx.x * 8; k < K; k += 256 * 8) {
+        const uint4 v = *reinterpret_cast<const uint4*>(xr + k);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            mx = fmaxf(mx, fabsf(__uint_as_float(w[i] << 16)));
+            mx = fmaxf(mx, fabsf(__uint_as_float(w[i] & 0xFFFF0000u)));
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    __shared__ float wmax[8];
+    if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    mx = wmax[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) mx = fmaxf(mx, wmax[i]);
+    // exponent of the largest magnitude; c brings it to 2^14
+    int c = 0;
+    if (mx > 0.f && mx < INFINITY) {
+        const int e = static_cast<int>((__float_as_uint(mx) >> 23) & 0xFF) - 127;   // floor(log2), normal mx
+        c = 14 - e;
+        if (c > 120) c = 120;
+        if (c < -120) c = -120;
+    }
+    const float scale = __uint_as_float(static_cast<uint32_t>(127 + c) << 23);
+    if (threadIdx.x == 0) inv_scale[m] = __uint_as_float(static_cast<uint32_t>(127 - c) << 23);
+    for (int k = threadIdx.x * 8; k < K; k += 256 * 8) {
+        const uint4 v = *reinterpret_cast<const uint4*>(xr + k);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __half lo = __float2half_rn(__uint_as_float(w[i] << 16) * scale);
+            const __half hi = __float2half_rn(__uint_as_float(w[i] & 0xFFFF0000u) * scale);
+            o[i] = static_cast<uint32_t>(__half_as_ushort(lo)) | (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
+        }
+        *reinterpret_cast<uint4*>(yr + k) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    grid_launch_dependents();
+}
+
+// ---------------------------------------------------------------- host
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+cudaError_t set_smem_limit() {
+    static cudaError_t status = cudaErrorUnknown;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        status = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    });
+    return status;
+}
+
+}  // namespace
+
+GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sm_count) {
+    GemmPlan p = {};
+    if (sm_count <= 0) sm_count = 152;
+    p.R = ceil_div(N, kTileRows);
+    p.RP = ceil_div(p.R, 2);
+    p.G = K / kGroup;
+    p.T = ceil_div(M, kMaxNT);
+    p.NT = static_cast<int>(round_up(ceil_div(M, p.T), 16));
+    // split K when there are too few (row pair, token tile) items to fill
+    // the SMs: as many splits as one wave holds, each at least 4 groups long
+    const int64_t tiles = p.RP * p.T;
+    int64_t ks = tiles < sm_count ? sm_count / tiles : 1;
+    if (ks > p.G / 4) ks = p.G / 4;
+    if (ks < 1) ks = 1;
+    p.KS = ks;
+    p.items = tiles * ks;
+    p.grid = p.items < sm_count ? p.items : sm_count;
+    // workspace: error word | X16 [M][K] fp16 | 2^-c per row | tile counters | split partials
+    size_t off = kWorkspaceErrBytes;
+    p.off_x16 = off;
+    off += round_up(M * K * 2, 1024);
+    p.off_inv = off;
+    off += round_up(M * 4, 256);
+    p.off_counters = off;
+    off += round_up(tiles * 4, 256);
+    p.off_partial = off;
+    if (p.KS > 1) off += static_cast<size_t>(tiles * p.KS * 2 * p.NT * kTileRows) * sizeof(float);
+    p.ws_bytes = off;
+    return p;
+}
+
+cudaError_t launch_gemm(const uint16_t* X, int64_t ldx, const uint8_t* tiled, int64_t M, int64_t N, int64_t K,
+                        const OutputSplit& out, void* ws, const GemmPlan& plan, cudaStream_t stream) {
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    __half* x16 = reinterpret_cast<__half*>(w + plan.off_x16);
+    float* inv = reinterpret_cast<float*>(w + plan.off_inv);
+    // activations -> fp16 (programmatic dependent launch: waits for the kernel before)
+    {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(M));
+        cfg.blockDim = dim3(256);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, xprep_kernel, X, ldx, static_cast<int>(K), x16, inv);
+        if (e != cudaSuccess) return e;
+    }
+    EncodeTiledFn enc = encode_tiled_fn();
+    if (enc == nullptr) return cudaErrorNotSupported;
+    // X16 viewed as [K/64 chunks][M rows][64]: one box = 64 x NT x 4 chunks
+    CUtensorMap map;
+    const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(K / 64)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, 128};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(plan.NT), 2 * kXG};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, x16, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+        CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    cudaError_t e = set_smem_limit();
+    if (e != cudaSuccess) return e;
+    GemmArgs a = {};
+    a.codes = tiled;
+    a.scales = tiled + plan.R * plan.G * kUnitCodeBytes;
+    a.inv_scale = inv;
+    a.M = static_cast<int>(M);
+    a.NT = plan.NT;
+    a.G = static_cast<int>(plan.G);
+    a.R = static_cast<int>(plan.R);
+    a.RP = static_cast<int>(plan.RP);
+    a.T = static_cast<int>(plan.T);
+    a.KS = static_cast<int>(plan.KS);
+    a.N = N;
+    a.items = plan.items;
+    a.out = out;
+    a.err = reinterpret_cast<int*>(w);
+    a.counters = reinterpret_cast<int*>(w + plan.off_counters);
+    a.partial = reinterpret_cast<float*>(w + plan.off_partial);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(plan.grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemm_kernel, map, a);
+}
+
+}  // namespace tern

@@ -58,24 +58,25 @@ cudaError_t launch_stream(const uint16_t* X, int64_t ldx, const uint8_t* tiled, 
                           int64_t K, const OutputSplit& out, void* ws, const StreamPlan& plan,
                           cudaStream_t stream);
 
-// Tensor-core (tcgen05) plan for M > kStreamMaxM.
-struct UmmaPlan {
-    int ntok;              // tokens per tile (UMMA N): 16, 32, 64 or 128
+// Tensor-core GEMM plan for M > kStreamMaxM: items of 256 weight rows x NT
+// tokens x a range of groups along K, persistent CTAs.
+struct GemmPlan {
     int64_t R;             // 128-row tiles
-    int64_t G;             // groups per row
-    int64_t token_tiles;
-    int64_t U;             // units = token_tiles x R x G
-    int64_t V;             // workers
-    int64_t grid;          // CTAs
-    size_t smem;           // dynamic shared memory per CTA
-    size_t ws_bytes;       // workspace: error word, tile counters, partial slots
+    int64_t RP;            // pairs of row tiles
+    int64_t G;             // groups along K
+    int64_t T;             // token tiles
+    int NT;                // tokens per tile
+    int64_t KS;            // splits of K
+    int64_t items;
+    int64_t grid;
+    size_t off_x16, off_inv, off_counters, off_partial;   // workspace layout
+    size_t ws_bytes;
 };
 
-UmmaPlan plan_umma(int64_t M, int64_t N, int64_t K, int sm_count);
+GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sm_count);
 
-cudaError_t launch_umma(const uint16_t* X, int64_t ldx, const uint8_t* tiled, int64_t M, int64_t N,
-                        int64_t K, const OutputSplit& out, void* ws, const UmmaPlan& plan,
-                        cudaStream_t stream);
+cudaError_t launch_gemm(const uint16_t* X, int64_t ldx, const uint8_t* tiled, int64_t M, int64_t N, int64_t K,
+                        const OutputSplit& out, void* ws, const GemmPlan& plan, cudaStream_t stream);
 
 // Size of the error word + padding at the start of every linear workspace.
 constexpr size_t kWorkspaceErrBytes = 256;

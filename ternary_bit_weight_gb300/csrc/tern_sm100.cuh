@@ -110,6 +110,23 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// Named barrier `id` (1..15) across `count` threads (a multiple of 32) that
+// also ORs a predicate over them: every thread gets the same answer, so a
+// group of warps can agree to leave a loop together (none is left waiting
+// at a later barrier).
+__device__ __forceinline__ bool named_barrier_or(uint32_t id, uint32_t count, bool pred) {
+    uint32_t any;
+    asm volatile(
+        "{\n\t.reg .pred p, a;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred a, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, a;\n\t}"
+        : "=r"(any)
+        : "r"(pred ? 1u : 0u), "r"(id), "r"(count)
+        : "memory");
+    return any != 0;
+}
+
 // --------------------------------------------------------- async copies
 
 // Contiguous global -> shared copy completing on an mbarrier (16-byte
