@@ -130,4 +130,27 @@ __device__ __forceinline__ void store_y(const OutputSplit& out, int m, int64_t n
         static_cast<float*>(out.y[j])[idx] = v;
 }
 
+// Output row n of the concatenated N: address of element (m = 0, n) and the
+// stride between tokens, so that a thread owning one row stores with one
+// multiply-add per element.
+struct RowOut {
+    char* base;
+    int64_t ld;
+    int bf16;
+};
+__device__ __forceinline__ RowOut row_out(const OutputSplit& out, int64_t n) {
+    const int j = output_of(out, n);
+    RowOut o;
+    o.base = static_cast<char*>(out.y[j]) + (n - out.offset[j]) * (out.bf16 ? 2 : 4);
+    o.ld = out.ldy[j];
+    o.bf16 = out.bf16;
+    return o;
+}
+__device__ __forceinline__ void store_row(const RowOut& o, int m, float v) {
+    if (o.bf16)
+        reinterpret_cast<__nv_bfloat16*>(o.base)[(int64_t)m * o.ld] = __float2bfloat16_rn(v);
+    else
+        reinterpret_cast<float*>(o.base)[(int64_t)m * o.ld] = v;
+}
+
 }  // namespace tern

@@ -45,8 +45,9 @@ namespace {
 
 constexpr int kDecWarps = 8;                    // warpgroup r decodes row tile r of the pair
 constexpr int kEpiWarp0 = kDecWarps;            // 4 warps
-constexpr int kProducerWarp = kEpiWarp0 + 4;
-constexpr int kMmaWarp = kProducerWarp + 1;
+constexpr int kProducerWarp = kEpiWarp0 + 4;    // weights
+constexpr int kXWarp0 = kProducerWarp + 1;      // 2 warps: activation stages, alternately
+constexpr int kMmaWarp = kXWarp0 + 2;
 constexpr int kThreads = (kMmaWarp + 1) * 32;
 constexpr int kMaxNT = 128;                     // tokens per tile (UMMA N)
 constexpr int kTmemCols = 512;
@@ -56,22 +57,23 @@ constexpr int kDCol0 = 2 * kAU * kACols;        // two accumulators of NT column
 static_assert(kDCol0 + 2 * kMaxNT <= kTmemCols, "tensor-memory budget");
 constexpr int kWG = 4;                          // groups per weight stage
 constexpr int kWS = 2;                          // weight stages
-constexpr int kXG = 2;                          // groups per activation stage (one TMA copy)
-constexpr int kXS = 2;                          // activation stages
+constexpr int kXG = 1;                          // groups per activation stage (one TMA copy)
+constexpr int kXS = 4;                          // activation stages; producer warp = stage mod 2
 constexpr int kXStageMax = kXG * 2 * kMaxNT * 128;          // 2 chunks of 64 per group
 constexpr int kWStage = 2 * kWG * kUnitBytes;              // both row tiles
 constexpr int kCtrlBytes = 1024;
 constexpr int kSmemBytes = 1024 + kXS * kXStageMax + kWS * kWStage + kCtrlBytes;
 static_assert(kSmemBytes <= 232448, "shared-memory budget");
+static_assert(kXS % 2 == 0, "each activation stage has one producer warp");
 
 // control block offsets
 constexpr int kBarXFull = 0;                                 // [kXS]
 constexpr int kBarXEmpty = kBarXFull + 8 * kXS;              // [kXS]
 constexpr int kBarWFull = kBarXEmpty + 8 * kXS;              // [kWS]
 constexpr int kBarWEmpty = kBarWFull + 8 * kWS;              // [kWS]
-constexpr int kBarAFull = kBarWEmpty + 8 * kWS;              // [2][kAU]
-constexpr int kBarAEmpty = kBarAFull + 8 * 2 * kAU;          // [2][kAU]
-constexpr int kBarDFull = kBarAEmpty + 8 * 2 * kAU;
+constexpr int kBarAFull = kBarWEmpty + 8 * kWS;              // [kAU], both row tiles
+constexpr int kBarAEmpty = kBarAFull + 8 * kAU;              // [kAU]
+constexpr int kBarDFull = kBarAEmpty + 8 * kAU;
 constexpr int kBarDEmpty = kBarDFull + 8;
 constexpr int kBarDrain = kBarDEmpty + 8;
 constexpr int kTmemPtr = kBarDrain + 8;
@@ -102,10 +104,14 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return __all_sync(0xffffffffu, got);
 }
 
-__device__ __forceinline__ bool leader_wait(uint32_t bar, uint32_t parity, volatile int* abort, int lane) {
-    uint32_t got = 1;
-    if (lane == 0) got = mbar_wait(bar, parity, abort) ? 1u : 0u;
-    return __shfl_sync(0xffffffffu, got, 0) != 0;
+// Each lane with `active` set waits for its own barrier; the warp goes on when
+// all have completed.  The common case (all complete) costs one test and one
+// vote: a wait in the MMA warp is time the tensor pipe stands idle, since the
+// issue of a group's MMAs returns only once the pipe has taken all but the last.
+__device__ __forceinline__ bool vote_wait(uint32_t bar, uint32_t parity, bool active, volatile int* abort) {
+    if (__all_sync(0xffffffffu, !active || mbar_test_wait(bar, parity))) return true;
+    const bool got = !active || mbar_wait(bar, parity, abort);
+    return __all_sync(0xffffffffu, got);
 }
 
 // 3-D TMA load (coordinates c0 innermost).
@@ -116,6 +122,21 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
         : "memory");
+}
+
+// 2^-c_m of C consecutive tokens (the workspace holds at least 32 entries
+// past the last token tile).  Every lane reads the same addresses.
+template <int C>
+__device__ __forceinline__ void load_inv(const float* p, float (&inv)[C]) {
+    const float4* q = reinterpret_cast<const float4*>(p);
+#pragma unroll
+    for (int i = 0; i < C / 4; ++i) {
+        const float4 v = __ldg(q + i);
+        inv[4 * i] = v.x;
+        inv[4 * i + 1] = v.y;
+        inv[4 * i + 2] = v.z;
+        inv[4 * i + 3] = v.w;
+    }
 }
 
 // Item i -> (row-tile pair, token tile, K split), token tile slowest so that
@@ -162,9 +183,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
             mbar_init(cb + kBarWFull + 8 * i, 1);
             mbar_init(cb + kBarWEmpty + 8 * i, kDecWarps);
         }
-        for (int i = 0; i < 2 * kAU; ++i) {
-            mbar_init(cb + kBarAFull + 8 * i, 4);
-            mbar_init(cb + kBarAEmpty + 8 * i, 1);
+        for (int i = 0; i < kAU; ++i) {
+            mbar_init(cb + kBarAFull + 8 * i, kDecWarps);   // both row tiles
+            mbar_init(cb + kBarAEmpty + 8 * i, 1);          // MMA commit
         }
         mbar_init(cb + kBarDFull, 1);
         mbar_init(cb + kBarDEmpty, 4);
@@ -176,7 +197,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
         tmem_alloc(smem_u32(tmem_base_ptr), kTmemCols);
         tmem_relinquish();
     }
-    if (warp == kProducerWarp && lane == 0) prefetch_tensormap(&xmap);
+    if (warp == kXWarp0 && lane == 0) prefetch_tensormap(&xmap);
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
@@ -184,74 +205,89 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
     grid_launch_dependents();
 
     if (warp == kProducerWarp) {
-        // ---------------------------------------------------------- producer
-        grid_dependency_wait();   // the converted activations come from the kernel before
-        int xs = 0, ws = 0;
-        uint32_t x_round = 0, w_round = 0;
-        int64_t xcount = 0, wcount = 0;
-        for (int64_t i = blockIdx.x; i < a.items; i += gridDim.x) {
+        // -------------------------------------------------- weight producer
+        // a CTA's copies complete at a rate per issuing warp, so weights and
+        // activations have their own producer warps
+        int ws = 0;
+        uint32_t w_round = 0;
+        int64_t wcount = 0;
+        bool ok = true;
+        for (int64_t i = blockIdx.x; i < a.items && ok; i += gridDim.x) {
             const Item it = item_of(a, i);
             int g0, g1;
             group_range(a, it.ks, g0, g1);
             const bool two = 2 * it.bp + 1 < a.R;
-            bool ok = true;
-            for (int g = g0; g < g1 && ok; ++g) {
-                if ((g - g0) % kWG == 0) {   // weights of up to kWG groups, both row tiles
-                    if (wcount >= kWS && !(ok = warp_wait(cb + kBarWEmpty + 8 * ws, (w_round - 1) & 1u, abort_flag))) break;
-                    const int cnt = g1 - g < kWG ? g1 - g : kWG;
-                    const uint32_t st = wring + ws * kWStage;
-                    if (elect_one()) {
-                        mbar_arrive_expect_tx(cb + kBarWFull + 8 * ws, (two ? 2 : 1) * cnt * kUnitBytes);
+            for (int g = g0; g < g1; g += kWG) {   // weights of up to kWG groups, both row tiles
+                if (wcount >= kWS && !(ok = warp_wait(cb + kBarWEmpty + 8 * ws, (w_round - 1) & 1u, abort_flag))) break;
+                const int cnt = g1 - g < kWG ? g1 - g : kWG;
+                const uint32_t st = wring + ws * kWStage;
+                if (elect_one()) {
+                    mbar_arrive_expect_tx(cb + kBarWFull + 8 * ws, (two ? 2 : 1) * cnt * kUnitBytes);
 #pragma unroll
-                        for (int rt = 0; rt < 2; ++rt) {
-                            if (rt == 1 && !two) break;
-                            const int64_t u = (int64_t)(2 * it.bp + rt) * a.G + g;
-                            bulk_load(st + rt * kWG * kUnitCodeBytes, a.codes + u * kUnitCodeBytes, cnt * kUnitCodeBytes,
-                                      cb + kBarWFull + 8 * ws);
-                            bulk_load(st + 2 * kWG * kUnitCodeBytes + rt * kWG * kUnitScaleBytes,
-                                      a.scales + u * kUnitScaleBytes, cnt * kUnitScaleBytes, cb + kBarWFull + 8 * ws);
-                        }
-                    }
-                    __syncwarp();
-                    ++wcount;
-                    if (++ws == kWS) {
-                        ws = 0;
-                        ++w_round;
+                    for (int rt = 0; rt < 2; ++rt) {
+                        if (rt == 1 && !two) break;
+                        const int64_t u = (int64_t)(2 * it.bp + rt) * a.G + g;
+                        bulk_load(st + rt * kWG * kUnitCodeBytes, a.codes + u * kUnitCodeBytes, cnt * kUnitCodeBytes,
+                                  cb + kBarWFull + 8 * ws);
+                        bulk_load(st + 2 * kWG * kUnitCodeBytes + rt * kWG * kUnitScaleBytes,
+                                  a.scales + u * kUnitScaleBytes, cnt * kUnitScaleBytes, cb + kBarWFull + 8 * ws);
                     }
                 }
-                if ((g - g0) % kXG == 0) {   // activations of up to kXG groups: 4 chunks of 64 along K
-                    if (xcount >= kXS && !(ok = warp_wait(cb + kBarXEmpty + 8 * xs, (x_round - 1) & 1u, abort_flag))) break;
-                    if (elect_one()) {
-                        mbar_arrive_expect_tx(cb + kBarXFull + 8 * xs, x_stage);
-                        tma_load_3d(xring + xs * kXStageMax, &xmap, 0, it.n * NT, 2 * g, cb + kBarXFull + 8 * xs);
-                    }
-                    __syncwarp();
-                    ++xcount;
-                    if (++xs == kXS) {
-                        xs = 0;
-                        ++x_round;
-                    }
+                __syncwarp();
+                ++wcount;
+                if (++ws == kWS) {
+                    ws = 0;
+                    ++w_round;
                 }
             }
-            if (!ok) break;
         }
         if (*abort_flag) {
             volatile int no_abort = 0;
-            for (int t = 0; t < kXS; ++t) {
-                (void)mbar_wait(cb + kBarXFull + 8 * t, 0, &no_abort);
-                (void)mbar_wait(cb + kBarXFull + 8 * t, 1, &no_abort);
-            }
             for (int t = 0; t < kWS; ++t) {
                 (void)mbar_wait(cb + kBarWFull + 8 * t, 0, &no_abort);
                 (void)mbar_wait(cb + kBarWFull + 8 * t, 1, &no_abort);
             }
         }
+    } else if (warp == kXWarp0 || warp == kXWarp0 + 1) {
+        // ---------------------------------------------- activation producers
+        // activation stage j (over all items' groups, in order) belongs to
+        // producer warp j mod 2; it is stage j mod kXS of the ring
+        const int q = warp - kXWarp0;
+        grid_dependency_wait();   // the converted activations come from the kernel before
+        int64_t j = 0;            // activation stages so far (all producers)
+        bool ok = true;
+        for (int64_t i = blockIdx.x; i < a.items && ok; i += gridDim.x) {
+            const Item it = item_of(a, i);
+            int g0, g1;
+            group_range(a, it.ks, g0, g1);
+            for (int g = g0; g < g1; g += kXG, ++j) {
+                if ((j & 1) != q) continue;
+                const int xs = static_cast<int>(j % kXS);
+                const uint32_t round = static_cast<uint32_t>(j / kXS);
+                if (round > 0 && !(ok = warp_wait(cb + kBarXEmpty + 8 * xs, (round - 1) & 1u, abort_flag))) break;
+                if (elect_one()) {
+                    mbar_arrive_expect_tx(cb + kBarXFull + 8 * xs, x_stage);
+                    tma_load_3d(xring + xs * kXStageMax, &xmap, 0, it.n * NT, 2 * g, cb + kBarXFull + 8 * xs);
+                }
+                __syncwarp();
+            }
+        }
+        if (*abort_flag) {
+            volatile int no_abort = 0;
+            for (int t = q; t < kXS; t += 2) {
+                (void)mbar_wait(cb + kBarXFull + 8 * t, 0, &no_abort);
+                (void)mbar_wait(cb + kBarXFull + 8 * t, 1, &no_abort);
+            }
+        }
     } else if (warp == kMmaWarp) {
         // --------------------------------------------------------------- MMA
+        // per group one vote over: activation stage full (lane 0), A slot of
+        // both row tiles full (lane 1), accumulators drained (lane 2, first
+        // group of an item)
         const uint32_t idesc = idesc_fp16_f32(128, static_cast<uint32_t>(NT));
         const uint64_t bdesc0 = smem_desc_kmajor_sw128(xring);
-        int xs = 0, al0 = 0, al1 = 0;       // A slots of row tile 0 and 1 (tile 1 may be absent)
-        uint32_t x_ph = 0, a_ph0 = 0, a_ph1 = 0;
+        int xs = 0, al = 0;
+        uint32_t x_ph = 0, a_ph = 0;
         uint32_t d_round = 0;
         bool ok = true;
         for (int64_t i = blockIdx.x; i < a.items && ok; i += gridDim.x) {
@@ -259,14 +295,24 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
             int g0, g1;
             group_range(a, it.ks, g0, g1);
             const bool two = 2 * it.bp + 1 < a.R;
-            // the accumulators are free once the epilogue has read the last item's
-            if (d_round > 0 && !(ok = leader_wait(cb + kBarDEmpty, (d_round - 1) & 1u, abort_flag, lane))) break;
             for (int g = g0; g < g1; ++g) {
                 const int xg = (g - g0) % kXG;
-                if (xg == 0 && !(ok = leader_wait(cb + kBarXFull + 8 * xs, x_ph, abort_flag, lane))) break;
-                ok = leader_wait(cb + kBarAFull + 8 * al0, a_ph0, abort_flag, lane) &&
-                     (!two || leader_wait(cb + kBarAFull + 8 * (kAU + al1), a_ph1, abort_flag, lane));
-                if (!ok) break;
+                uint32_t bar = 0, par = 0;
+                bool act = false;
+                if (lane == 0) {
+                    act = xg == 0;
+                    bar = cb + kBarXFull + 8 * xs;
+                    par = x_ph;
+                } else if (lane == 1) {
+                    act = true;
+                    bar = cb + kBarAFull + 8 * al;
+                    par = a_ph;
+                } else if (lane == 2) {
+                    act = g == g0 && d_round > 0;
+                    bar = cb + kBarDEmpty;
+                    par = (d_round - 1) & 1u;
+                }
+                if (!(ok = vote_wait(bar, par, act, abort_flag))) break;
                 tc_fence_after_sync();
                 // chunk 2*xg (+1) of the stage; +32 bytes per K-step inside a chunk
                 const uint64_t b0 = bdesc0 + ((uint32_t)(xs * kXStageMax + 2 * xg * NT * 128) >> 4);
@@ -275,22 +321,17 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint64_t bdesc = b0 + (uint32_t)((kk >> 2) * (NT * 128 / 16)) + 2 * (kk & 3);
                         const uint32_t acc = (g > g0 || kk > 0) ? 1u : 0u;
-                        umma_bf16_tmem_a(tmem + kDCol0, tmem + al0 * kACols + 8 * kk, bdesc, idesc, acc);
-                        if (two) umma_bf16_tmem_a(tmem + kDCol0 + NT, tmem + (kAU + al1) * kACols + 8 * kk, bdesc, idesc, acc);
+                        umma_bf16_tmem_a(tmem + kDCol0, tmem + al * kACols + 8 * kk, bdesc, idesc, acc);
+                        if (two) umma_bf16_tmem_a(tmem + kDCol0 + NT, tmem + (kAU + al) * kACols + 8 * kk, bdesc, idesc, acc);
                     }
-                    umma_commit(cb + kBarAEmpty + 8 * al0);
-                    if (two) umma_commit(cb + kBarAEmpty + 8 * (kAU + al1));
+                    umma_commit(cb + kBarAEmpty + 8 * al);
                     if (xg == kXG - 1 || g == g1 - 1) umma_commit(cb + kBarXEmpty + 8 * xs);
                     if (g == g1 - 1) umma_commit(cb + kBarDFull);
                 }
                 __syncwarp();
-                if (++al0 == kAU) {
-                    al0 = 0;
-                    a_ph0 ^= 1u;
-                }
-                if (two && ++al1 == kAU) {
-                    al1 = 0;
-                    a_ph1 ^= 1u;
+                if (++al == kAU) {
+                    al = 0;
+                    a_ph ^= 1u;
                 }
                 if (xg == kXG - 1 || g == g1 - 1) {
                     if (++xs == kXS) {
@@ -307,11 +348,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
         (void)mbar_wait(cb + kBarDrain, 0, &no_abort);
     } else if (warp < kDecWarps) {
         // ------------------------------------------------------------ decode
+        // both warpgroups keep the A ring's phases even when an item has no
+        // second row tile (they then arrive without decoding)
         const int rt = warp >> 2;                       // row tile of the pair
         const int r = threadIdx.x & 127;                // weight row in the tile = tensor-memory lane
         const uint32_t tm = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + rt * kAU * kACols;
-        const uint32_t bar_afull = cb + kBarAFull + 8 * rt * kAU;
-        const uint32_t bar_aempty = cb + kBarAEmpty + 8 * rt * kAU;
+        const uint32_t bar_afull = cb + kBarAFull;
+        const uint32_t bar_aempty = cb + kBarAEmpty;
         int ws = 0, al = 0;
         uint32_t w_ph = 0, a_ph = 0;
         int64_t acount = 0;
@@ -324,17 +367,21 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
             for (int g = g0; g < g1; ++g) {
                 const int wg = (g - g0) % kWG;
                 if (wg == 0 && !(ok = warp_wait(cb + kBarWFull + 8 * ws, w_ph, abort_flag))) break;
+                uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0;
+                uint32_t s2 = 0;
                 if (mine) {
                     const uint8_t* st = wring_ptr + ws * kWStage;
-                    const uint4 c0 = lds_v4(st + rt * kWG * kUnitCodeBytes + wg * kUnitCodeBytes + 16 * r);
-                    const uint4 c1 = lds_v4(st + rt * kWG * kUnitCodeBytes + wg * kUnitCodeBytes + 2048 + 16 * r);
+                    c0 = lds_v4(st + rt * kWG * kUnitCodeBytes + wg * kUnitCodeBytes + 16 * r);
+                    c1 = lds_v4(st + rt * kWG * kUnitCodeBytes + wg * kUnitCodeBytes + 2048 + 16 * r);
                     const uint32_t sb = *reinterpret_cast<const uint16_t*>(
                         st + 2 * kWG * kUnitCodeBytes + rt * kWG * kUnitScaleBytes + wg * kUnitScaleBytes + 2 * r);
-                    const uint32_t s2 = sb | (sb << 16);
-                    if (acount >= kAU) {
-                        if (!(ok = warp_wait(bar_aempty + 8 * al, a_ph ^ 1u, abort_flag))) break;
-                        tc_fence_after_sync();
-                    }
+                    s2 = sb | (sb << 16);
+                }
+                if (acount >= kAU) {
+                    if (!(ok = warp_wait(bar_aempty + 8 * al, a_ph ^ 1u, abort_flag))) break;
+                    tc_fence_after_sync();
+                }
+                if (mine) {
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
                         const uint4 c = hh == 0 ? c0 : c1;
@@ -346,14 +393,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
                         tmem_st_32x32b_x32(tm + al * kACols + 32 * hh, p);
                     }
                     tmem_st_wait();
-                    tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar_afull + 8 * al);
-                    ++acount;
-                    if (++al == kAU) {
-                        al = 0;
-                        a_ph ^= 1u;
-                    }
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_afull + 8 * al);
+                ++acount;
+                if (++al == kAU) {
+                    al = 0;
+                    a_ph ^= 1u;
                 }
                 if (wg == kWG - 1 || g == g1 - 1) {
                     __syncwarp();
@@ -383,18 +430,24 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
             const bool two = 2 * it.bp + 1 < a.R;
             const int64_t tile = (int64_t)it.n * a.RP + it.bp;
             if (a.KS == 1) {
-                // final values straight from tensor memory
+                // final values straight from tensor memory, 32 tokens per load
                 for (int rt = 0; rt < 2; ++rt) {
                     if (rt == 1 && !two) break;
                     const int64_t row = (int64_t)(2 * it.bp + rt) * kTileRows + r;
-                    for (int c = 0; c < NT; c += 16) {
-                        uint32_t d[16];
-                        tmem_ld_32x32b_x16(tm + rt * NT + c, d);
-                        tmem_ld_wait();
-                        if (row < a.N)
+                    const bool live = row < a.N;
+                    const RowOut o = row_out(a.out, live ? row : 0);
+                    for (int c = 0; c < NT; c += 32) {
+                        float inv[32];
+                        load_inv(a.inv_scale + m0 + c, inv);
+                        uint32_t d[32];
+                        if (c + 32 <= NT)
+                            tmem_ld32_sync(tm + rt * NT + c, d);
+                        else
+                            tmem_ld16_sync(tm + rt * NT + c, d);
+                        if (live)
 #pragma unroll
-                            for (int m = 0; m < 16; ++m)
-                                if (c + m < mvalid) store_y(a.out, m0 + c + m, row, __uint_as_float(d[m]) * __ldg(a.inv_scale + m0 + c + m));
+                            for (int m = 0; m < 32; ++m)
+                                if (c + m < mvalid) store_row(o, m0 + c + m, __uint_as_float(d[m]) * inv[m]);
                     }
                 }
                 tc_fence_before_sync();
@@ -406,12 +459,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
                 float* base = a.partial + (tile * a.KS + it.ks) * (2 * (int64_t)NT * kTileRows);
                 for (int rt = 0; rt < 2; ++rt) {
                     if (rt == 1 && !two) break;
-                    for (int c = 0; c < NT; c += 16) {
-                        uint32_t d[16];
-                        tmem_ld_32x32b_x16(tm + rt * NT + c, d);
-                        tmem_ld_wait();
+                    for (int c = 0; c < NT; c += 32) {
+                        uint32_t d[32];
+                        if (c + 32 <= NT)
+                            tmem_ld32_sync(tm + rt * NT + c, d);
+                        else
+                            tmem_ld16_sync(tm + rt * NT + c, d);
 #pragma unroll
-                        for (int m = 0; m < 16; ++m) base[((int64_t)rt * NT + c + m) * kTileRows + r] = __uint_as_float(d[m]);
+                        for (int m = 0; m < 32; ++m)
+                            if (c + m < NT) base[((int64_t)rt * NT + c + m) * kTileRows + r] = __uint_as_float(d[m]);
                     }
                 }
                 tc_fence_before_sync();
@@ -433,6 +489,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
                     for (int rt = 0; rt < 2; ++rt) {
                         if (rt == 1 && !two) break;
                         const int64_t row = (int64_t)(2 * it.bp + rt) * kTileRows + r;
+                        const bool live = row < a.N;
+                        const RowOut o = row_out(a.out, live ? row : 0);
                         for (int c = 0; c < mvalid; c += 16) {
                             float v[16];
 #pragma unroll
@@ -442,10 +500,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
 #pragma unroll
                                 for (int m = 0; m < 16; ++m) v[m] += __ldcg(src + m * kTileRows);
                             }
-                            if (row < a.N)
+                            float inv[16];
+                            load_inv(a.inv_scale + m0 + c, inv);
+                            if (live)
 #pragma unroll
                                 for (int m = 0; m < 16; ++m)
-                                    if (c + m < mvalid) store_y(a.out, m0 + c + m, row, v[m] * __ldg(a.inv_scale + m0 + c + m));
+                                    if (c + m < mvalid) store_row(o, m0 + c + m, v[m] * inv[m]);
                         }
                     }
                     if (r == 0) a.counters[tile] = 0;   // leave the workspace zeroed
@@ -569,7 +629,7 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sm_count) {
     p.off_x16 = off;
     off += round_up(M * K * 2, 1024);
     p.off_inv = off;
-    off += round_up(M * 4, 256);
+    off += round_up((p.T * p.NT + 32) * 4, 256);   // read 32 at a time from any token tile
     p.off_counters = off;
     off += round_up(tiles * 4, 256);
     p.off_partial = off;
