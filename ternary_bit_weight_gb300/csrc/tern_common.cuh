@@ -56,54 +56,87 @@ __device__ __forceinline__ void grid_launch_dependents() {
 // involved fits the format's precision, gives
 //   t = r * 2^-p - (BASE * 2^-p + 1) = v - 1.
 
-template <int P>
-__device__ __forceinline__ uint32_t decode_pair_bf16(uint32_t w) {
-    // bf16x2 bit patterns: 2^-p and -(128 * 2^-p + 1) in both halves
-    constexpr uint32_t kMul = P == 0 ? 0x3F803F80u : P == 2 ? 0x3E803E80u : P == 4 ? 0x3D803D80u : 0x3C803C80u;
-    constexpr uint32_t kAdd = P == 0 ? 0xC301C301u : P == 2 ? 0xC204C204u : P == 4 ? 0xC110C110u : 0xC040C040u;
-    const uint32_t r = (w & (0x00030003u << P)) | 0x43004300u;
-    uint32_t out;
-    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(out) : "r"(r), "r"(kMul), "r"(kAdd));
-    return out;
+//
+// The four masks, the base and the FMA constants live in registers that the
+// compiler cannot see through (an opaque move), and the mask-and-merge is an
+// explicit LOP3: with the constants as immediates the compiler splits it
+// into two integer operations, and the integer pipe is the decoder's limit.
+
+__device__ __forceinline__ uint32_t opaque_reg(uint32_t v) {
+    asm volatile("mov.b32 %0, %0;" : "+r"(v));
+    return v;
+}
+
+struct DecodeConsts {
+    uint32_t mask[4];   // fields of pair p = 2i in both halves
+    uint32_t base;
+    uint32_t mul[4];    // 2^-p in both halves
+    uint32_t add[4];    // -(BASE * 2^-p + 1) in both halves
+};
+
+// bf16: BASE = 128.0 (0x4300)
+__device__ __forceinline__ DecodeConsts decode_consts_bf16() {
+    DecodeConsts k;
+    const uint32_t mul[4] = {0x3F803F80u, 0x3E803E80u, 0x3D803D80u, 0x3C803C80u};
+    const uint32_t add[4] = {0xC301C301u, 0xC204C204u, 0xC110C110u, 0xC040C040u};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        k.mask[i] = opaque_reg(0x00030003u << (2 * i));
+        k.mul[i] = opaque_reg(mul[i]);
+        k.add[i] = opaque_reg(add[i]);
+    }
+    k.base = opaque_reg(0x43004300u);
+    return k;
+}
+
+// fp16: BASE = 1024.0 (0x6400)
+__device__ __forceinline__ DecodeConsts decode_consts_fp16() {
+    DecodeConsts k;
+    const uint32_t mul[4] = {0x3C003C00u, 0x34003400u, 0x2C002C00u, 0x24002400u};
+    const uint32_t add[4] = {0xE401E401u, 0xDC04DC04u, 0xD410D410u, 0xCC40CC40u};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        k.mask[i] = opaque_reg(0x00030003u << (2 * i));
+        k.mul[i] = opaque_reg(mul[i]);
+        k.add[i] = opaque_reg(add[i]);
+    }
+    k.base = opaque_reg(0x64006400u);
+    return k;
+}
+
+__device__ __forceinline__ uint32_t merge_field(uint32_t w, uint32_t mask, uint32_t base) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(w), "r"(mask), "r"(base));   // (w & mask) | base
+    return r;
 }
 
 // All eight bf16x2 pairs of one code word: out[i] = (t[k0+2i], t[k0+2i+1]).
-__device__ __forceinline__ void decode_word_bf16(uint32_t w, uint32_t* out) {
+__device__ __forceinline__ void decode_word_bf16(uint32_t w, const DecodeConsts& k, uint32_t* out) {
     const uint32_t w8 = w >> 8;
-    out[0] = decode_pair_bf16<0>(w);
-    out[1] = decode_pair_bf16<2>(w);
-    out[2] = decode_pair_bf16<4>(w);
-    out[3] = decode_pair_bf16<6>(w);
-    out[4] = decode_pair_bf16<0>(w8);
-    out[5] = decode_pair_bf16<2>(w8);
-    out[6] = decode_pair_bf16<4>(w8);
-    out[7] = decode_pair_bf16<6>(w8);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t r = merge_field(h == 0 ? w : w8, k.mask[i], k.base);
+            asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(out[4 * h + i]) : "r"(r), "r"(k.mul[i]), "r"(k.add[i]));
+        }
+    }
 }
 
 // fp16 variant: t as exact fp16 (+-1, 0), then times the row's FP16 scale
 // s (given in both halves): t * s is exactly +-s or 0.
-template <int P>
-__device__ __forceinline__ uint32_t decode_pair_fp16_scaled(uint32_t w, uint32_t s2) {
-    // f16x2 bit patterns: 2^-p and -(1024 * 2^-p + 1) in both halves
-    constexpr uint32_t kMul = P == 0 ? 0x3C003C00u : P == 2 ? 0x34003400u : P == 4 ? 0x2C002C00u : 0x24002400u;
-    constexpr uint32_t kAdd = P == 0 ? 0xE401E401u : P == 2 ? 0xDC04DC04u : P == 4 ? 0xD410D410u : 0xCC40CC40u;
-    const uint32_t r = (w & (0x00030003u << P)) | 0x64006400u;
-    uint32_t t, out;
-    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(t) : "r"(r), "r"(kMul), "r"(kAdd));
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(out) : "r"(t), "r"(s2));
-    return out;
-}
-
-__device__ __forceinline__ void decode_word_fp16_scaled(uint32_t w, uint32_t s2, uint32_t* out) {
+__device__ __forceinline__ void decode_word_fp16_scaled(uint32_t w, uint32_t s2, const DecodeConsts& k, uint32_t* out) {
     const uint32_t w8 = w >> 8;
-    out[0] = decode_pair_fp16_scaled<0>(w, s2);
-    out[1] = decode_pair_fp16_scaled<2>(w, s2);
-    out[2] = decode_pair_fp16_scaled<4>(w, s2);
-    out[3] = decode_pair_fp16_scaled<6>(w, s2);
-    out[4] = decode_pair_fp16_scaled<0>(w8, s2);
-    out[5] = decode_pair_fp16_scaled<2>(w8, s2);
-    out[6] = decode_pair_fp16_scaled<4>(w8, s2);
-    out[7] = decode_pair_fp16_scaled<6>(w8, s2);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t r = merge_field(h == 0 ? w : w8, k.mask[i], k.base);
+            uint32_t t;
+            asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(t) : "r"(r), "r"(k.mul[i]), "r"(k.add[i]));
+            asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(out[4 * h + i]) : "r"(t), "r"(s2));
+        }
+    }
 }
 
 __device__ __forceinline__ float fp16_bits_to_float(uint32_t bits16) {

@@ -355,6 +355,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
         const uint32_t tm = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + rt * kAU * kACols;
         const uint32_t bar_afull = cb + kBarAFull;
         const uint32_t bar_aempty = cb + kBarAEmpty;
+        const DecodeConsts dk = decode_consts_fp16();
         int ws = 0, al = 0;
         uint32_t w_ph = 0, a_ph = 0;
         int64_t acount = 0;
@@ -386,10 +387,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
                     for (int hh = 0; hh < 2; ++hh) {
                         const uint4 c = hh == 0 ? c0 : c1;
                         uint32_t p[32];
-                        decode_word_fp16_scaled(c.x, s2, p);
-                        decode_word_fp16_scaled(c.y, s2, p + 8);
-                        decode_word_fp16_scaled(c.z, s2, p + 16);
-                        decode_word_fp16_scaled(c.w, s2, p + 24);
+                        decode_word_fp16_scaled(c.x, s2, dk, p);
+                        decode_word_fp16_scaled(c.y, s2, dk, p + 8);
+                        decode_word_fp16_scaled(c.z, s2, dk, p + 16);
+                        decode_word_fp16_scaled(c.w, s2, dk, p + 24);
                         tmem_st_32x32b_x32(tm + al * kACols + 32 * hh, p);
                     }
                     tmem_st_wait();

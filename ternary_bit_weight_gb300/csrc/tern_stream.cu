@@ -405,6 +405,7 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
         const int q = warp >> 2;
         const int r = threadIdx.x & 127;   // weight row in the tile = tensor-memory lane
         const uint32_t tm = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + q * kAQ * kACols;
+        const DecodeConsts dk = decode_consts_bf16();
         const int codes_off = C::OffCodes + 16 * r;   // + unit in stage * 4096 (+ 2048 second half)
         const uint32_t bar_afull = cb + kBarAFull + 8 * kAQ * q;
         const uint32_t bar_aempty = cb + kBarAEmpty + 8 * kAQ * q;
@@ -433,10 +434,10 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
             for (int hh = 0; hh < 2; ++hh) {
                 const uint4 c = hh == 0 ? c0 : c1;
                 uint32_t p[32];
-                decode_word_bf16(c.x, p);
-                decode_word_bf16(c.y, p + 8);
-                decode_word_bf16(c.z, p + 16);
-                decode_word_bf16(c.w, p + 24);
+                decode_word_bf16(c.x, dk, p);
+                decode_word_bf16(c.y, dk, p + 8);
+                decode_word_bf16(c.z, dk, p + 16);
+                decode_word_bf16(c.w, dk, p + 24);
                 tmem_st_32x32b_x32(a_tm + 32 * hh, p);
             }
             tmem_st_wait();
