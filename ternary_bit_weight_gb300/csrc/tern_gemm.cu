@@ -281,9 +281,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
         }
     } else if (warp == kMmaWarp) {
         // --------------------------------------------------------------- MMA
-        // per group one vote over: activation stage full (lane 0), A slot of
-        // both row tiles full (lane 1), accumulators drained (lane 2, first
-        // group of an item)
+        // per group one vote over: activation stage full (lane 1), A slot of
+        // both row tiles full (lane 2), accumulators drained (lane 3, first
+        // group of an item).  Lane 0 issues the MMAs and commits and tests
+        // no barrier: a thread's barrier operations wait behind its own
+        // commits, that is, until its last MMAs have completed.
         const uint32_t idesc = idesc_fp16_f32(128, static_cast<uint32_t>(NT));
         const uint64_t bdesc0 = smem_desc_kmajor_sw128(xring);
         int xs = 0, al = 0;
@@ -299,15 +301,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
                 const int xg = (g - g0) % kXG;
                 uint32_t bar = 0, par = 0;
                 bool act = false;
-                if (lane == 0) {
+                if (lane == 1) {
                     act = xg == 0;
                     bar = cb + kBarXFull + 8 * xs;
                     par = x_ph;
-                } else if (lane == 1) {
+                } else if (lane == 2) {
                     act = true;
                     bar = cb + kBarAFull + 8 * al;
                     par = a_ph;
-                } else if (lane == 2) {
+                } else if (lane == 3) {
                     act = g == g0 && d_round > 0;
                     bar = cb + kBarDEmpty;
                     par = (d_round - 1) & 1u;
@@ -383,16 +385,16 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
                     tc_fence_after_sync();
                 }
                 if (mine) {
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        const uint4 c = hh == 0 ? c0 : c1;
-                        uint32_t p[32];
-                        decode_word_fp16_scaled(c.x, s2, dk, p);
-                        decode_word_fp16_scaled(c.y, s2, dk, p + 8);
-                        decode_word_fp16_scaled(c.z, s2, dk, p + 16);
-                        decode_word_fp16_scaled(c.w, s2, dk, p + 24);
-                        tmem_st_32x32b_x32(tm + al * kACols + 32 * hh, p);
-                    }
+                    uint32_t p[64];
+                    decode_word_fp16_scaled(c0.x, s2, dk, p);
+                    decode_word_fp16_scaled(c0.y, s2, dk, p + 8);
+                    decode_word_fp16_scaled(c0.z, s2, dk, p + 16);
+                    decode_word_fp16_scaled(c0.w, s2, dk, p + 24);
+                    decode_word_fp16_scaled(c1.x, s2, dk, p + 32);
+                    decode_word_fp16_scaled(c1.y, s2, dk, p + 40);
+                    decode_word_fp16_scaled(c1.z, s2, dk, p + 48);
+                    decode_word_fp16_scaled(c1.w, s2, dk, p + 56);
+                    tmem_st_32x32b_x64(tm + al * kACols, p);
                     tmem_st_wait();
                 }
                 tc_fence_before_sync();

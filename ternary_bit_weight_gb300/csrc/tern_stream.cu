@@ -59,11 +59,19 @@ namespace tern {
 namespace {
 
 // warp roles
+// The MMA warps come first: a warp scheduler that has to choose among ready
+// warps favours the older (lower) ones, and the decode warps, always ready
+// with long runs of independent integer and FMA work, would otherwise hold
+// the issue slots of their sub-partition for hundreds of cycles at a time.
+// Warp w reaches tensor-memory lanes 32 (w mod 4) .. +31, so each
+// warpgroup of decode or promotion warps starts at a multiple of 4.
+constexpr int kMmaWarp0 = 0;                    // one MMA warp per decode stream, SMSPs 0 and 1
+constexpr int kProducerWarp = 2;                // SMSP 2 (warp 3 only allocates tensor memory)
+constexpr int kAllocWarp = 3;
+constexpr int kDecWarp0 = 4;
 constexpr int kDecWarps = 8;                    // 2 streams x 1 warpgroup (whole units)
-constexpr int kPromWarp0 = kDecWarps;           // 4 warps
-constexpr int kProducerWarp = kPromWarp0 + 4;   // on SMSP 0
-constexpr int kMmaWarp0 = kProducerWarp + 1;    // one MMA warp per decode stream, SMSPs 1 and 2
-constexpr int kThreads = (kMmaWarp0 + 2) * 32;
+constexpr int kPromWarp0 = kDecWarp0 + kDecWarps;   // 4 warps
+constexpr int kThreads = (kPromWarp0 + 4) * 32;
 // tensor memory: each decode stream has its own A ring; accumulators come
 // in pairs of 16-column slots (one even unit, one odd unit)
 constexpr int kTmemCols = 512;
@@ -139,7 +147,7 @@ __device__ __forceinline__ int64_t owner_worker(int64_t u, int64_t U, int64_t V)
 // partials in the CTA's slot, and the last contributing CTA to arrive for
 // that row quarter sums all partials in CTA order.
 template <int NCOL>
-__device__ __forceinline__ void flush_tile(const StreamArgs& a, int64_t v, int64_t b, int64_t first_tile,
+__device__ __noinline__ void flush_tile(const StreamArgs& a, int64_t v, int64_t b, int64_t first_tile,
                                            bool whole, float (&acc)[NCOL], int r) {
     const int lane = r & 31, quad = r >> 5;
     const int64_t row = b * kTileRows + r;
@@ -196,12 +204,13 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return __all_sync(0xffffffffu, got);
 }
 
-// Bounded wait by lane 0 alone, its result broadcast to the warp (for warps
-// that only issue asynchronous work after the wait).
-__device__ __forceinline__ bool leader_wait(uint32_t bar, uint32_t parity, volatile int* abort, int lane) {
-    uint32_t got = 1;
-    if (lane == 0) got = mbar_wait(bar, parity, abort) ? 1u : 0u;
-    return __shfl_sync(0xffffffffu, got, 0) != 0;
+// Each lane with `active` set waits for its own barrier; the warp goes on
+// when all have completed.  The common case costs one test and one vote:
+// while an MMA warp waits, its share of the tensor pipe stands idle.
+__device__ __forceinline__ bool vote_wait(uint32_t bar, uint32_t parity, bool active, volatile int* abort) {
+    if (__all_sync(0xffffffffu, !active || mbar_test_wait(bar, parity))) return true;
+    const bool got = !active || mbar_wait(bar, parity, abort);
+    return __all_sync(0xffffffffu, got);
 }
 
 template <bool ONE>
@@ -252,7 +261,7 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
         *abort_flag = 0;
         mbar_fence_init();
     }
-    if (warp == 0) {
+    if (warp == kAllocWarp) {
         tmem_alloc(smem_u32(tmem_base_ptr), kTmemCols);
         tmem_relinquish();
     }
@@ -322,7 +331,7 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
             }
             (void)mbar_wait(cb + kBarX, 0, &no_abort);
         }
-    } else if (warp >= kMmaWarp0) {
+    } else if (warp < kMmaWarp0 + 2) {
         // --------------------------------------------------------------- MMA
         // MMA warp q serves decode stream q (units q, q+2, ...).  The whole
         // warp runs the loop with warp-uniform descriptors; lane 0 waits and
@@ -330,7 +339,6 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
         const int q = warp - kMmaWarp0;
         constexpr uint32_t idesc = idesc_bf16_f32(128, kNtok);
         bool ok = true;
-        if (ONE) ok = leader_wait(cb + kBarX, 0, abort_flag, lane);
         int32_t g = static_cast<int32_t>((u0 + q) % G);   // group of unit j
         const int32_t g_step = 2 % G;
         // B descriptors: M == 1 the resident row (+16 per group, +2 per K-step);
@@ -346,10 +354,31 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
         for (int32_t j = q; j < n && ok; j += 2) {
             const int32_t k = j >> 1;
             const int us = j % kPS;
-            ok = (k < kDP || leader_wait(cb + kBarDEmpty + 8 * dp, d_ph ^ 1u, abort_flag, lane)) &&
-                 (ONE || us >= 2 || leader_wait(bar_full + 8 * s, full_ph, abort_flag, lane)) &&
-                 leader_wait(bar_afull + 8 * al, a_ph, abort_flag, lane);
-            if (!ok) break;
+            // one vote: D pair free (lane 1), stage full (lane 2), A slot
+            // full (lane 3), activation row copied (lane 4, first unit).
+            // Lane 0 issues the MMAs and commits and tests no barrier: a
+            // thread's barrier operations wait behind its own commits, that
+            // is, until its last MMAs have completed.
+            uint32_t bar = 0, par = 0;
+            bool act = false;
+            if (lane == 1) {
+                act = k >= kDP;
+                bar = cb + kBarDEmpty + 8 * dp;
+                par = d_ph ^ 1u;
+            } else if (lane == 2) {
+                act = !ONE && us < 2;
+                bar = bar_full + 8 * s;
+                par = full_ph;
+            } else if (lane == 3) {
+                act = true;
+                bar = bar_afull + 8 * al;
+                par = a_ph;
+            } else if (lane == 4) {
+                act = ONE && j == q;
+                bar = cb + kBarX;
+                par = 0;
+            }
+            if (!(ok = vote_wait(bar, par, act, abort_flag))) break;
             tc_fence_after_sync();
             const uint32_t a_tm = a_tm0 + al * kACols;
             const uint32_t d_tm = d_tm0 + 2 * dp * kNtok;
@@ -388,7 +417,7 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
         // been consumed, so the arrival cannot count towards that phase
         if (ok && q == 1 && (n & 1)) {
             const int32_t k = n >> 1;
-            if (k < kDP || leader_wait(cb + kBarDEmpty + 8 * dp, d_ph ^ 1u, abort_flag, lane)) {
+            if (vote_wait(cb + kBarDEmpty + 8 * dp, d_ph ^ 1u, lane == 1 && k >= kDP, abort_flag)) {
                 if (elect_one()) umma_commit(cb + kBarDFull + 8 * dp);
                 __syncwarp();
             }
@@ -398,11 +427,11 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
         __syncwarp();
         volatile int no_abort = 0;
         (void)mbar_wait(cb + kBarDrain + 8 * q, 0, &no_abort);
-    } else if (warp < kDecWarps) {
+    } else if (warp >= kDecWarp0 && warp < kDecWarp0 + kDecWarps) {
         // ---------------------------------------------------- decode streams
         // stream q (one warpgroup) decodes units j = q, q+2, ...: each
         // thread the 128 weights of its row
-        const int q = warp >> 2;
+        const int q = (warp - kDecWarp0) >> 2;
         const int r = threadIdx.x & 127;   // weight row in the tile = tensor-memory lane
         const uint32_t tm = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + q * kAQ * kACols;
         const DecodeConsts dk = decode_consts_bf16();
@@ -429,16 +458,17 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
                 if (!warp_wait(bar_aempty + 8 * al, a_ph ^ 1u, abort_flag)) break;
                 tc_fence_after_sync();
             }
-            const uint32_t a_tm = tm + al * kACols;
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const uint4 c = hh == 0 ? c0 : c1;
-                uint32_t p[32];
-                decode_word_bf16(c.x, dk, p);
-                decode_word_bf16(c.y, dk, p + 8);
-                decode_word_bf16(c.z, dk, p + 16);
-                decode_word_bf16(c.w, dk, p + 24);
-                tmem_st_32x32b_x32(a_tm + 32 * hh, p);
+            {
+                uint32_t p[64];
+                decode_word_bf16(c0.x, dk, p);
+                decode_word_bf16(c0.y, dk, p + 8);
+                decode_word_bf16(c0.z, dk, p + 16);
+                decode_word_bf16(c0.w, dk, p + 24);
+                decode_word_bf16(c1.x, dk, p + 32);
+                decode_word_bf16(c1.y, dk, p + 40);
+                decode_word_bf16(c1.z, dk, p + 48);
+                decode_word_bf16(c1.w, dk, p + 56);
+                tmem_st_32x32b_x64(tm + al * kACols, p);
             }
             tmem_st_wait();
             tc_fence_before_sync();
@@ -449,7 +479,7 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
                 a_ph ^= 1u;
             }
         }
-    } else if (warp < kPromWarp0 + 4) {
+    } else if (warp >= kPromWarp0) {
         // ------------------------------------------------------- promotion
         const int r = threadIdx.x & 127;   // weight row in the tile = tensor-memory lane
         const uint32_t tm = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + kDCol0;
@@ -524,7 +554,7 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
     tc_fence_before_sync();
     __syncthreads();
     if (*abort_flag && threadIdx.x == 0) atomicOr(a.err, 1);
-    if (warp == 0) {
+    if (warp == kAllocWarp) {
         tc_fence_after_sync();
         tmem_dealloc(tmem, kTmemCols);
     }
