@@ -65,13 +65,17 @@ namespace {
 // the issue slots of their sub-partition for hundreds of cycles at a time.
 // Warp w reaches tensor-memory lanes 32 (w mod 4) .. +31, so each
 // warpgroup of decode or promotion warps starts at a multiple of 4.
-constexpr int kMmaWarp0 = 0;                    // one MMA warp per decode stream, SMSPs 0 and 1
-constexpr int kProducerWarp = 2;                // SMSP 2 (warp 3 only allocates tensor memory)
-constexpr int kAllocWarp = 3;
+// MMA warp m (warps 0, 1 and, at M = 1, 3) issues units m, m+W, ... for W
+// MMA warps: a warp's MMA issue is slow next to busy decoders, so M = 1,
+// with nothing else to copy, spreads it over three.
+constexpr int kMaxMmaWarps = 3;
+constexpr int kProducerWarp = 2;
+constexpr int kAllocWarp = 0;
 constexpr int kDecWarp0 = 4;
 constexpr int kDecWarps = 8;                    // 2 streams x 1 warpgroup (whole units)
 constexpr int kPromWarp0 = kDecWarp0 + kDecWarps;   // 4 warps
 constexpr int kThreads = (kPromWarp0 + 4) * 32;
+__device__ __forceinline__ int mma_index(int warp) { return warp < 2 ? warp : warp == 3 ? 2 : -1; }
 // tensor memory: each decode stream has its own A ring; accumulators come
 // in pairs of 16-column slots (one even unit, one odd unit)
 constexpr int kTmemCols = 512;
@@ -89,15 +93,15 @@ constexpr int kMaxStages = 48;
 
 template <bool ONE>
 struct SCfg {
+    static constexpr int MmaWarps = ONE ? 3 : 2;
     static constexpr int NCOL = ONE ? 1 : kNtok;        // token columns promoted per unit
     static constexpr int XUnit = ONE ? 0 : kNtok * kGroup * 2;   // one unit's X tile
     static constexpr int OffCodes = kPS * XUnit;         // X tiles first (1024-byte aligned)
     static constexpr int OffScales = OffCodes + kPS * kUnitCodeBytes;
     static constexpr int StageBytes = static_cast<int>(round_up(OffScales + kPS * kUnitScaleBytes, ONE ? 16 : 1024));
     // a stage is released by every decode warp, the promotion warps (they
-    // read the scales) and, when X travels in the stage, both MMA
-    // warps
-    static constexpr int EmptyCount = kDecWarps + 4 + (ONE ? 0 : 2);
+    // read the scales) and, when X travels in the stage, every MMA warp
+    static constexpr int EmptyCount = kDecWarps + 4 + (ONE ? 0 : MmaWarps);
 };
 
 // control block offsets
@@ -106,13 +110,13 @@ constexpr int kBarAEmpty = kBarAFull + 8 * 2 * kAQ;          // [2][kAQ]
 constexpr int kBarDFull = kBarAEmpty + 8 * 2 * kAQ;          // [kDP]
 constexpr int kBarDEmpty = kBarDFull + 8 * kDP;              // [kDP]
 constexpr int kBarX = kBarDEmpty + 8 * kDP;                  // activation row copied (M == 1)
-constexpr int kBarDrain = kBarX + 8;                         // [2]
-constexpr int kTmemPtr = kBarDrain + 16;
+constexpr int kBarDrain = kBarX + 8;                         // [kMaxMmaWarps]
+constexpr int kTmemPtr = kBarDrain + 8 * kMaxMmaWarps;
 constexpr int kAbort = kTmemPtr + 4;
 constexpr int kBarStages = 256;                              // full[S], empty[S]
 static_assert(kAbort + 4 <= kBarStages, "control block");
 static_assert(kBarStages + 16 * kMaxStages <= kCtrlBytes, "control block");
-static_assert(kPS % 2 == 0, "stages hold whole pairs");
+static_assert(kPS % 2 == 0, "with activation tiles in the stages, each of the two MMA warps has units in every full stage");
 
 // M == 1 shared-memory layout before the stages: the activation row (2K
 // bytes) and 256 bytes the tensor cores may read past its end.
@@ -147,7 +151,7 @@ __device__ __forceinline__ int64_t owner_worker(int64_t u, int64_t U, int64_t V)
 // partials in the CTA's slot, and the last contributing CTA to arrive for
 // that row quarter sums all partials in CTA order.
 template <int NCOL>
-__device__ __noinline__ void flush_tile(const StreamArgs& a, int64_t v, int64_t b, int64_t first_tile,
+__device__ __forceinline__ void flush_tile(const StreamArgs& a, int64_t v, int64_t b, int64_t first_tile,
                                            bool whole, float (&acc)[NCOL], int r) {
     const int lane = r & 31, quad = r >> 5;
     const int64_t row = b * kTileRows + r;
@@ -256,8 +260,7 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
             mbar_init(cb + kBarDEmpty + 8 * i, 4);               // the promotion warps
         }
         mbar_init(cb + kBarX, 1);
-        mbar_init(cb + kBarDrain, 1);
-        mbar_init(cb + kBarDrain + 8, 1);
+        for (int i = 0; i < kMaxMmaWarps; ++i) mbar_init(cb + kBarDrain + 8 * i, 1);
         *abort_flag = 0;
         mbar_fence_init();
     }
@@ -331,34 +334,32 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
             }
             (void)mbar_wait(cb + kBarX, 0, &no_abort);
         }
-    } else if (warp < kMmaWarp0 + 2) {
+    } else if (mma_index(warp) >= 0 && mma_index(warp) < C::MmaWarps) {
         // --------------------------------------------------------------- MMA
-        // MMA warp q serves decode stream q (units q, q+2, ...).  The whole
-        // warp runs the loop with warp-uniform descriptors; lane 0 waits and
-        // one elected lane (always the same) issues the MMAs and commits.
-        const int q = warp - kMmaWarp0;
+        // MMA warp m issues units j = m, m + 4, ... (stream j mod 2, that
+        // stream's unit j / 2).  The whole warp runs the loop with
+        // warp-uniform descriptors; one elected lane issues the MMAs and
+        // commits.  Each unit's eight MMAs start its own accumulator, so the
+        // order between MMA warps does not matter.
+        const int m = mma_index(warp);
+        constexpr int kMmaWarps = C::MmaWarps;
         constexpr uint32_t idesc = idesc_bf16_f32(128, kNtok);
         bool ok = true;
-        int32_t g = static_cast<int32_t>((u0 + q) % G);   // group of unit j
-        const int32_t g_step = 2 % G;
+        int32_t g = static_cast<int32_t>((u0 + m) % G);   // group of unit j
         // B descriptors: M == 1 the resident row (+16 per group, +2 per K-step);
         // else the unit's X tile in the stage
         const uint64_t bdesc_x = smem_desc_kmajor_noswz(sbase, 16, 16);
         const uint64_t bdesc_ring = smem_desc_kmajor_sw128(ring);
-        const uint32_t bar_afull = cb + kBarAFull + 8 * kAQ * q;
-        const uint32_t bar_aempty = cb + kBarAEmpty + 8 * kAQ * q;
-        const uint32_t a_tm0 = tmem + q * kAQ * kACols;
-        const uint32_t d_tm0 = tmem + kDCol0 + q * kNtok;
-        int s = 0, al = 0, dp = 0;   // stage, A slot, D pair slot
-        uint32_t full_ph = 0, a_ph = 0, d_ph = 0;
-        for (int32_t j = q; j < n && ok; j += 2) {
-            const int32_t k = j >> 1;
-            const int us = j % kPS;
+        // stage of unit j (M > 1; kMmaWarps divides kPS): tracked, not divided
+        int us = m, s = 0;
+        uint32_t full_ph = 0;
+        for (int32_t j = m; j < n && ok; j += kMmaWarps) {
+            const int q = j & 1;                 // decode stream
+            const int32_t k = j >> 1;            // pair = the stream's unit index
+            const int al = k % kAQ, dp = k % kDP;
+            const uint32_t a_ph = (k / kAQ) & 1u, d_ph = (k / kDP) & 1u;
             // one vote: D pair free (lane 1), stage full (lane 2), A slot
-            // full (lane 3), activation row copied (lane 4, first unit).
-            // Lane 0 issues the MMAs and commits and tests no barrier: a
-            // thread's barrier operations wait behind its own commits, that
-            // is, until its last MMAs have completed.
+            // full (lane 3), activation row copied (lane 4, first units)
             uint32_t bar = 0, par = 0;
             bool act = false;
             if (lane == 1) {
@@ -366,22 +367,22 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
                 bar = cb + kBarDEmpty + 8 * dp;
                 par = d_ph ^ 1u;
             } else if (lane == 2) {
-                act = !ONE && us < 2;
+                act = !ONE && us < kMmaWarps;
                 bar = bar_full + 8 * s;
                 par = full_ph;
             } else if (lane == 3) {
                 act = true;
-                bar = bar_afull + 8 * al;
+                bar = cb + kBarAFull + 8 * (kAQ * q + al);
                 par = a_ph;
             } else if (lane == 4) {
-                act = ONE && j == q;
+                act = ONE && j == m;
                 bar = cb + kBarX;
                 par = 0;
             }
             if (!(ok = vote_wait(bar, par, act, abort_flag))) break;
             tc_fence_after_sync();
-            const uint32_t a_tm = a_tm0 + al * kACols;
-            const uint32_t d_tm = d_tm0 + 2 * dp * kNtok;
+            const uint32_t a_tm = tmem + (q * kAQ + al) * kACols;
+            const uint32_t d_tm = tmem + kDCol0 + (2 * dp + q) * kNtok;
             const uint64_t b0 = ONE ? bdesc_x + 16u * (uint32_t)g
                                     : bdesc_ring + ((uint32_t)(s * C::StageBytes + us * C::XUnit) >> 4);
             if (elect_one()) {
@@ -392,41 +393,39 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
                     const uint32_t step = ONE ? 2 * kk : (kk >> 2) * (kNtok * 128 / 16) + 2 * (kk & 3);
                     umma_bf16_tmem_a(d_tm, a_tm + 8 * kk, b0 + step, idesc, kk > 0 ? 1u : 0u);
                 }
-                umma_commit(bar_aempty + 8 * al);
+                umma_commit(cb + kBarAEmpty + 8 * (kAQ * q + al));
                 umma_commit(cb + kBarDFull + 8 * dp);
-                if (!ONE && (us >= kPS - 2 || j + 2 >= n)) umma_commit(bar_empty + 8 * s);
+                if (!ONE && (us + kMmaWarps >= kPS || j + kMmaWarps >= n)) umma_commit(bar_empty + 8 * s);
             }
             __syncwarp();
-            g += g_step;
-            if (g >= G) g -= G;
-            if (++al == kAQ) {
-                al = 0;
-                a_ph ^= 1u;
-            }
-            if (++dp == kDP) {
-                dp = 0;
-                d_ph ^= 1u;
-            }
-            if (us >= kPS - 2 && ++s == S) {
-                s = 0;
-                full_ph ^= 1u;
+            g += kMmaWarps;
+            while (g >= G) g -= G;
+            if (!ONE && (us += kMmaWarps) >= kPS) {
+                us -= kPS;
+                if (++s == S) {
+                    s = 0;
+                    full_ph ^= 1u;
+                }
             }
         }
-        // odd n: the last pair has no unit for MMA warp 1, which still
-        // signals its accumulator pair -- after the slot's previous pair has
-        // been consumed, so the arrival cannot count towards that phase
-        if (ok && q == 1 && (n & 1)) {
+        // odd n: the last pair has no stream-1 unit; the warp that would
+        // have issued it still signals the pair's accumulators -- after the
+        // slot's previous pair has been consumed, so that the arrival cannot
+        // count towards that phase
+        if (ok && (n & 1) && n % kMmaWarps == m) {
             const int32_t k = n >> 1;
+            const int dp = k % kDP;
+            const uint32_t d_ph = (k / kDP) & 1u;
             if (vote_wait(cb + kBarDEmpty + 8 * dp, d_ph ^ 1u, lane == 1 && k >= kDP, abort_flag)) {
                 if (elect_one()) umma_commit(cb + kBarDFull + 8 * dp);
                 __syncwarp();
             }
         }
         // every MMA this warp issued has completed before tensor memory is freed
-        if (elect_one()) umma_commit(cb + kBarDrain + 8 * q);
+        if (elect_one()) umma_commit(cb + kBarDrain + 8 * m);
         __syncwarp();
         volatile int no_abort = 0;
-        (void)mbar_wait(cb + kBarDrain + 8 * q, 0, &no_abort);
+        (void)mbar_wait(cb + kBarDrain + 8 * m, 0, &no_abort);
     } else if (warp >= kDecWarp0 && warp < kDecWarp0 + kDecWarps) {
         // ---------------------------------------------------- decode streams
         // stream q (one warpgroup) decodes units j = q, q+2, ...: each
