@@ -19,7 +19,8 @@
  *         §3   disk layout and GPU layout must be reconciled;
  *         §4.2 the op: x [M,K], packed w [N,K/4], scale [N,K/128] -> y [M,N];
  *              signs accumulated inside a 128-block, scale applied once at
- *              the block boundary;
+ *              the block boundary; the page's kernel takes half-precision
+ *              activations and writes a half-precision output;
  *         §4.4 inputs are reshaped to a 2-D contiguous [tokens, hidden].
  *   [B27] "Porting ternary Bonsai 2 27B to vLLM", m.xxqk.cn/news/594847
  *         §5.2 FP16 scales are stored little-endian.
@@ -49,6 +50,10 @@
 #ifdef __cplusplus
 extern "C" {
 #endif
+
+/* Element type of activations (x_type) and outputs (out_type). */
+typedef enum { TERN_X_BF16 = 0, TERN_X_F16 = 1 } tern_x_type;
+typedef enum { TERN_OUT_F32 = 0, TERN_OUT_BF16 = 1, TERN_OUT_F16 = 2 } tern_out_type;
 
 typedef enum {
     TERN_OK = 0,
@@ -157,7 +162,10 @@ tern_status tern_unrepack(const void* d_tiled, int64_t N, int64_t K, uint8_t* d_
  *            Calls that may overlap in time need separate workspaces.  Its
  *            first 32-bit word is an error word: the kernel sets it non-zero
  *            (and returns early, leaving Y incomplete) only if a pipeline
- *            wait timed out, which correct inputs never cause.
+ *            wait timed out (2 s), which correct inputs never cause.  Read
+ *            it with tern_workspace_error.  A call that ended that way may
+ *            also leave tile counters and partial sums behind: clear the
+ *            whole workspace (tern_workspace_reset) before it serves again.
  * M == 0 or N == 0 is a no-op.  K must be a positive multiple of 128.
  * X is read after any preceding kernel on the stream completes; kernels
  * launched with programmatic dependent launch may begin streaming weights
@@ -201,6 +209,72 @@ tern_status tern_linear_multi(const uint16_t* d_X, int64_t ldx, const void* d_ti
 tern_status tern_linear_noalloc(const uint16_t* d_X, int64_t ldx, const void* d_tiled,
                                 int64_t M, int64_t N, int64_t K, float* d_Y, int64_t ldy,
                                 void* stream);
+
+/* The general form of tern_linear_multi ([EMB] §4.2 half-precision
+ * activations and output; §2.2 fused projections):
+ *   d_X      device [M, ldx] of bf16 (x_type TERN_X_BF16) or fp16
+ *            (TERN_X_F16) bits; alignment as tern_linear.  fp16 and bf16
+ *            inputs are used exactly (the weights are exact in both
+ *            formats and products accumulate in fp32).
+ *   d_Ys[j]  device [M, ldys[j]] outputs of out_type: fp32, or bf16 / fp16
+ *            rounded to nearest even from the fp32 result (4-byte aligned
+ *            for fp32, 2-byte otherwise).
+ * Other arguments as tern_linear_multi; unknown x_type or out_type values
+ * return TERN_ERR_SHAPE. */
+tern_status tern_linear_ex(const void* d_X, int x_type, int64_t ldx, const void* d_tiled,
+                           int64_t M, int64_t K, int n_out, const int64_t* n_sizes,
+                           void* const* d_Ys, const int64_t* ldys, int out_type,
+                           void* d_ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Fused gate+up projection with SwiGLU ([EMB] §2.2: gate and up are one
+ * fused tensor cut by offsets):
+ *   h[m, i] = silu(gate[m, i]) * up[m, i],  silu(g) = g / (1 + exp(-g)),
+ * with gate and up each the linear layer above over their I rows.
+ *
+ * GLU tile layout: the tiled layout of a 2*ceil(I/16)*16-row weight whose
+ * row n is gate row 16*(n/32) + n%32 when n%32 < 16 and up row
+ * 16*(n/32) + n%32 - 16 otherwise (blocks of 16 rows alternating; rows
+ * past I are zero).  Paired rows then meet in one warp of the epilogue.
+ * ---------------------------------------------------------------------- */
+
+/* Bytes of the GLU tile layout: tern_tiled_bytes(2*ceil(I/16)*16, K). */
+size_t tern_tiled_glu_bytes(int64_t I, int64_t K);
+
+/* (gate, up) on-disk pairs -> GLU tile layout.  Each of the two sources is
+ * an on-disk pair as for tern_repack with I rows; a fused [2I, K/4] tensor
+ * passes d_packed_up = d_packed_gate + I*K/4 (and likewise the scales).
+ * Alignments, errors and d_err as tern_repack. */
+tern_status tern_repack_glu(const uint8_t* d_packed_gate, const uint16_t* d_scales_gate,
+                            const uint8_t* d_packed_up, const uint16_t* d_scales_up,
+                            int64_t I, int64_t K, void* d_tiled, size_t tiled_bytes,
+                            int32_t* d_err, void* stream);
+
+/* Workspace bytes of tern_linear_swiglu. */
+size_t tern_swiglu_workspace_bytes(int64_t M, int64_t I, int64_t K);
+
+/* h = silu(X . gate^T) * (X . up^T) in one pass over the GLU tile layout.
+ *   d_H  device [M, ldh] of out_type, ldh >= I.
+ * gate and up are computed as by tern_linear (fp32, same error bound) and
+ * combined in fp32 before the output conversion.  Other arguments as
+ * tern_linear_ex. */
+tern_status tern_linear_swiglu(const void* d_X, int x_type, int64_t ldx, const void* d_tiled_glu,
+                               int64_t M, int64_t I, int64_t K, void* d_H, int64_t ldh,
+                               int out_type, void* d_ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Workspace maintenance (library conveniences; the pages have none).
+ * ---------------------------------------------------------------------- */
+
+/* Copy the workspace's error word to *h_err (host) and wait for `stream`
+ * to reach that point -- the one call in this header that synchronises
+ * (the stream only).  Non-zero: a call that used the workspace gave up
+ * after a pipeline wait timed out; its outputs are incomplete. */
+tern_status tern_workspace_error(const void* d_ws, int32_t* h_err, void* stream);
+
+/* Zero ws_bytes of the workspace on `stream` (the state a workspace must be
+ * in before its first use, and again after an error). */
+tern_status tern_workspace_reset(void* d_ws, size_t ws_bytes, void* stream);
 
 #ifdef __cplusplus
 }

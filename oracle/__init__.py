@@ -68,6 +68,12 @@ def _load():
             lib.orc_linear.restype = None
             lib.orc_linear_cols.argtypes = [vp, i64, vp, vp, i64, i64, i64, vp, i64, vp, vp]
             lib.orc_linear_cols.restype = None
+            lib.orc_linear_x.argtypes = [vp, ctypes.c_int, i64, vp, vp, i64, i64, i64, vp, vp]
+            lib.orc_linear_x.restype = None
+            lib.orc_linear_cols_x.argtypes = [vp, ctypes.c_int, i64, vp, vp, i64, i64, i64, vp, i64, vp, vp]
+            lib.orc_linear_cols_x.restype = None
+            lib.orc_swiglu.argtypes = [vp, vp, i64, vp]
+            lib.orc_swiglu.restype = None
             lib.orc_num_threads.argtypes = []
             lib.orc_num_threads.restype = ctypes.c_int
             _lib = lib
@@ -133,31 +139,71 @@ def unrepack(tiled: np.ndarray, N: int, K: int):
     return packed, scales, int(bad)
 
 
-def linear(x_bf16: np.ndarray, packed: np.ndarray, scales: np.ndarray, K: int):
-    """Y[M, N] = X . (s (.) T)^T in fp64, and the per-output bound sum_k |x w|."""
-    x = _c(x_bf16, np.uint16)
+def linear(x_bits: np.ndarray, packed: np.ndarray, scales: np.ndarray, K: int, x_f16: bool = False):
+    """Y[M, N] = X . (s (.) T)^T in fp64, and the per-output bound sum_k |x w|.
+    X holds bf16 bits, or fp16 bits with ``x_f16``."""
+    x = _c(x_bits, np.uint16)
     packed = _c(packed, np.uint8)
     scales = _c(scales, np.uint16)
     M, N = x.shape[0], packed.shape[0]
     y = np.empty((M, N), dtype=np.float64)
     b = np.empty((M, N), dtype=np.float64)
-    _load().orc_linear(x.ctypes.data, K, packed.ctypes.data, scales.ctypes.data,
-                       M, N, K, y.ctypes.data, b.ctypes.data)
+    _load().orc_linear_x(x.ctypes.data, int(x_f16), K, packed.ctypes.data, scales.ctypes.data,
+                         M, N, K, y.ctypes.data, b.ctypes.data)
     return y, b
 
 
-def linear_cols(x_bf16: np.ndarray, packed: np.ndarray, scales: np.ndarray, K: int, cols):
+def linear_cols(x_bits: np.ndarray, packed: np.ndarray, scales: np.ndarray, K: int, cols,
+                x_f16: bool = False):
     """Like ``linear`` for the output columns ``cols`` only: returns [M, len(cols)]."""
-    x = _c(x_bf16, np.uint16)
+    x = _c(x_bits, np.uint16)
     packed = _c(packed, np.uint8)
     scales = _c(scales, np.uint16)
     cols = _c(np.asarray(cols), np.int64)
     M, N = x.shape[0], packed.shape[0]
     y = np.empty((M, cols.size), dtype=np.float64)
     b = np.empty((M, cols.size), dtype=np.float64)
-    _load().orc_linear_cols(x.ctypes.data, K, packed.ctypes.data, scales.ctypes.data,
-                            M, N, K, cols.ctypes.data, cols.size, y.ctypes.data, b.ctypes.data)
+    _load().orc_linear_cols_x(x.ctypes.data, int(x_f16), K, packed.ctypes.data, scales.ctypes.data,
+                              M, N, K, cols.ctypes.data, cols.size, y.ctypes.data, b.ctypes.data)
     return y, b
+
+
+def swiglu(g: np.ndarray, u: np.ndarray) -> np.ndarray:
+    """silu(g) * u elementwise in fp64 (silu(g) = g / (1 + e^-g))."""
+    g = _c(g, np.float64)
+    u = _c(u, np.float64)
+    h = np.empty_like(g)
+    _load().orc_swiglu(g.ctypes.data, u.ctypes.data, g.size, h.ctypes.data)
+    return h
+
+
+def glu_rows(I: int) -> int:
+    """Rows of the GLU tile layout: 2 * ceil(I/16) * 16."""
+    return 2 * ((I + 15) // 16) * 16
+
+
+def glu_source(n: int):
+    """Source of GLU row n: ('gate' or 'up', row index), from the layout's
+    definition (blocks of 16 rows alternating between gate and up)."""
+    block, j = divmod(n, 32)
+    return ("gate" if j < 16 else "up"), 16 * block + (j % 16)
+
+
+def repack_glu(packed_gate, scales_gate, packed_up, scales_up, K: int):
+    """(gate, up) on-disk pairs of I rows -> GLU tile layout bytes: the
+    interleaved weight assembled row by row, then ``repack``."""
+    packed_gate = _c(packed_gate, np.uint8)
+    packed_up = _c(packed_up, np.uint8)
+    I = packed_gate.shape[0]
+    rows = glu_rows(I)
+    packed = np.zeros((rows, K // 4), dtype=np.uint8)
+    scales = np.zeros((rows, K // 128), dtype=np.uint16)
+    for n in range(rows):
+        which, i = glu_source(n)
+        if i < I:
+            packed[n] = (packed_gate if which == "gate" else packed_up)[i]
+            scales[n] = (scales_gate if which == "gate" else scales_up)[i]
+    return repack(packed, scales, K)
 
 
 def num_threads() -> int:

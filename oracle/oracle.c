@@ -14,7 +14,8 @@
  *                first weight in the lowest two bits; scale blocks cut
  *                contiguously along K; the unpack routine (shifts 0,2,4,6)
  *          §4.2  shapes: x [M,K], packed w [N,K/4] uint8, scale [N,K/128]
- *                half, y = x . W^T
+ *                half, y = x . W^T; the page's kernel reads half-precision
+ *                (fp16) activations
  *   [B27]  "Porting ternary Bonsai 2 27B to vLLM", m.xxqk.cn/news/594847
  *          §5.2  scales are little-endian FP16
  *
@@ -230,13 +231,14 @@ int64_t orc_unrepack(const uint8_t* tiled, int64_t N, int64_t K,
 /* ------------------------------------------------------------------ linear */
 
 /* One output: y = sum_k x[k] * t[n,k] * s[n,k/128] in fp64, k ascending, and
-   the tolerance scale sum_k |x[k] * t[n,k] * s[n,k/128]|. */
-static void dot_row(const uint16_t* xrow, const uint8_t* packed, const uint16_t* scales,
+   the tolerance scale sum_k |x[k] * t[n,k] * s[n,k/128]|.  x_f16: the
+   activations are fp16 bits, else bf16 bits. */
+static void dot_row(const uint16_t* xrow, int x_f16, const uint8_t* packed, const uint16_t* scales,
                     int64_t K, int64_t n, double* y, double* bound) {
     double acc = 0.0, mag = 0.0;
     int64_t G = K / 128;
     for (int64_t k = 0; k < K; ++k) {
-        double x = orc_bf16_to_double(xrow[k]);
+        double x = x_f16 ? orc_fp16_to_double(xrow[k]) : orc_bf16_to_double(xrow[k]);
         double w = (double)orc_code_to_ternary(packed_code(packed, K, n, k))
                  * orc_fp16_to_double(scales[n * G + k / 128]);
         acc += x * w;
@@ -248,24 +250,44 @@ static void dot_row(const uint16_t* xrow, const uint8_t* packed, const uint16_t*
 
 /* Y[m,n] (row stride N) and its bound for all m < M, n < N.
    X is bf16 bits [M, ldx]; packed [N, K/4]; scales fp16 bits [N, K/128]. */
-void orc_linear(const uint16_t* X, int64_t ldx, const uint8_t* packed,
-                const uint16_t* scales, int64_t M, int64_t N, int64_t K,
-                double* Y, double* bound) {
+void orc_linear_x(const uint16_t* X, int x_f16, int64_t ldx, const uint8_t* packed,
+                  const uint16_t* scales, int64_t M, int64_t N, int64_t K,
+                  double* Y, double* bound) {
     #pragma omp parallel for schedule(dynamic, 16) collapse(2)
     for (int64_t m = 0; m < M; ++m)
         for (int64_t n = 0; n < N; ++n)
-            dot_row(X + m * ldx, packed, scales, K, n, &Y[m * N + n], &bound[m * N + n]);
+            dot_row(X + m * ldx, x_f16, packed, scales, K, n, &Y[m * N + n], &bound[m * N + n]);
 }
 
-/* Same as orc_linear for a list of output columns: Y[m, j] for n = cols[j]. */
-void orc_linear_cols(const uint16_t* X, int64_t ldx, const uint8_t* packed,
-                     const uint16_t* scales, int64_t M, int64_t N, int64_t K,
-                     const int64_t* cols, int64_t ncols, double* Y, double* bound) {
+void orc_linear(const uint16_t* X, int64_t ldx, const uint8_t* packed,
+                const uint16_t* scales, int64_t M, int64_t N, int64_t K,
+                double* Y, double* bound) {
+    orc_linear_x(X, 0, ldx, packed, scales, M, N, K, Y, bound);
+}
+
+/* Same as orc_linear_x for a list of output columns: Y[m, j] for n = cols[j]. */
+void orc_linear_cols_x(const uint16_t* X, int x_f16, int64_t ldx, const uint8_t* packed,
+                       const uint16_t* scales, int64_t M, int64_t N, int64_t K,
+                       const int64_t* cols, int64_t ncols, double* Y, double* bound) {
     (void)N;
     #pragma omp parallel for schedule(dynamic, 4) collapse(2)
     for (int64_t m = 0; m < M; ++m)
         for (int64_t j = 0; j < ncols; ++j)
-            dot_row(X + m * ldx, packed, scales, K, cols[j], &Y[m * ncols + j], &bound[m * ncols + j]);
+            dot_row(X + m * ldx, x_f16, packed, scales, K, cols[j], &Y[m * ncols + j], &bound[m * ncols + j]);
+}
+
+void orc_linear_cols(const uint16_t* X, int64_t ldx, const uint8_t* packed,
+                     const uint16_t* scales, int64_t M, int64_t N, int64_t K,
+                     const int64_t* cols, int64_t ncols, double* Y, double* bound) {
+    orc_linear_cols_x(X, 0, ldx, packed, scales, M, N, K, cols, ncols, Y, bound);
+}
+
+/* ------------------------------------------------------------------ SwiGLU */
+
+/* silu(g) * u, with silu(g) = g / (1 + e^-g) (the textbook definition of
+   the sigmoid-weighted linear unit), elementwise over count values. */
+void orc_swiglu(const double* g, const double* u, int64_t count, double* h) {
+    for (int64_t i = 0; i < count; ++i) h[i] = g[i] / (1.0 + exp(-g[i])) * u[i];
 }
 
 /* Number of OpenMP threads the oracle runs with (1 without OpenMP). */

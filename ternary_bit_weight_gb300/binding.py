@@ -15,13 +15,17 @@ import os
 from . import build as _build
 
 TERN_OK = 0
+TERN_X_BF16, TERN_X_F16 = 0, 1
+TERN_OUT_F32, TERN_OUT_BF16, TERN_OUT_F16 = 0, 1, 2
 STATUS_NAMES = {0: "TERN_OK", 1: "TERN_ERR_NULL", 2: "TERN_ERR_SHAPE", 3: "TERN_ERR_ALIGN",
                 4: "TERN_ERR_SIZE", 5: "TERN_ERR_UNSUPPORTED", 6: "TERN_ERR_CUDA"}
 
 # Every symbol include/tern.h declares.
 EXPORTED = ("tern_status_string", "tern_version", "tern_pack", "tern_unpack", "tern_tiled_bytes",
             "tern_repack", "tern_unrepack", "tern_workspace_bytes", "tern_linear",
-            "tern_linear_multi", "tern_linear_noalloc")
+            "tern_linear_multi", "tern_linear_noalloc", "tern_linear_ex", "tern_tiled_glu_bytes",
+            "tern_repack_glu", "tern_swiglu_workspace_bytes", "tern_linear_swiglu",
+            "tern_workspace_error", "tern_workspace_reset")
 
 
 class TernError(RuntimeError):
@@ -59,6 +63,21 @@ def _load():
     lib.tern_linear_multi.restype = i32
     lib.tern_linear_noalloc.argtypes = [vp, i64, vp, i64, i64, i64, vp, i64, vp]
     lib.tern_linear_noalloc.restype = i32
+    lib.tern_linear_ex.argtypes = [vp, i32, i64, vp, i64, i64, i32, ctypes.POINTER(i64),
+                                   ctypes.POINTER(vp), ctypes.POINTER(i64), i32, vp, sz, vp]
+    lib.tern_linear_ex.restype = i32
+    lib.tern_tiled_glu_bytes.argtypes = [i64, i64]
+    lib.tern_tiled_glu_bytes.restype = sz
+    lib.tern_repack_glu.argtypes = [vp, vp, vp, vp, i64, i64, vp, sz, vp, vp]
+    lib.tern_repack_glu.restype = i32
+    lib.tern_swiglu_workspace_bytes.argtypes = [i64, i64, i64]
+    lib.tern_swiglu_workspace_bytes.restype = sz
+    lib.tern_linear_swiglu.argtypes = [vp, i32, i64, vp, i64, i64, i64, vp, i64, i32, vp, sz, vp]
+    lib.tern_linear_swiglu.restype = i32
+    lib.tern_workspace_error.argtypes = [vp, vp, vp]
+    lib.tern_workspace_error.restype = i32
+    lib.tern_workspace_reset.argtypes = [vp, sz, vp]
+    lib.tern_workspace_reset.restype = i32
     return lib
 
 
@@ -162,3 +181,57 @@ def tern_linear_noalloc(X, ldx: int, tiled, M: int, N: int, K: int, Y, ldy: int,
     """tern_linear with the library's built-in scratch instead of a workspace."""
     _check(_lib.tern_linear_noalloc(_p(X), ldx, _p(tiled), M, N, K, _p(Y), ldy, _s(stream)),
            "tern_linear_noalloc")
+
+
+def _nbytes(t):
+    return 0 if t is None or isinstance(t, int) else t.numel() * t.element_size()
+
+
+def tern_linear_ex(X, x_type: int, ldx: int, tiled, M: int, K: int, n_sizes, Ys, ldys, out_type: int,
+                   ws=None, ws_bytes: int | None = None, stream=None):
+    """Multi-output linear with the activation and output element types chosen."""
+    n_out = len(n_sizes)
+    sizes = (ctypes.c_int64 * n_out)(*[int(v) for v in n_sizes])
+    ptrs = (ctypes.c_void_p * n_out)(*[_p(y) for y in Ys])
+    lds = (ctypes.c_int64 * n_out)(*[int(v) for v in ldys])
+    if ws_bytes is None:
+        ws_bytes = _nbytes(ws)
+    _check(_lib.tern_linear_ex(_p(X), x_type, ldx, _p(tiled), M, K, n_out, sizes, ptrs, lds, out_type,
+                               _p(ws), ws_bytes, _s(stream)), "tern_linear_ex")
+
+
+def tern_tiled_glu_bytes(I: int, K: int) -> int:
+    return int(_lib.tern_tiled_glu_bytes(I, K))
+
+
+def tern_repack_glu(packed_gate, scales_gate, packed_up, scales_up, I: int, K: int, tiled,
+                    tiled_bytes: int | None = None, err=None, stream=None):
+    if tiled_bytes is None:
+        tiled_bytes = _nbytes(tiled)
+    _check(_lib.tern_repack_glu(_p(packed_gate), _p(scales_gate), _p(packed_up), _p(scales_up), I, K,
+                                _p(tiled), tiled_bytes, _p(err), _s(stream)), "tern_repack_glu")
+
+
+def tern_swiglu_workspace_bytes(M: int, I: int, K: int) -> int:
+    return int(_lib.tern_swiglu_workspace_bytes(M, I, K))
+
+
+def tern_linear_swiglu(X, x_type: int, ldx: int, tiled_glu, M: int, I: int, K: int, H, ldh: int,
+                       out_type: int, ws=None, ws_bytes: int | None = None, stream=None):
+    if ws_bytes is None:
+        ws_bytes = _nbytes(ws)
+    _check(_lib.tern_linear_swiglu(_p(X), x_type, ldx, _p(tiled_glu), M, I, K, _p(H), ldh, out_type,
+                                   _p(ws), ws_bytes, _s(stream)), "tern_linear_swiglu")
+
+
+def tern_workspace_error(ws, stream=None) -> int:
+    """The workspace's error word (waits for ``stream`` to reach this point)."""
+    out = ctypes.c_int32(0)
+    _check(_lib.tern_workspace_error(_p(ws), ctypes.addressof(out), _s(stream)), "tern_workspace_error")
+    return int(out.value)
+
+
+def tern_workspace_reset(ws, ws_bytes: int | None = None, stream=None):
+    if ws_bytes is None:
+        ws_bytes = _nbytes(ws)
+    _check(_lib.tern_workspace_reset(_p(ws), ws_bytes, _s(stream)), "tern_workspace_reset")

@@ -18,7 +18,7 @@ inline tern_status from_cuda(cudaError_t e) { return e == cudaSuccess ? TERN_OK 
 
 inline bool valid_group_shape(int64_t N, int64_t K) { return N >= 0 && K > 0 && K % tern::kGroup == 0; }
 
-tern_status run_linear(const uint16_t* X, int64_t ldx, const void* tiled, int64_t M, int64_t N,
+tern_status run_linear(const uint16_t* X, bool x_f16, int64_t ldx, const void* tiled, int64_t M, int64_t N,
                        int64_t K, const tern::OutputSplit& out, void* ws, size_t ws_bytes,
                        cudaStream_t stream) {
     const int sms = tern::device_sm_count();
@@ -30,11 +30,11 @@ tern_status run_linear(const uint16_t* X, int64_t ldx, const void* tiled, int64_
     if (M <= tern::kStreamMaxM) {
         const tern::StreamPlan plan = tern::plan_stream(M, N, K, sms);
         if (ws_bytes < plan.ws_bytes) return TERN_ERR_SIZE;
-        e = tern::launch_stream(X, ldx, w, M, N, K, out, ws, plan, stream);
+        e = tern::launch_stream(X, x_f16, ldx, w, M, N, K, out, ws, plan, stream);
     } else {
         const tern::GemmPlan plan = tern::plan_gemm(M, N, K, sms);
         if (ws_bytes < plan.ws_bytes) return TERN_ERR_SIZE;
-        e = tern::launch_gemm(X, ldx, w, M, N, K, out, ws, plan, stream);
+        e = tern::launch_gemm(X, x_f16, ldx, w, M, N, K, out, ws, plan, stream);
     }
     return e == cudaSuccess ? TERN_OK : TERN_ERR_CUDA;
 }
@@ -82,7 +82,7 @@ const char* tern_status_string(int status) {
     }
 }
 
-int tern_version(void) { return 10000; }
+int tern_version(void) { return 10100; }
 
 tern_status tern_pack(const int8_t* d_t, int64_t N, int64_t K, uint8_t* d_packed, int32_t* d_err,
                       void* stream) {
@@ -152,16 +152,27 @@ tern_status tern_linear(const uint16_t* d_X, int64_t ldx, const void* d_tiled, i
     out.offset[1] = N;
     out.y[0] = d_Y;
     out.ldy[0] = ldy;
-    return run_linear(d_X, ldx, d_tiled, M, N, K, out, d_ws, ws_bytes, as_stream(stream));
+    return run_linear(d_X, false, ldx, d_tiled, M, N, K, out, d_ws, ws_bytes, as_stream(stream));
 }
 
 tern_status tern_linear_multi(const uint16_t* d_X, int64_t ldx, const void* d_tiled, int64_t M,
                               int64_t K, int n_out, const int64_t* n_sizes, float* const* d_Ys,
                               const int64_t* ldys, void* d_ws, size_t ws_bytes, void* stream) {
+    return tern_linear_ex(d_X, TERN_X_BF16, ldx, d_tiled, M, K, n_out, n_sizes,
+                          reinterpret_cast<void* const*>(d_Ys), ldys, TERN_OUT_F32, d_ws, ws_bytes, stream);
+}
+
+tern_status tern_linear_ex(const void* d_X, int x_type, int64_t ldx, const void* d_tiled, int64_t M,
+                           int64_t K, int n_out, const int64_t* n_sizes, void* const* d_Ys,
+                           const int64_t* ldys, int out_type, void* d_ws, size_t ws_bytes, void* stream) {
+    if (x_type != TERN_X_BF16 && x_type != TERN_X_F16) return TERN_ERR_SHAPE;
+    if (out_type != TERN_OUT_F32 && out_type != TERN_OUT_BF16 && out_type != TERN_OUT_F16) return TERN_ERR_SHAPE;
     if (n_out < 1 || n_out > tern::kMaxOutputs) return TERN_ERR_SHAPE;
     if (n_sizes == nullptr || d_Ys == nullptr || ldys == nullptr) return TERN_ERR_NULL;
     tern::OutputSplit out = {};
     out.n_out = n_out;
+    out.bf16 = out_type == TERN_OUT_BF16 ? 1 : out_type == TERN_OUT_F16 ? 2 : 0;
+    const uintptr_t y_align = out.bf16 ? 2 : 4;
     int64_t N = 0;
     for (int j = 0; j < n_out; ++j) {
         if (n_sizes[j] < 0) return TERN_ERR_SHAPE;
@@ -171,17 +182,86 @@ tern_status tern_linear_multi(const uint16_t* d_X, int64_t ldx, const void* d_ti
     for (int j = n_out; j <= tern::kMaxOutputs; ++j) out.offset[j] = N;
     if (M < 0 || !valid_group_shape(N, K)) return TERN_ERR_SHAPE;
     if (M == 0 || N == 0) return TERN_OK;
-    tern_status st = check_x_w(d_X, ldx, d_tiled, M, K);
+    const uint16_t* X = static_cast<const uint16_t*>(d_X);
+    tern_status st = check_x_w(X, ldx, d_tiled, M, K);
     if (st != TERN_OK) return st;
     for (int j = 0; j < n_out; ++j) {
         if (n_sizes[j] == 0) { out.y[j] = nullptr; out.ldy[j] = 0; continue; }
         if (d_Ys[j] == nullptr) return TERN_ERR_NULL;
         if (ldys[j] < n_sizes[j]) return TERN_ERR_SHAPE;
-        if (!aligned(d_Ys[j], 4)) return TERN_ERR_ALIGN;
+        if (!aligned(d_Ys[j], y_align)) return TERN_ERR_ALIGN;
         out.y[j] = d_Ys[j];
         out.ldy[j] = ldys[j];
     }
-    return run_linear(d_X, ldx, d_tiled, M, N, K, out, d_ws, ws_bytes, as_stream(stream));
+    return run_linear(X, x_type == TERN_X_F16, ldx, d_tiled, M, N, K, out, d_ws, ws_bytes, as_stream(stream));
+}
+
+size_t tern_tiled_glu_bytes(int64_t I, int64_t K) {
+    if (I < 0) return 0;
+    return tern_tiled_bytes(tern::glu_rows(I), K);
+}
+
+tern_status tern_repack_glu(const uint8_t* d_packed_gate, const uint16_t* d_scales_gate,
+                            const uint8_t* d_packed_up, const uint16_t* d_scales_up, int64_t I, int64_t K,
+                            void* d_tiled, size_t tiled_bytes, int32_t* d_err, void* stream) {
+    if (!valid_group_shape(I, K)) return TERN_ERR_SHAPE;
+    if (I == 0) return TERN_OK;
+    if (d_packed_gate == nullptr || d_scales_gate == nullptr || d_packed_up == nullptr ||
+        d_scales_up == nullptr || d_tiled == nullptr)
+        return TERN_ERR_NULL;
+    if (!aligned(d_packed_gate, 4) || !aligned(d_packed_up, 4) || !aligned(d_scales_gate, 2) ||
+        !aligned(d_scales_up, 2) || !aligned(d_tiled, 16))
+        return TERN_ERR_ALIGN;
+    if (d_err != nullptr && !aligned(d_err, 4)) return TERN_ERR_ALIGN;
+    if (tiled_bytes < tern_tiled_glu_bytes(I, K)) return TERN_ERR_SIZE;
+    return from_cuda(tern::launch_repack_glu(d_packed_gate, d_scales_gate, d_packed_up, d_scales_up, I, K,
+                                             static_cast<uint8_t*>(d_tiled), d_err, as_stream(stream)));
+}
+
+size_t tern_swiglu_workspace_bytes(int64_t M, int64_t I, int64_t K) {
+    if (I <= 0) return 0;
+    return tern_workspace_bytes(M, tern::glu_rows(I), K);
+}
+
+tern_status tern_linear_swiglu(const void* d_X, int x_type, int64_t ldx, const void* d_tiled_glu, int64_t M,
+                               int64_t I, int64_t K, void* d_H, int64_t ldh, int out_type, void* d_ws,
+                               size_t ws_bytes, void* stream) {
+    if (x_type != TERN_X_BF16 && x_type != TERN_X_F16) return TERN_ERR_SHAPE;
+    if (out_type != TERN_OUT_F32 && out_type != TERN_OUT_BF16 && out_type != TERN_OUT_F16) return TERN_ERR_SHAPE;
+    if (M < 0 || !valid_group_shape(I, K)) return TERN_ERR_SHAPE;
+    if (M == 0 || I == 0) return TERN_OK;
+    const uint16_t* X = static_cast<const uint16_t*>(d_X);
+    tern_status st = check_x_w(X, ldx, d_tiled_glu, M, K);
+    if (st != TERN_OK) return st;
+    if (d_H == nullptr) return TERN_ERR_NULL;
+    if (ldh < I) return TERN_ERR_SHAPE;
+    if (!aligned(d_H, out_type == TERN_OUT_F32 ? 4 : 2)) return TERN_ERR_ALIGN;
+    const int64_t N = tern::glu_rows(I);
+    tern::OutputSplit out = {};
+    out.n_out = 1;
+    out.bf16 = out_type == TERN_OUT_BF16 ? 1 : out_type == TERN_OUT_F16 ? 2 : 0;
+    out.glu = 1;
+    out.glu_cols = I;
+    out.offset[0] = 0;
+    for (int j = 1; j <= tern::kMaxOutputs; ++j) out.offset[j] = N;
+    out.y[0] = d_H;
+    out.ldy[0] = ldh;
+    return run_linear(X, x_type == TERN_X_F16, ldx, d_tiled_glu, M, N, K, out, d_ws, ws_bytes, as_stream(stream));
+}
+
+tern_status tern_workspace_error(const void* d_ws, int32_t* h_err, void* stream) {
+    if (d_ws == nullptr || h_err == nullptr) return TERN_ERR_NULL;
+    if (!aligned(d_ws, 256)) return TERN_ERR_ALIGN;
+    cudaError_t e = cudaMemcpyAsync(h_err, d_ws, sizeof(int32_t), cudaMemcpyDeviceToHost, as_stream(stream));
+    if (e == cudaSuccess) e = cudaStreamSynchronize(as_stream(stream));
+    return from_cuda(e);
+}
+
+tern_status tern_workspace_reset(void* d_ws, size_t ws_bytes, void* stream) {
+    if (d_ws == nullptr) return TERN_ERR_NULL;
+    if (!aligned(d_ws, 256)) return TERN_ERR_ALIGN;
+    if (ws_bytes == 0) return TERN_OK;
+    return from_cuda(cudaMemsetAsync(d_ws, 0, ws_bytes, as_stream(stream)));
 }
 
 }  // extern "C"

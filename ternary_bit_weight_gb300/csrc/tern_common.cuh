@@ -123,6 +123,20 @@ __device__ __forceinline__ void decode_word_bf16(uint32_t w, const DecodeConsts&
     }
 }
 
+// All eight fp16x2 pairs of one code word, t exact in fp16 (for fp16
+// activations).
+__device__ __forceinline__ void decode_word_f16(uint32_t w, const DecodeConsts& k, uint32_t* out) {
+    const uint32_t w8 = w >> 8;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t r = merge_field(h == 0 ? w : w8, k.mask[i], k.base);
+            asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(out[4 * h + i]) : "r"(r), "r"(k.mul[i]), "r"(k.add[i]));
+        }
+    }
+}
+
 // fp16 variant: t as exact fp16 (+-1, 0), then times the row's FP16 scale
 // s (given in both halves): t * s is exactly +-s or 0.
 __device__ __forceinline__ void decode_word_fp16_scaled(uint32_t w, uint32_t s2, const DecodeConsts& k, uint32_t* out) {
@@ -153,37 +167,51 @@ __device__ __forceinline__ int output_of(const OutputSplit& out, int64_t n) {
     return j;
 }
 
-// Store y as output element (m, n) of the concatenated N.
-__device__ __forceinline__ void store_y(const OutputSplit& out, int m, int64_t n, float v) {
-    const int j = output_of(out, n);
-    const int64_t idx = (int64_t)m * out.ldy[j] + (n - out.offset[j]);
-    if (out.bf16)
-        static_cast<__nv_bfloat16*>(out.y[j])[idx] = __float2bfloat16_rn(v);
-    else
-        static_cast<float*>(out.y[j])[idx] = v;
-}
-
 // Output row n of the concatenated N: address of element (m = 0, n) and the
 // stride between tokens, so that a thread owning one row stores with one
 // multiply-add per element.
 struct RowOut {
     char* base;
     int64_t ld;
-    int bf16;
+    int otype;   // 0 fp32, 1 bf16, 2 fp16
 };
 __device__ __forceinline__ RowOut row_out(const OutputSplit& out, int64_t n) {
-    const int j = output_of(out, n);
+    const int j = out.glu ? 0 : output_of(out, n);
     RowOut o;
     o.base = static_cast<char*>(out.y[j]) + (n - out.offset[j]) * (out.bf16 ? 2 : 4);
     o.ld = out.ldy[j];
-    o.bf16 = out.bf16;
+    o.otype = out.bf16;
     return o;
 }
-__device__ __forceinline__ void store_row(const RowOut& o, int m, float v) {
-    if (o.bf16)
-        reinterpret_cast<__nv_bfloat16*>(o.base)[(int64_t)m * o.ld] = __float2bfloat16_rn(v);
+__device__ __forceinline__ void store_elem(void* base, int64_t idx, int otype, float v) {
+    if (otype == 1)
+        static_cast<__nv_bfloat16*>(base)[idx] = __float2bfloat16_rn(v);
+    else if (otype == 2)
+        static_cast<__half*>(base)[idx] = __float2half_rn(v);
     else
-        reinterpret_cast<float*>(o.base)[(int64_t)m * o.ld] = v;
+        static_cast<float*>(base)[idx] = v;
+}
+__device__ __forceinline__ void store_row(const RowOut& o, int m, float v) {
+    store_elem(o.base, (int64_t)m * o.ld, o.otype, v);
+}
+
+// Final value v of output (m, row), the row being lane (row mod 32) of the
+// calling warp; every lane of the warp calls with the same m.  `live`: the
+// row exists (row < N).  With the GLU layout the partner lane (lane ^ 16)
+// holds the matching up (or gate) value, and the gate lane stores
+// silu(gate) * up in fp32 at column 16*(row/32) + row%32.
+__device__ __forceinline__ void store_out(const OutputSplit& out, const RowOut& o, int m, int64_t row, float v,
+                                          bool live) {
+    if (out.glu) {
+        const float u = __shfl_xor_sync(0xffffffffu, v, 16);
+        const int64_t i = (row >> 5) * 16 + (row & 15);
+        if ((row & 16) == 0 && i < out.glu_cols) {
+            const float h = v / (1.0f + expf(-v)) * u;
+            store_elem(out.y[0], (int64_t)m * out.ldy[0] + i, out.bf16, h);
+        }
+    } else if (live) {
+        store_row(o, m, v);
+    }
 }
 
 }  // namespace tern

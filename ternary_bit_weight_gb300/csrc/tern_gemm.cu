@@ -447,10 +447,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
                             tmem_ld32_sync(tm + rt * NT + c, d);
                         else
                             tmem_ld16_sync(tm + rt * NT + c, d);
-                        if (live)
 #pragma unroll
-                            for (int m = 0; m < 32; ++m)
-                                if (c + m < mvalid) store_row(o, m0 + c + m, __uint_as_float(d[m]) * inv[m]);
+                        for (int m = 0; m < 32; ++m)
+                            if (c + m < mvalid) store_out(a.out, o, m0 + c + m, row, __uint_as_float(d[m]) * inv[m], live);
                     }
                 }
                 tc_fence_before_sync();
@@ -505,10 +504,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
                             }
                             float inv[16];
                             load_inv(a.inv_scale + m0 + c, inv);
-                            if (live)
 #pragma unroll
-                                for (int m = 0; m < 16; ++m)
-                                    if (c + m < mvalid) store_row(o, m0 + c + m, v[m] * inv[m]);
+                            for (int m = 0; m < 16; ++m)
+                                if (c + m < mvalid) store_out(a.out, o, m0 + c + m, row, v[m] * inv[m], live);
                         }
                     }
                     if (r == 0) a.counters[tile] = 0;   // leave the workspace zeroed
@@ -529,7 +527,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
 
 // Activation rows -> fp16 scaled by 2^c_m (largest magnitude in [2^14,
 // 2^15)), and 2^-c_m per row.  One CTA per row.
-__global__ void __launch_bounds__(256) xprep_kernel(const uint16_t* __restrict__ X, int64_t ldx, int K,
+__device__ __forceinline__ float x_lo(uint32_t w, int x_f16) {
+    return x_f16 ? __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xFFFFu))) : __uint_as_float(w << 16);
+}
+__device__ __forceinline__ float x_hi(uint32_t w, int x_f16) {
+    return x_f16 ? __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16))) : __uint_as_float(w & 0xFFFF0000u);
+}
+
+__global__ void __launch_bounds__(256) xprep_kernel(const uint16_t* __restrict__ X, int x_f16, int64_t ldx, int K,
                                                      __half* __restrict__ X16, float* __restrict__ inv_scale) {
     const int m = blockIdx.x;
     const uint16_t* xr = X + (int64_t)m * ldx;
@@ -541,8 +546,8 @@ __global__ void __launch_bounds__(256) xprep_kernel(const uint16_t* __restrict__
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            mx = fmaxf(mx, fabsf(__uint_as_float(w[i] << 16)));
-            mx = fmaxf(mx, fabsf(__uint_as_float(w[i] & 0xFFFF0000u)));
+            mx = fmaxf(mx, fabsf(x_lo(w[i], x_f16)));
+            mx = fmaxf(mx, fabsf(x_hi(w[i], x_f16)));
         }
     }
 #pragma unroll
@@ -569,8 +574,8 @@ __global__ void __launch_bounds__(256) xprep_kernel(const uint16_t* __restrict__
         uint32_t o[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const __half lo = __float2half_rn(__uint_as_float(w[i] << 16) * scale);
-            const __half hi = __float2half_rn(__uint_as_float(w[i] & 0xFFFF0000u) * scale);
+            const __half lo = __float2half_rn(x_lo(w[i], x_f16) * scale);
+            const __half hi = __float2half_rn(x_hi(w[i], x_f16) * scale);
             o[i] = static_cast<uint32_t>(__half_as_ushort(lo)) | (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
         }
         *reinterpret_cast<uint4*>(yr + k) = make_uint4(o[0], o[1], o[2], o[3]);
@@ -641,8 +646,8 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sm_count) {
     return p;
 }
 
-cudaError_t launch_gemm(const uint16_t* X, int64_t ldx, const uint8_t* tiled, int64_t M, int64_t N, int64_t K,
-                        const OutputSplit& out, void* ws, const GemmPlan& plan, cudaStream_t stream) {
+cudaError_t launch_gemm(const uint16_t* X, bool x_f16, int64_t ldx, const uint8_t* tiled, int64_t M, int64_t N,
+                        int64_t K, const OutputSplit& out, void* ws, const GemmPlan& plan, cudaStream_t stream) {
     uint8_t* w = static_cast<uint8_t*>(ws);
     __half* x16 = reinterpret_cast<__half*>(w + plan.off_x16);
     float* inv = reinterpret_cast<float*>(w + plan.off_inv);
@@ -657,7 +662,7 @@ cudaError_t launch_gemm(const uint16_t* X, int64_t ldx, const uint8_t* tiled, in
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        cudaError_t e = cudaLaunchKernelEx(&cfg, xprep_kernel, X, ldx, static_cast<int>(K), x16, inv);
+        cudaError_t e = cudaLaunchKernelEx(&cfg, xprep_kernel, X, x_f16 ? 1 : 0, ldx, static_cast<int>(K), x16, inv);
         if (e != cudaSuccess) return e;
     }
     EncodeTiledFn enc = encode_tiled_fn();

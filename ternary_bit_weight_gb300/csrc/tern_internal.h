@@ -15,6 +15,13 @@ cudaError_t launch_unpack(const uint8_t* packed, int64_t count, int8_t* t, int32
                           cudaStream_t stream);
 cudaError_t launch_repack(const uint8_t* packed, const uint16_t* scales, int64_t N, int64_t K,
                           uint8_t* tiled, int32_t* err, cudaStream_t stream);
+// GLU layout: gate and up rows interleaved in blocks of 16 (tiled row n is
+// gate row 16*(n/32) + n%32 when n%32 < 16, else the up row of that index);
+// glu_rows(I) combined rows, padded with zero rows.
+constexpr int64_t glu_rows(int64_t I) { return 2 * ((I + 15) / 16) * 16; }
+cudaError_t launch_repack_glu(const uint8_t* packed_gate, const uint16_t* scales_gate, const uint8_t* packed_up,
+                              const uint16_t* scales_up, int64_t I, int64_t K, uint8_t* tiled, int32_t* err,
+                              cudaStream_t stream);
 cudaError_t launch_unrepack(const uint8_t* tiled, int64_t N, int64_t K, uint8_t* packed,
                             uint16_t* scales, int32_t* err, cudaStream_t stream);
 
@@ -23,10 +30,15 @@ constexpr int kMaxOutputs = 4;
 
 // Where the rows of the concatenated N go: rows [offset[j], offset[j+1])
 // to output j, element (m, n) at y[j][m * ldy[j] + n - offset[j]], stored as
-// fp32 or (bf16 != 0) as bf16 rounded to nearest even.
+// fp32, bf16 or fp16 (rounded to nearest even).
+// glu != 0: the rows are the GLU interleave of gate and up (see glu_rows);
+// the one output y[0] receives h[m, i] = silu(gate[m, i]) * up[m, i] for
+// i < glu_cols at y[0][m * ldy[0] + i].
 struct OutputSplit {
     int n_out;
-    int bf16;
+    int bf16;      // 1: bf16 output, 2: fp16 output, 0: fp32
+    int glu;
+    int64_t glu_cols;
     int64_t offset[kMaxOutputs + 1];
     void* y[kMaxOutputs];
     int64_t ldy[kMaxOutputs];
@@ -54,8 +66,9 @@ struct StreamPlan {
 
 StreamPlan plan_stream(int64_t M, int64_t N, int64_t K, int sm_count);
 
-cudaError_t launch_stream(const uint16_t* X, int64_t ldx, const uint8_t* tiled, int64_t M, int64_t N,
-                          int64_t K, const OutputSplit& out, void* ws, const StreamPlan& plan,
+// x_f16: X holds fp16 rather than bf16 bits.
+cudaError_t launch_stream(const uint16_t* X, bool x_f16, int64_t ldx, const uint8_t* tiled, int64_t M,
+                          int64_t N, int64_t K, const OutputSplit& out, void* ws, const StreamPlan& plan,
                           cudaStream_t stream);
 
 // Tensor-core GEMM plan for M > kStreamMaxM: items of 256 weight rows x NT
@@ -75,8 +88,8 @@ struct GemmPlan {
 
 GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sm_count);
 
-cudaError_t launch_gemm(const uint16_t* X, int64_t ldx, const uint8_t* tiled, int64_t M, int64_t N, int64_t K,
-                        const OutputSplit& out, void* ws, const GemmPlan& plan, cudaStream_t stream);
+cudaError_t launch_gemm(const uint16_t* X, bool x_f16, int64_t ldx, const uint8_t* tiled, int64_t M, int64_t N,
+                        int64_t K, const OutputSplit& out, void* ws, const GemmPlan& plan, cudaStream_t stream);
 
 // Size of the error word + padding at the start of every linear workspace.
 constexpr size_t kWorkspaceErrBytes = 256;

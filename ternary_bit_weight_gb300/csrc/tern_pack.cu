@@ -1,6 +1,9 @@
-// Byte-format kernels of libtern: pack, unpack, repack (disk -> tiled) and
-// unrepack (tiled -> disk).  All are memory-bound single passes, one thread
-// per 32-bit output word, and bit-exact by construction.  Every thread
+// Byte-format kernels of libtern: pack, unpack, repack (disk -> tiled, also
+// into the GLU-interleaved layout) and unrepack (tiled -> disk).  All are
+// memory-bound single passes and bit-exact by construction: pack, unpack and
+// unrepack with one thread per 32-bit output word, repack with one thread
+// per (unit, row) so that its reads are whole DRAM sectors and its writes
+// whole 512-byte runs per warp.  Every thread
 // fences its writes before exiting, so that a following linear-layer kernel
 // that starts early (programmatic dependent launch) and streams weights
 // before its grid dependency resolves sees them.
@@ -116,14 +119,18 @@ __device__ __forceinline__ uint32_t disk_to_tiled_word(uint32_t src, int& bad) {
     // v = t + 1: code 01 (+1) -> 10, code 10 (-1) -> 00, codes 00/11 -> 01
     const uint32_t v_bit1 = lo & ~hi;
     const uint32_t v_bit0 = ~(lo ^ hi) & 0x55555555u;
-    const uint32_t v = v_bit0 | (v_bit1 << 1);
-    uint32_t out = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        out |= ((v >> (4 * i)) & 3u) << (2 * i);            // weight 2i
-        out |= ((v >> (4 * i + 2)) & 3u) << (16 + 2 * i);   // weight 2i+1
-    }
-    return out;
+    uint32_t v = v_bit0 | (v_bit1 << 1);
+    // Field i (weight k0+i) moves to field (i mod 2)*8 + i/2: a rotation of
+    // the four bits of the field index, done as three exchanges of adjacent
+    // index bits (bits 0-1, 1-2, 2-3), each one masked swap of fields.
+    auto swap_fields = [](uint32_t x, uint32_t mask, int shift) {
+        const uint32_t t = ((x >> shift) ^ x) & mask;
+        return x ^ t ^ (t << shift);
+    };
+    v = swap_fields(v, 0x0C0C0C0Cu, 2);
+    v = swap_fields(v, 0x00F000F0u, 4);
+    v = swap_fields(v, 0x0000FF00u, 8);
+    return v;
 }
 
 // Tiled word -> disk word (inverse of the above; v = 3 gives code 00 and counts).
@@ -161,27 +168,69 @@ __device__ __forceinline__ void tiled_scale_coords(int64_t j, int64_t G, int64_t
     n_lo = kTileRows * b + 2 * r2;
 }
 
+// Where the tiled rows come from: row n of one source, or (GLU) blocks of
+// 16 rows taken alternately from the gate and the up source, so that tiled
+// row n is gate row 16*(n/32) + n%32 when n%32 < 16 and the up row of the
+// same index otherwise.
+struct RepackSrc {
+    const uint8_t* packed[2];
+    const uint16_t* scales[2];
+    int64_t rows;   // rows per source
+    int glu;
+};
+
+__device__ __forceinline__ bool source_row(const RepackSrc& s, int64_t n, int& which, int64_t& row) {
+    if (!s.glu) {
+        which = 0;
+        row = n;
+    } else {
+        const int j = static_cast<int>(n & 31);
+        which = j >> 4;
+        row = (n >> 5) * 16 + (j & 15);
+    }
+    return row < s.rows;
+}
+
+// One thread per (unit, row): the row's 32 disk bytes of the group (one
+// DRAM sector) become its two 16-byte runs of the unit (a warp writes 512
+// contiguous bytes per run) and its scale.  VEC: the sources are 16-byte
+// aligned, so the 32 bytes come in two vector loads.
+template <bool VEC>
 __global__ void __launch_bounds__(kThreads)
-repack_kernel(const uint8_t* __restrict__ packed, const uint16_t* __restrict__ scales, int64_t N,
-              int64_t K, int64_t code_words, int64_t scale_words, uint32_t* __restrict__ tiled,
-              int32_t* err) {
+repack_kernel(const RepackSrc src, int64_t K, int64_t units, uint8_t* __restrict__ tiled, int32_t* err) {
     const int64_t G = K / kGroup;
+    const int64_t row_bytes = K / 4;
+    uint16_t* tscales = reinterpret_cast<uint16_t*>(tiled + units * kUnitCodeBytes);
     int bad = 0;
-    for (int64_t i = blockIdx.x * (int64_t)kThreads + threadIdx.x; i < code_words + scale_words;
+    for (int64_t i = blockIdx.x * (int64_t)kThreads + threadIdx.x; i < units * kTileRows;
          i += (int64_t)gridDim.x * kThreads) {
-        if (i < code_words) {
-            int64_t n, k0;
-            tiled_word_coords(i, G, n, k0);
-            uint32_t src = 0;   // padding rows: code 00 (weight 0)
-            if (n < N) src = *reinterpret_cast<const uint32_t*>(packed + n * (K / 4) + k0 / 4);
-            tiled[i] = disk_to_tiled_word(src, bad);
-        } else {
-            int64_t n_lo, g;
-            tiled_scale_coords(i - code_words, G, n_lo, g);
-            const uint32_t s_lo = n_lo < N ? scales[n_lo * G + g] : 0u;
-            const uint32_t s_hi = n_lo + 1 < N ? scales[(n_lo + 1) * G + g] : 0u;
-            tiled[i] = s_lo | (s_hi << 16);
+        const int64_t unit = i >> 7;
+        const int r = static_cast<int>(i & 127);
+        const int64_t b = unit / G, g = unit - b * G;
+        int which;
+        int64_t row;
+        const bool valid = source_row(src, b * kTileRows + r, which, row);
+        uint32_t w[8] = {0, 0, 0, 0, 0, 0, 0, 0};   // padding rows: code 00, weight 0
+        uint16_t sc = 0;
+        if (valid) {
+            const uint8_t* p = (which ? src.packed[1] : src.packed[0]) + row * row_bytes + 32 * g;
+            if (VEC) {
+                const uint4 a = __ldg(reinterpret_cast<const uint4*>(p));
+                const uint4 c = __ldg(reinterpret_cast<const uint4*>(p) + 1);
+                w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+                w[4] = c.x; w[5] = c.y; w[6] = c.z; w[7] = c.w;
+            } else {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) w[q] = __ldg(reinterpret_cast<const uint32_t*>(p) + q);
+            }
+            sc = __ldg((which ? src.scales[1] : src.scales[0]) + row * G + g);
         }
+        uint8_t* u = tiled + unit * kUnitCodeBytes + 16 * r;
+        *reinterpret_cast<uint4*>(u) = make_uint4(disk_to_tiled_word(w[0], bad), disk_to_tiled_word(w[1], bad),
+                                                  disk_to_tiled_word(w[2], bad), disk_to_tiled_word(w[3], bad));
+        *reinterpret_cast<uint4*>(u + 2048) = make_uint4(disk_to_tiled_word(w[4], bad), disk_to_tiled_word(w[5], bad),
+                                                         disk_to_tiled_word(w[6], bad), disk_to_tiled_word(w[7], bad));
+        tscales[unit * kTileRows + r] = sc;
     }
     __threadfence();   // writes visible GPU-wide before exit (early-starting successors)
     count_errors(err, bad);
@@ -262,11 +311,31 @@ cudaError_t launch_unpack(const uint8_t* packed, int64_t count, int8_t* t, int32
 
 cudaError_t launch_repack(const uint8_t* packed, const uint16_t* scales, int64_t N, int64_t K,
                           uint8_t* tiled, int32_t* err, cudaStream_t stream) {
-    const int64_t R = ceil_div(N, kTileRows), G = K / kGroup;
-    const int64_t code_words = R * G * (kUnitCodeBytes / 4);
-    const int64_t scale_words = R * G * (kUnitScaleBytes / 4);
-    return launch_flat(repack_kernel, code_words + scale_words, stream, packed, scales, N, K,
-                       code_words, scale_words, reinterpret_cast<uint32_t*>(tiled), err);
+    RepackSrc src = {};
+    src.packed[0] = src.packed[1] = packed;
+    src.scales[0] = src.scales[1] = scales;
+    src.rows = N;
+    src.glu = 0;
+    const int64_t units = ceil_div(N, kTileRows) * (K / kGroup);
+    const bool vec = (reinterpret_cast<uintptr_t>(packed) & 15) == 0;
+    return vec ? launch_flat(repack_kernel<true>, units * kTileRows, stream, src, K, units, tiled, err)
+               : launch_flat(repack_kernel<false>, units * kTileRows, stream, src, K, units, tiled, err);
+}
+
+cudaError_t launch_repack_glu(const uint8_t* packed_gate, const uint16_t* scales_gate, const uint8_t* packed_up,
+                              const uint16_t* scales_up, int64_t I, int64_t K, uint8_t* tiled, int32_t* err,
+                              cudaStream_t stream) {
+    RepackSrc src = {};
+    src.packed[0] = packed_gate;
+    src.packed[1] = packed_up;
+    src.scales[0] = scales_gate;
+    src.scales[1] = scales_up;
+    src.rows = I;
+    src.glu = 1;
+    const int64_t units = ceil_div(glu_rows(I), kTileRows) * (K / kGroup);
+    const bool vec = ((reinterpret_cast<uintptr_t>(packed_gate) | reinterpret_cast<uintptr_t>(packed_up)) & 15) == 0;
+    return vec ? launch_flat(repack_kernel<true>, units * kTileRows, stream, src, K, units, tiled, err)
+               : launch_flat(repack_kernel<false>, units * kTileRows, stream, src, K, units, tiled, err);
 }
 
 cudaError_t launch_unrepack(const uint8_t* tiled, int64_t N, int64_t K, uint8_t* packed,

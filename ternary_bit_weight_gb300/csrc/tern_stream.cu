@@ -156,11 +156,12 @@ __device__ __forceinline__ void flush_tile(const StreamArgs& a, int64_t v, int64
     const int lane = r & 31, quad = r >> 5;
     const int64_t row = b * kTileRows + r;
     const int mvalid = a.M < NCOL ? a.M : NCOL;
+    const bool live = row < a.N;
+    const RowOut o = row_out(a.out, live ? row : 0);
     if (whole) {
-        if (row < a.N)
 #pragma unroll
-            for (int m = 0; m < NCOL; ++m)
-                if (m < mvalid) store_y(a.out, m, row, acc[m]);
+        for (int m = 0; m < NCOL; ++m)
+            if (m < mvalid) store_out(a.out, o, m, row, acc[m], live);
         return;
     }
     const int64_t slot = 2 * v + (b == first_tile ? 0 : 1);
@@ -195,10 +196,9 @@ __device__ __forceinline__ void flush_tile(const StreamArgs& a, int64_t v, int64
         for (int m = 0; m < NCOL; ++m)
             if (m < mvalid) sum[m] += __ldcg(src + m * kTileRows);
     }
-    if (row < a.N)
 #pragma unroll
-        for (int m = 0; m < NCOL; ++m)
-            if (m < mvalid) store_y(a.out, m, row, sum[m]);
+    for (int m = 0; m < NCOL; ++m)
+        if (m < mvalid) store_out(a.out, o, m, row, sum[m], live);
     if (lane == 0) *counter = 0;   // leave the workspace zeroed
 }
 
@@ -217,7 +217,7 @@ __device__ __forceinline__ bool vote_wait(uint32_t bar, uint32_t parity, bool ac
     return __all_sync(0xffffffffu, got);
 }
 
-template <bool ONE>
+template <bool ONE, bool XF16>
 __global__ void __launch_bounds__(kThreads, 1)
 stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
     using C = SCfg<ONE>;
@@ -343,7 +343,7 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
         // order between MMA warps does not matter.
         const int m = mma_index(warp);
         constexpr int kMmaWarps = C::MmaWarps;
-        constexpr uint32_t idesc = idesc_bf16_f32(128, kNtok);
+        constexpr uint32_t idesc = XF16 ? idesc_fp16_f32(128, kNtok) : idesc_bf16_f32(128, kNtok);
         bool ok = true;
         int32_t g = static_cast<int32_t>((u0 + m) % G);   // group of unit j
         // B descriptors: M == 1 the resident row (+16 per group, +2 per K-step);
@@ -433,7 +433,7 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
         const int q = (warp - kDecWarp0) >> 2;
         const int r = threadIdx.x & 127;   // weight row in the tile = tensor-memory lane
         const uint32_t tm = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + q * kAQ * kACols;
-        const DecodeConsts dk = decode_consts_bf16();
+        const DecodeConsts dk = XF16 ? decode_consts_fp16() : decode_consts_bf16();
         const int codes_off = C::OffCodes + 16 * r;   // + unit in stage * 4096 (+ 2048 second half)
         const uint32_t bar_afull = cb + kBarAFull + 8 * kAQ * q;
         const uint32_t bar_aempty = cb + kBarAEmpty + 8 * kAQ * q;
@@ -459,14 +459,14 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
             }
             {
                 uint32_t p[64];
-                decode_word_bf16(c0.x, dk, p);
-                decode_word_bf16(c0.y, dk, p + 8);
-                decode_word_bf16(c0.z, dk, p + 16);
-                decode_word_bf16(c0.w, dk, p + 24);
-                decode_word_bf16(c1.x, dk, p + 32);
-                decode_word_bf16(c1.y, dk, p + 40);
-                decode_word_bf16(c1.z, dk, p + 48);
-                decode_word_bf16(c1.w, dk, p + 56);
+                const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if (XF16)
+                        decode_word_f16(cw[i], dk, p + 8 * i);
+                    else
+                        decode_word_bf16(cw[i], dk, p + 8 * i);
+                }
                 tmem_st_32x32b_x64(tm + al * kACols, p);
             }
             tmem_st_wait();
@@ -580,17 +580,18 @@ EncodeTiledFn encode_tiled_fn() {
     return fn;
 }
 
-template <bool ONE>
+template <bool ONE, bool XF16>
 cudaError_t set_smem_limit() {
     static cudaError_t status = cudaErrorUnknown;
     static std::once_flag once;
     std::call_once(once, [] {
-        status = cudaFuncSetAttribute(stream_kernel<ONE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+        status = cudaFuncSetAttribute(stream_kernel<ONE, XF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      kSmemLimit);
     });
     return status;
 }
 
-template <bool ONE>
+template <bool ONE, bool XF16>
 cudaError_t launch_one(const uint16_t* X, int64_t ldx, const StreamArgs& a, const StreamPlan& plan,
                        cudaStream_t stream) {
     CUtensorMap map;
@@ -603,12 +604,12 @@ cudaError_t launch_one(const uint16_t* X, int64_t ldx, const StreamArgs& a, cons
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldx) * 2};
         const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kNtok)};
         const cuuint32_t estr[2] = {1, 1};
-        if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(X), dims, strides, box, estr,
+        if (enc(&map, XF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(X), dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    cudaError_t e = set_smem_limit<ONE>();
+    cudaError_t e = set_smem_limit<ONE, XF16>();
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(plan.grid));
@@ -620,7 +621,7 @@ cudaError_t launch_one(const uint16_t* X, int64_t ldx, const StreamArgs& a, cons
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, stream_kernel<ONE>, map, a);
+    return cudaLaunchKernelEx(&cfg, stream_kernel<ONE, XF16>, map, a);
 }
 
 }  // namespace
@@ -650,8 +651,8 @@ StreamPlan plan_stream(int64_t M, int64_t N, int64_t K, int sm_count) {
     return p;
 }
 
-cudaError_t launch_stream(const uint16_t* X, int64_t ldx, const uint8_t* tiled, int64_t M, int64_t N,
-                          int64_t K, const OutputSplit& out, void* ws, const StreamPlan& plan,
+cudaError_t launch_stream(const uint16_t* X, bool x_f16, int64_t ldx, const uint8_t* tiled, int64_t M,
+                          int64_t N, int64_t K, const OutputSplit& out, void* ws, const StreamPlan& plan,
                           cudaStream_t stream) {
     StreamArgs a = {};
     a.codes = tiled;
@@ -671,7 +672,11 @@ cudaError_t launch_stream(const uint16_t* X, int64_t ldx, const uint8_t* tiled, 
     a.err = reinterpret_cast<int*>(w);
     a.counters = reinterpret_cast<int*>(w + kWorkspaceErrBytes);
     a.slots = reinterpret_cast<float*>(w + kWorkspaceErrBytes + static_cast<size_t>(round_up(plan.R * 4 * 4, 256)));
-    return plan.one ? launch_one<true>(X, ldx, a, plan, stream) : launch_one<false>(X, ldx, a, plan, stream);
+    if (x_f16)
+        return plan.one ? launch_one<true, true>(X, ldx, a, plan, stream)
+                        : launch_one<false, true>(X, ldx, a, plan, stream);
+    return plan.one ? launch_one<true, false>(X, ldx, a, plan, stream)
+                    : launch_one<false, false>(X, ldx, a, plan, stream);
 }
 
 }  // namespace tern

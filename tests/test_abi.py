@@ -44,7 +44,7 @@ def test_status_strings_and_version():
     for code, name in binding.STATUS_NAMES.items():
         assert binding.status_string(code).startswith(name)
     assert binding.status_string(99) == "TERN_ERR_UNKNOWN"
-    assert binding.tern_version() == 10000
+    assert binding.tern_version() == 10100
 
 
 @pytest.mark.parametrize("N,K", [(1, 128), (16, 128), (17, 256), (5120, 5120), (55296, 5120),
@@ -140,3 +140,48 @@ def test_product_package_never_imports_the_oracle():
             if fn.endswith((".py", ".cu", ".cuh", ".h", ".c", ".cpp")):
                 text = open(os.path.join(dirpath, fn)).read()
                 assert "oracle" not in text.replace("oracle_", ""), fn
+
+
+def test_linear_ex_and_swiglu_argument_errors():
+    lib = binding.library()
+    i64 = ctypes.c_int64
+    sizes = (i64 * 1)(64)
+    ptrs = (ctypes.c_void_p * 1)(FAKE)
+    lds = (i64 * 1)(64)
+    f = lib.tern_linear_ex
+    assert f(FAKE, 2, 256, FAKE, 1, 256, 1, sizes, ptrs, lds, 0, None, 0, None) == 2    # x_type
+    assert f(FAKE, 0, 256, FAKE, 1, 256, 1, sizes, ptrs, lds, 3, None, 0, None) == 2    # out_type
+    odd = (ctypes.c_void_p * 1)(FAKE + 2)
+    assert f(FAKE, 0, 256, FAKE, 1, 256, 1, sizes, odd, lds, 0, None, 0, None) == 3     # fp32 needs 4 B
+    assert f(FAKE, 1, 256, FAKE, 1, 256, 1, sizes, ptrs, lds, 3, None, 0, None) == 2
+    g = lib.tern_linear_swiglu
+    assert g(FAKE, 0, 256, FAKE, 1, 64, 256, FAKE, 63, 1, None, 0, None) == 2           # ldh < I
+    assert g(FAKE, 0, 256, FAKE, 1, 64, 200, FAKE, 64, 1, None, 0, None) == 2           # K % 128
+    assert g(FAKE, 0, 256, FAKE, 1, 64, 256, None, 64, 1, None, 0, None) == 1
+    assert g(FAKE, 0, 256, FAKE, 1, 64, 256, FAKE + 1, 64, 1, None, 0, None) == 3
+    assert g(FAKE, 0, 256, FAKE, 1, 64, 256, FAKE + 2, 64, 0, None, 0, None) == 3       # fp32 H
+    assert g(None, 0, 256, None, 0, 64, 256, None, 64, 1, None, 0, None) == 0           # M == 0
+
+
+def test_glu_sizes_follow_the_layout():
+    for I, K in [(1, 128), (16, 256), (20, 256), (27648, 5120), (3072, 1024)]:
+        rows = oracle.glu_rows(I)
+        assert binding.tern_tiled_glu_bytes(I, K) == oracle.tiled_bytes(rows, K)
+        assert binding.tern_swiglu_workspace_bytes(4, I, K) == binding.tern_workspace_bytes(4, rows, K)
+    need = binding.tern_tiled_glu_bytes(20, 256)
+    r = binding.library().tern_repack_glu
+    assert r(FAKE, FAKE, FAKE, FAKE, 20, 200, FAKE, need, None, None) == 2
+    assert r(FAKE, FAKE, None, FAKE, 20, 256, FAKE, need, None, None) == 1
+    assert r(FAKE, FAKE, FAKE + 2, FAKE, 20, 256, FAKE, need, None, None) == 3
+    assert r(FAKE, FAKE, FAKE, FAKE, 20, 256, FAKE, need - 1, None, None) == 4
+
+
+def test_workspace_maintenance_argument_errors():
+    lib = binding.library()
+    out = ctypes.c_int32(0)
+    assert lib.tern_workspace_error(None, ctypes.addressof(out), None) == 1
+    assert lib.tern_workspace_error(FAKE, None, None) == 1
+    assert lib.tern_workspace_error(FAKE + 16, ctypes.addressof(out), None) == 3
+    assert lib.tern_workspace_reset(None, 256, None) == 1
+    assert lib.tern_workspace_reset(FAKE + 16, 256, None) == 3
+    assert lib.tern_workspace_reset(FAKE, 0, None) == 0

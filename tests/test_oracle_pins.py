@@ -357,3 +357,87 @@ def test_prefix_and_row_range_consistency():
     t, s = synth.weights(wl, 0, lin)
     t2, s2 = synth.weights(wl, 0, lin, rows=slice(500, 530))
     assert np.array_equal(t[500:530], t2) and np.array_equal(s[500:530], s2)
+
+
+# ------------------------------------------------------ fp16 activations
+
+def test_linear_fp16_activations_match_dense_matmul():
+    # x given as IEEE half bits ("Ternary embedding model in vLLM" §4.2: the
+    # page's kernel reads half activations); brute force against numpy's half
+    rng = np.random.default_rng(11)
+    M, N, K = 3, 5, 256
+    t = rng.integers(-1, 2, (N, K)).astype(np.int8)
+    packed, _ = oracle.pack(t)
+    s = rng.uniform(0.01, 0.04, (N, K // 128)).astype(np.float16)
+    x = rng.standard_normal((M, K)).astype(np.float16)
+    y, b = oracle.linear(x.view(np.uint16), packed, s.view(np.uint16), K, x_f16=True)
+    w = t.astype(np.float64) * np.repeat(s.astype(np.float64), 128, axis=1)
+    ref = x.astype(np.float64) @ w.T
+    assert np.allclose(y, ref, rtol=0, atol=1e-12)
+    assert np.allclose(b, np.abs(x.astype(np.float64)) @ np.abs(w).T, rtol=1e-12)
+    # the same bits read as bf16 give a different answer: the flag is used
+    y2, _ = oracle.linear(x.view(np.uint16), packed, s.view(np.uint16), K, x_f16=False)
+    assert not np.allclose(y, y2)
+
+
+# ------------------------------------------------------------------ SwiGLU
+
+def test_swiglu_closed_forms():
+    g = np.array([0.0, 1.0, -1.0, 2.5, -30.0, 30.0])
+    u = np.array([3.0, 1.0, 2.0, -0.5, 1.0, 1.0])
+    h = oracle.swiglu(g, u)
+    sig = [1 / (1 + math.exp(-v)) for v in g]
+    want = [gv * sv * uv for gv, sv, uv in zip(g, sig, u)]
+    assert np.allclose(h, want, rtol=1e-15, atol=0)
+    assert h[0] == 0.0                                  # silu(0) = 0
+    assert abs(h[4]) < 1e-11 and abs(h[5] - 30.0) < 1e-11   # tails: 0 and identity
+    # gate and up are not interchangeable
+    assert not np.allclose(oracle.swiglu(u, g), h)
+
+
+def test_glu_layout_rows_from_its_definition():
+    # blocks of 16 rows alternate between gate and up; I = 20 -> 64 rows
+    assert oracle.glu_rows(20) == 64 and oracle.glu_rows(16) == 32 and oracle.glu_rows(1) == 32
+    want = {0: ("gate", 0), 15: ("gate", 15), 16: ("up", 0), 31: ("up", 15),
+            32: ("gate", 16), 47: ("gate", 31), 48: ("up", 16), 63: ("up", 31)}
+    for n, src in want.items():
+        assert oracle.glu_source(n) == src
+
+
+def test_repack_glu_rows_unrepack_to_their_sources():
+    rng = np.random.default_rng(5)
+    I, K = 20, 256
+    tg = rng.integers(-1, 2, (I, K)).astype(np.int8)
+    tu = rng.integers(-1, 2, (I, K)).astype(np.int8)
+    pg, _ = oracle.pack(tg)
+    pu, _ = oracle.pack(tu)
+    sg = rng.integers(0x2000, 0x2C00, (I, K // 128)).astype(np.uint16)
+    su = rng.integers(0x2000, 0x2C00, (I, K // 128)).astype(np.uint16)
+    tiled, bad = oracle.repack_glu(pg, sg, pu, su, K)
+    assert bad == 0
+    rows = oracle.glu_rows(I)
+    packed, scales, _ = oracle.unrepack(tiled, rows, K)
+    t_all, _ = oracle.unpack(packed, K)
+    # row 16 of the GLU weight is up row 0, row 33 gate row 17, rows of i >= 20 zero
+    assert np.array_equal(t_all[16], tu[0]) and np.array_equal(scales[16], su[0])
+    assert np.array_equal(t_all[33], tg[17]) and np.array_equal(scales[33], sg[17])
+    assert np.array_equal(t_all[0], tg[0]) and np.array_equal(t_all[50], tu[18])
+    assert not t_all[36].any() and not scales[36].any()      # gate row 20: padding
+    assert not t_all[52].any() and not t_all[63].any()       # up rows 20, 31: padding
+
+
+def test_swiglu_of_the_layer_by_hand():
+    # one-hot x at k0: gate = x * t_g * s_g, up = x * t_u * s_u
+    K = 128
+    x = np.zeros((1, K), dtype=np.float32)
+    x[0, 7] = 1.5
+    xb = (x.view(np.uint32) >> 16).astype(np.uint16)
+    tg = np.zeros((1, K), dtype=np.int8); tg[0, 7] = 1
+    tu = np.zeros((1, K), dtype=np.int8); tu[0, 7] = -1
+    s = np.array([[0x3800]], dtype=np.uint16)           # 0.5
+    g, _ = oracle.linear(xb, oracle.pack(tg)[0], s, K)
+    u, _ = oracle.linear(xb, oracle.pack(tu)[0], s, K)
+    h = oracle.swiglu(g, u)
+    gv, uv = 0.75, -0.75
+    assert g[0, 0] == gv and u[0, 0] == uv
+    assert abs(h[0, 0] - gv / (1 + math.exp(-gv)) * uv) < 1e-15
