@@ -28,6 +28,10 @@ Reported (one JSON line on rank 0):
   cpu_baseline  the fp64 CPU oracle timed on a bounded sample
 
 `--impl reference` times the CPU oracle alone (the reference arm).
+`--profile NAME` runs one linear of layer 0 (qkv, o, gate_up, down,
+gate_up_swiglu) or the repack of it (repack) `--reps` times at batch `--M`
+and exits: the program the committed ncu summaries under profiles/ were
+captured from.
 """
 from __future__ import annotations
 
@@ -146,7 +150,11 @@ def build_stack(wl, layers, dev, tb, torch):
             tb.tern_pack(t_d, lin.N, lin.K, packed)
             del t_d
             disk[(layer, lin.name)] = (packed, torch.from_numpy(s.view(np.int16)).to(dev))
-    # repack every layer (disk -> tiled), timed with events
+    # repack every layer (disk -> tiled) into buffers allocated beforehand,
+    # timed with events around the repack launches alone
+    for layer in range(layers):
+        for lin in wl.linears:
+            tiled[(layer, lin.name)] = torch.empty(tb.tern_tiled_bytes(lin.N, lin.K), dtype=torch.uint8, device=dev)
     s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     repack_bytes = 0
     torch.cuda.synchronize()
@@ -154,9 +162,8 @@ def build_stack(wl, layers, dev, tb, torch):
     for layer in range(layers):
         for lin in wl.linears:
             packed, sc = disk[(layer, lin.name)]
-            out = torch.empty(tb.tern_tiled_bytes(lin.N, lin.K), dtype=torch.uint8, device=dev)
+            out = tiled[(layer, lin.name)]
             tb.tern_repack(packed, sc, lin.N, lin.K, out)
-            tiled[(layer, lin.name)] = out
             # read disk codes + scales, write tiled codes + scales
             repack_bytes += packed.numel() + 2 * sc.numel() + out.numel()
     s1.record()
@@ -165,12 +172,16 @@ def build_stack(wl, layers, dev, tb, torch):
 
 
 class Step:
-    """All linears of the stack at batch M, with X/Y arenas on the device."""
+    """All linears of the stack at batch M, with X/Y arenas on the device.
+    out_type: the outputs' element type (fp32 by default; bf16 through
+    tern_linear_ex)."""
 
-    def __init__(self, wl, layers, M, tiled, dev, tb, torch, host_copies=True):
+    def __init__(self, wl, layers, M, tiled, dev, tb, torch, host_copies=True, out_type=0):
         import synth
         self.tb, self.torch = tb, torch
         self.M = M
+        self.out_type = out_type
+        out_size = 4 if out_type == 0 else 2
         self.calls = []
         xs, x_off, y_off = [], 0, 0
         plan = []
@@ -184,27 +195,34 @@ class Step:
         x_host = torch.from_numpy(np.concatenate(xs).view(np.int16))
         self.x_host = x_host.pin_memory() if host_copies else None
         self.x_dev = x_host.to(dev)
-        self.y_dev = torch.zeros(y_off, dtype=torch.float32, device=dev)
+        self.y_dev = torch.zeros(y_off, dtype=torch.float32 if out_type == 0 else torch.bfloat16, device=dev)
         self.y_host = torch.empty(y_off, dtype=torch.float32).pin_memory() if host_copies else None
         ws_need = 0
         self.bytes = 0
         self.flops = 0
         for layer, lin, xo, yo in plan:
             ws_need = max(ws_need, tb.tern_workspace_bytes(M, lin.N, lin.K))
-            self.bytes += linear_bytes(M, lin.N, lin.K)
+            self.bytes += linear_bytes(M, lin.N, lin.K) - (4 - out_size) * M * lin.N
             self.flops += 2 * M * lin.N * lin.K
         self.ws = torch.zeros(max(ws_need, 256), dtype=torch.uint8, device=dev)
         self.ws_bytes = ws_need
         for layer, lin, xo, yo in plan:
             X = self.x_dev.data_ptr() + 2 * xo
-            Yp = self.y_dev.data_ptr() + 4 * yo
+            Yp = self.y_dev.data_ptr() + out_size * yo
             self.calls.append((lin, X, tiled[(layer, lin.name)], Yp))
         self.launches_per_call = 1
 
     def run_call(self, call, stream=None):
         tb, M = self.tb, self.M
         lin, X, tl, Yp = call
-        if len(lin.splits) == 1:
+        if self.out_type != 0:
+            ys, off = [], 0
+            for n in lin.splits:
+                ys.append(Yp + 2 * M * off)
+                off += n
+            tb.tern_linear_ex(X, tb.TERN_X_BF16, lin.K, tl, M, lin.K, list(lin.splits), ys, list(lin.splits),
+                              self.out_type, self.ws, self.ws_bytes, stream)
+        elif len(lin.splits) == 1:
             tb.tern_linear(X, lin.K, tl, M, lin.N, lin.K, Yp, lin.N, self.ws, self.ws_bytes, stream)
         else:
             ys, off = [], 0
@@ -443,11 +461,11 @@ def leg_per_linear(wl, layers, tiled, dev, tb, torch, Ms, local):
     return out
 
 
-def leg_prefill(wl, tiled, dev, tb, torch, Ms, local):
+def leg_prefill(wl, tiled, dev, tb, torch, Ms, local, out_type=0):
     """One layer's four linears at prefill batch sizes: TFLOP/s."""
     out = {}
     for M in Ms:
-        st = Step(wl, 1, M, tiled, dev, tb, torch, host_copies=False)
+        st = Step(wl, 1, M, tiled, dev, tb, torch, host_copies=False, out_type=out_type)
         st.run()
         ms, clocks = timed_region(torch, st.run, 2, local, min_ms=200.0)
         out[str(M)] = {"ms": ms, "tflops": st.flops / (ms / 1e3) / 1e12, "clocks": clocks}
@@ -477,6 +495,102 @@ def leg_workload(name, Ms, dev, tb, torch, local, reps=20):
     return out
 
 
+def glu_weights(wl, layers, dev, tb, torch):
+    """The gate+up linear of each layer in the GLU tile layout (tern_repack_glu
+    from the fused on-disk tensor, gate rows then up rows)."""
+    import synth
+    lin = next(l for l in wl.linears if l.name == "gate_up")
+    I, K = lin.splits[0], lin.K
+    out = []
+    for layer in range(layers):
+        t, s = synth.weights(wl, layer, lin)
+        t_d = torch.from_numpy(t).to(dev)
+        packed = torch.empty((lin.N, K // 4), dtype=torch.uint8, device=dev)
+        tb.tern_pack(t_d, lin.N, K, packed)
+        del t_d
+        sc = torch.from_numpy(s.view(np.int16)).to(dev)
+        tiled = torch.empty(tb.tern_tiled_glu_bytes(I, K), dtype=torch.uint8, device=dev)
+        tb.tern_repack_glu(packed, sc, packed.data_ptr() + I * (K // 4), sc.data_ptr() + I * (K // 128) * 2,
+                           I, K, tiled)
+        out.append(tiled)
+    return lin, out
+
+
+def leg_swiglu(wl, layers, dev, tb, torch, Ms, local):
+    """Fused gate+up + SwiGLU (tern_linear_swiglu, bf16 h), one launch per
+    layer back to back: GB/s of weights (+ X, h) and TFLOP/s per launch."""
+    import synth
+    lin, glu = glu_weights(wl, layers, dev, tb, torch)
+    I, K = lin.splits[0], lin.K
+    out = {}
+    for M in Ms:
+        xs = [torch.from_numpy(synth.activations(wl, l, lin, M).view(np.int16)).to(dev) for l in range(layers)]
+        H = torch.empty((M, I), dtype=torch.bfloat16, device=dev)
+        ws = torch.zeros(max(tb.tern_swiglu_workspace_bytes(M, I, K), 256), dtype=torch.uint8, device=dev)
+
+        def one_pass():
+            for l in range(layers):
+                tb.tern_linear_swiglu(xs[l], tb.TERN_X_BF16, K, glu[l], M, I, K, H, I, tb.TERN_OUT_BF16, ws)
+        one_pass()
+        ms, clocks = timed_region(torch, one_pass, 1, local, min_ms=100.0)
+        us = ms * 1e3 / layers
+        nbytes = lin.N * K // 4 + 2 * lin.N * (K // 128) + 2 * M * K + 2 * M * I
+        out[str(M)] = {"us": us, "gbs": nbytes / (us * 1e-6) / 1e9,
+                       "tflops": 2 * M * lin.N * K / (us * 1e-6) / 1e12, "clocks": clocks}
+        del xs, H, ws
+    del glu
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_profile(args):
+    """A few calls of one layer-0 linear (or its repack) for an ncu capture."""
+    import torch
+    import synth
+    from ternary_bit_weight_gb300 import binding as tb
+    dev = torch.device("cuda", 0)
+    wl = synth.WORKLOADS[args.workload]
+    name = args.profile
+    if name == "gate_up_swiglu":
+        lin, glu = glu_weights(wl, 1, dev, tb, torch)
+        I, K = lin.splits[0], lin.K
+        X = torch.from_numpy(synth.activations(wl, 0, lin, args.M).view(np.int16)).to(dev)
+        H = torch.empty((args.M, I), dtype=torch.bfloat16, device=dev)
+        ws = torch.zeros(max(tb.tern_swiglu_workspace_bytes(args.M, I, K), 256), dtype=torch.uint8, device=dev)
+        for _ in range(args.reps):
+            tb.tern_linear_swiglu(X, tb.TERN_X_BF16, K, glu[0], args.M, I, K, H, I, tb.TERN_OUT_BF16, ws)
+        torch.cuda.synchronize()
+        print("ok", name, args.M)
+        return
+    lname = "gate_up" if name == "repack" else name
+    lin = next(l for l in wl.linears if l.name == lname)
+    t, s = synth.weights(wl, 0, lin)
+    t_d = torch.from_numpy(t).to(dev)
+    packed = torch.empty((lin.N, lin.K // 4), dtype=torch.uint8, device=dev)
+    tb.tern_pack(t_d, lin.N, lin.K, packed)
+    del t_d
+    sc = torch.from_numpy(s.view(np.int16)).to(dev)
+    tiled = torch.empty(tb.tern_tiled_bytes(lin.N, lin.K), dtype=torch.uint8, device=dev)
+    if name == "repack":
+        for _ in range(args.reps):
+            tb.tern_repack(packed, sc, lin.N, lin.K, tiled)
+        torch.cuda.synchronize()
+        print("ok repack", lin.N, lin.K)
+        return
+    tb.tern_repack(packed, sc, lin.N, lin.K, tiled)
+    X = torch.from_numpy(synth.activations(wl, 0, lin, args.M).view(np.int16)).to(dev)
+    Y = torch.empty((args.M, lin.N), dtype=torch.float32, device=dev)
+    ws = torch.zeros(max(tb.tern_workspace_bytes(args.M, lin.N, lin.K), 256), dtype=torch.uint8, device=dev)
+    ys, off = [], 0
+    for n in lin.splits:
+        ys.append(Y.data_ptr() + 4 * args.M * off)
+        off += n
+    for _ in range(args.reps):
+        tb.tern_linear_multi(X, lin.K, tiled, args.M, lin.K, list(lin.splits), ys, list(lin.splits), ws)
+    torch.cuda.synchronize()
+    print("ok", name, args.M)
+
+
 # ------------------------------------------------------------------ main
 
 def main():
@@ -491,11 +605,17 @@ def main():
     ap.add_argument("--no-legs", action="store_true", help="only the headline step")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--profile", default=None,
+                    help="run one layer-0 linear (or 'repack', 'gate_up_swiglu') --reps times and exit")
+    ap.add_argument("--reps", type=int, default=6)
     args = ap.parse_args()
 
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank)
+        return
+    if args.profile:
+        run_profile(args)
         return
 
     import torch
@@ -583,6 +703,10 @@ def main():
         legs["prefill27b"] = leg_prefill(wl, tiled, dev, tb, torch, [1024, 2048, 4096], local)
         for v in legs["prefill27b"].values():
             v["frac_of_bf16_peak"] = v["tflops"] / bf16_peak
+        legs["prefill27b_bf16_out"] = leg_prefill(wl, tiled, dev, tb, torch, [4096], local, out_type=1)
+        for v in legs["prefill27b_bf16_out"].values():
+            v["frac_of_bf16_peak"] = v["tflops"] / bf16_peak
+        legs["swiglu27b"] = leg_swiglu(wl, min(layers, 8), dev, tb, torch, [1, 64, 1024], local)
         del tiled
         torch.cuda.empty_cache()
         legs["embed06b"] = leg_workload("embed06b", [1, 32, 512], dev, tb, torch, local)
