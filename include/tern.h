@@ -263,6 +263,39 @@ tern_status tern_linear_swiglu(const void* d_X, int x_type, int64_t ldx, const v
                                int out_type, void* d_ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * int8-activation variant ([EMB] §4.1-§4.3: the page's third route, signs
+ * accumulated as integers inside each 128-wide group and the float scale
+ * applied once at the group boundary).  The page does not define how the
+ * activations become integers; this library quantises per token:
+ *   a[m]    = max_k |x[m,k]| / 127                         (fp32)
+ *   q[m,k]  = rint(x[m,k] * (127 / max_k |x[m,k]|))        (fp32, ties to
+ *             even), within [-127, 127]; a zero row gives a = 0, q = 0
+ *   Y[m,n]  = a[m] * sum_g s[n,g] * I[m,n,g],  I = sum_{k in g} t[n,k] q[m,k]
+ * I is an exact int32.  The result satisfies
+ * |Y - Y_exact| <= 1e-4 * sum_k |a[m] q[m,k] W[n,k]| per output.
+ * ---------------------------------------------------------------------- */
+
+/* Bytes of the quantised activations of M x K (tern_quantize_x output). */
+size_t tern_xq_bytes(int64_t M, int64_t K);
+
+/* X (bf16 or fp16 bits, [M, ldx], 2-byte aligned) -> d_xq (device,
+ * tern_xq_bytes(M, K) bytes, 16-byte aligned: q in this library's order,
+ * within each row and each run of 16 weights k0..k0+15 first the even
+ * then the odd k) and d_a (device fp32 [M]).  K a positive multiple of 128. */
+tern_status tern_quantize_x(const void* d_X, int x_type, int64_t ldx, int64_t M, int64_t K,
+                            void* d_xq, float* d_a, void* stream);
+
+/* Workspace bytes of tern_linear_i8 (256-byte aligned, zero-filled before
+ * first use; its first word is the error word as for tern_linear). */
+size_t tern_i8_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/* Y = the int8-activation layer above, from tern_quantize_x's (d_xq, d_a)
+ * and the tiled weights; d_Y [M, ldy] of out_type.  Deterministic. */
+tern_status tern_linear_i8(const void* d_xq, const float* d_a, const void* d_tiled, int64_t M,
+                           int64_t N, int64_t K, void* d_Y, int64_t ldy, int out_type,
+                           void* d_ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * Workspace maintenance (library conveniences; the pages have none).
  * ---------------------------------------------------------------------- */
 

@@ -72,6 +72,10 @@ def _load():
             lib.orc_linear_x.restype = None
             lib.orc_linear_cols_x.argtypes = [vp, ctypes.c_int, i64, vp, vp, i64, i64, i64, vp, i64, vp, vp]
             lib.orc_linear_cols_x.restype = None
+            lib.orc_quantize_x.argtypes = [vp, ctypes.c_int, i64, i64, i64, vp, vp]
+            lib.orc_quantize_x.restype = None
+            lib.orc_linear_i8.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp]
+            lib.orc_linear_i8.restype = None
             lib.orc_swiglu.argtypes = [vp, vp, i64, vp]
             lib.orc_swiglu.restype = None
             lib.orc_num_threads.argtypes = []
@@ -165,6 +169,30 @@ def linear_cols(x_bits: np.ndarray, packed: np.ndarray, scales: np.ndarray, K: i
     b = np.empty((M, cols.size), dtype=np.float64)
     _load().orc_linear_cols_x(x.ctypes.data, int(x_f16), K, packed.ctypes.data, scales.ctypes.data,
                               M, N, K, cols.ctypes.data, cols.size, y.ctypes.data, b.ctypes.data)
+    return y, b
+
+
+def quantize_x(x_bits: np.ndarray, x_f16: bool = False):
+    """Per-token absmax int8: (q int8 [M, K] in k order, a fp32 [M])."""
+    x = _c(x_bits, np.uint16)
+    M, K = x.shape
+    q = np.empty((M, K), dtype=np.int8)
+    a = np.empty(M, dtype=np.float32)
+    _load().orc_quantize_x(x.ctypes.data, int(x_f16), K, M, K, q.ctypes.data, a.ctypes.data)
+    return q, a
+
+
+def linear_i8(q: np.ndarray, a: np.ndarray, packed: np.ndarray, scales: np.ndarray, K: int):
+    """Y = a * sum_g s * (exact integer group sums of t q), and its bound."""
+    q = _c(q, np.int8)
+    a = _c(a, np.float32)
+    packed = _c(packed, np.uint8)
+    scales = _c(scales, np.uint16)
+    M, N = q.shape[0], packed.shape[0]
+    y = np.empty((M, N), dtype=np.float64)
+    b = np.empty((M, N), dtype=np.float64)
+    _load().orc_linear_i8(q.ctypes.data, a.ctypes.data, packed.ctypes.data, scales.ctypes.data, M, N, K,
+                          y.ctypes.data, b.ctypes.data)
     return y, b
 
 

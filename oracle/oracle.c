@@ -31,6 +31,7 @@
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 /* ------------------------------------------------------------------ scalars */
@@ -280,6 +281,61 @@ void orc_linear_cols(const uint16_t* X, int64_t ldx, const uint8_t* packed,
                      const uint16_t* scales, int64_t M, int64_t N, int64_t K,
                      const int64_t* cols, int64_t ncols, double* Y, double* bound) {
     orc_linear_cols_x(X, 0, ldx, packed, scales, M, N, K, cols, ncols, Y, bound);
+}
+
+/* --------------------------------------------------- int8 activations */
+
+/* Per-token absmax quantisation (the reading taken for the page's third
+   route, "Ternary embedding model in vLLM" §4.1-§4.3, which leaves the
+   quantiser open): in fp32, as the kernel does it, so that both sides take
+   every rounding decision in the same precision:
+     mx = max_k |x|, a = mx / 127, q = rint(x * (127 / mx)) in [-127, 127];
+   rint rounds ties to even (the default rounding mode).  q in natural
+   k order, [M, K]. */
+void orc_quantize_x(const uint16_t* X, int x_f16, int64_t ldx, int64_t M, int64_t K,
+                    int8_t* q, float* a) {
+    for (int64_t m = 0; m < M; ++m) {
+        const uint16_t* xr = X + m * ldx;
+        float mx = 0.0f;
+        for (int64_t k = 0; k < K; ++k) {
+            float v = (float)(x_f16 ? orc_fp16_to_double(xr[k]) : orc_bf16_to_double(xr[k]));
+            if (fabsf(v) > mx) mx = fabsf(v);
+        }
+        float inv = mx > 0.0f ? 127.0f / mx : 0.0f;
+        a[m] = mx / 127.0f;
+        for (int64_t k = 0; k < K; ++k) {
+            float v = (float)(x_f16 ? orc_fp16_to_double(xr[k]) : orc_bf16_to_double(xr[k]));
+            float r = rintf(v * inv);
+            if (r > 127.0f) r = 127.0f;
+            if (r < -127.0f) r = -127.0f;
+            q[m * K + k] = (int8_t)r;
+        }
+    }
+}
+
+/* Y[m,n] = a[m] * sum_g s[n,g] * sum_{k in g} t[n,k] q[m,k] in fp64 (the
+   integer group sums are exact), and the bound sum_k |a q t s|. */
+void orc_linear_i8(const int8_t* q, const float* a, const uint8_t* packed, const uint16_t* scales,
+                   int64_t M, int64_t N, int64_t K, double* Y, double* bound) {
+    int64_t G = K / 128;
+    #pragma omp parallel for schedule(dynamic, 16) collapse(2)
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0, mag = 0.0;
+            for (int64_t g = 0; g < G; ++g) {
+                long isum = 0, iabs = 0;
+                for (int64_t k = 128 * g; k < 128 * g + 128; ++k) {
+                    int t = orc_code_to_ternary(packed_code(packed, K, n, k));
+                    isum += (long)t * q[m * K + k];
+                    iabs += labs((long)t * q[m * K + k]);
+                }
+                double s = orc_fp16_to_double(scales[n * G + g]);
+                acc += s * (double)isum;
+                mag += fabs(s) * (double)iabs;
+            }
+            Y[m * N + n] = (double)a[m] * acc;
+            bound[m * N + n] = (double)a[m] * mag;
+        }
 }
 
 /* ------------------------------------------------------------------ SwiGLU */

@@ -25,7 +25,8 @@ EXPORTED = ("tern_status_string", "tern_version", "tern_pack", "tern_unpack", "t
             "tern_repack", "tern_unrepack", "tern_workspace_bytes", "tern_linear",
             "tern_linear_multi", "tern_linear_noalloc", "tern_linear_ex", "tern_tiled_glu_bytes",
             "tern_repack_glu", "tern_swiglu_workspace_bytes", "tern_linear_swiglu",
-            "tern_workspace_error", "tern_workspace_reset")
+            "tern_workspace_error", "tern_workspace_reset", "tern_xq_bytes", "tern_quantize_x",
+            "tern_i8_workspace_bytes", "tern_linear_i8")
 
 
 class TernError(RuntimeError):
@@ -78,6 +79,14 @@ def _load():
     lib.tern_workspace_error.restype = i32
     lib.tern_workspace_reset.argtypes = [vp, sz, vp]
     lib.tern_workspace_reset.restype = i32
+    lib.tern_xq_bytes.argtypes = [i64, i64]
+    lib.tern_xq_bytes.restype = sz
+    lib.tern_quantize_x.argtypes = [vp, i32, i64, i64, i64, vp, vp, vp]
+    lib.tern_quantize_x.restype = i32
+    lib.tern_i8_workspace_bytes.argtypes = [i64, i64, i64]
+    lib.tern_i8_workspace_bytes.restype = sz
+    lib.tern_linear_i8.argtypes = [vp, vp, vp, i64, i64, i64, vp, i64, i32, vp, sz, vp]
+    lib.tern_linear_i8.restype = i32
     return lib
 
 
@@ -235,3 +244,23 @@ def tern_workspace_reset(ws, ws_bytes: int | None = None, stream=None):
     if ws_bytes is None:
         ws_bytes = _nbytes(ws)
     _check(_lib.tern_workspace_reset(_p(ws), ws_bytes, _s(stream)), "tern_workspace_reset")
+
+
+def tern_xq_bytes(M: int, K: int) -> int:
+    return int(_lib.tern_xq_bytes(M, K))
+
+
+def tern_quantize_x(X, x_type: int, ldx: int, M: int, K: int, xq, a, stream=None):
+    _check(_lib.tern_quantize_x(_p(X), x_type, ldx, M, K, _p(xq), _p(a), _s(stream)), "tern_quantize_x")
+
+
+def tern_i8_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(_lib.tern_i8_workspace_bytes(M, N, K))
+
+
+def tern_linear_i8(xq, a, tiled, M: int, N: int, K: int, Y, ldy: int, out_type: int = 0, ws=None,
+                   ws_bytes: int | None = None, stream=None):
+    if ws_bytes is None:
+        ws_bytes = _nbytes(ws)
+    _check(_lib.tern_linear_i8(_p(xq), _p(a), _p(tiled), M, N, K, _p(Y), ldy, out_type, _p(ws), ws_bytes,
+                               _s(stream)), "tern_linear_i8")

@@ -249,6 +249,55 @@ tern_status tern_linear_swiglu(const void* d_X, int x_type, int64_t ldx, const v
     return run_linear(X, x_type == TERN_X_F16, ldx, d_tiled_glu, M, N, K, out, d_ws, ws_bytes, as_stream(stream));
 }
 
+size_t tern_xq_bytes(int64_t M, int64_t K) {
+    if (M < 0 || K <= 0 || K % tern::kGroup != 0) return 0;
+    return tern::i8_xq_bytes(M, K);
+}
+
+tern_status tern_quantize_x(const void* d_X, int x_type, int64_t ldx, int64_t M, int64_t K, void* d_xq,
+                            float* d_a, void* stream) {
+    if (x_type != TERN_X_BF16 && x_type != TERN_X_F16) return TERN_ERR_SHAPE;
+    if (M < 0 || K <= 0 || K % tern::kGroup != 0 || ldx < K) return TERN_ERR_SHAPE;
+    if (M == 0) return TERN_OK;
+    if (d_X == nullptr || d_xq == nullptr || d_a == nullptr) return TERN_ERR_NULL;
+    if (!aligned(d_X, 2) || !aligned(d_xq, 16) || !aligned(d_a, 4)) return TERN_ERR_ALIGN;
+    return from_cuda(tern::launch_quantize_x(static_cast<const uint16_t*>(d_X), x_type == TERN_X_F16, ldx, M, K,
+                                             static_cast<int8_t*>(d_xq), d_a, as_stream(stream)));
+}
+
+size_t tern_i8_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+    if (M <= 0 || !valid_group_shape(N, K) || N == 0) return 0;
+    return tern::plan_i8(M, N, K, tern::device_sm_count()).ws_bytes;
+}
+
+tern_status tern_linear_i8(const void* d_xq, const float* d_a, const void* d_tiled, int64_t M, int64_t N,
+                           int64_t K, void* d_Y, int64_t ldy, int out_type, void* d_ws, size_t ws_bytes,
+                           void* stream) {
+    if (out_type != TERN_OUT_F32 && out_type != TERN_OUT_BF16 && out_type != TERN_OUT_F16) return TERN_ERR_SHAPE;
+    if (M < 0 || !valid_group_shape(N, K)) return TERN_ERR_SHAPE;
+    if (M == 0 || N == 0) return TERN_OK;
+    if (M > (int64_t(1) << 30)) return TERN_ERR_SHAPE;
+    if (d_xq == nullptr || d_a == nullptr || d_tiled == nullptr || d_Y == nullptr || d_ws == nullptr)
+        return TERN_ERR_NULL;
+    if (ldy < N) return TERN_ERR_SHAPE;
+    if (!aligned(d_xq, 16) || !aligned(d_a, 4) || !aligned(d_tiled, 16) || !aligned(d_ws, 256) ||
+        !aligned(d_Y, out_type == TERN_OUT_F32 ? 4 : 2))
+        return TERN_ERR_ALIGN;
+    const int sms = tern::device_sm_count();
+    if (sms <= 0) return TERN_ERR_UNSUPPORTED;
+    const tern::I8Plan plan = tern::plan_i8(M, N, K, sms);
+    if (ws_bytes < plan.ws_bytes) return TERN_ERR_SIZE;
+    tern::OutputSplit out = {};
+    out.n_out = 1;
+    out.bf16 = out_type == TERN_OUT_BF16 ? 1 : out_type == TERN_OUT_F16 ? 2 : 0;
+    out.offset[0] = 0;
+    for (int j = 1; j <= tern::kMaxOutputs; ++j) out.offset[j] = N;
+    out.y[0] = d_Y;
+    out.ldy[0] = ldy;
+    return from_cuda(tern::launch_i8(static_cast<const int8_t*>(d_xq), d_a, static_cast<const uint8_t*>(d_tiled),
+                                     M, N, K, out, d_ws, plan, as_stream(stream)));
+}
+
 tern_status tern_workspace_error(const void* d_ws, int32_t* h_err, void* stream) {
     if (d_ws == nullptr || h_err == nullptr) return TERN_ERR_NULL;
     if (!aligned(d_ws, 256)) return TERN_ERR_ALIGN;

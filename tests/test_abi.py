@@ -22,7 +22,7 @@ HEADER = os.path.join(ROOT, "include", "tern.h")
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(tern_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(tern_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declarations_match_binding():
@@ -185,3 +185,21 @@ def test_workspace_maintenance_argument_errors():
     assert lib.tern_workspace_reset(None, 256, None) == 1
     assert lib.tern_workspace_reset(FAKE + 16, 256, None) == 3
     assert lib.tern_workspace_reset(FAKE, 0, None) == 0
+
+
+def test_i8_argument_errors():
+    lib = binding.library()
+    assert binding.tern_xq_bytes(3, 256) == 768 and binding.tern_xq_bytes(3, 100) == 0
+    q = lib.tern_quantize_x
+    assert q(FAKE, 2, 256, 1, 256, FAKE, FAKE, None) == 2          # x_type
+    assert q(FAKE, 0, 128, 1, 256, FAKE, FAKE, None) == 2          # ldx < K
+    assert q(FAKE, 0, 256, 1, 256, None, FAKE, None) == 1
+    assert q(FAKE, 0, 256, 1, 256, FAKE + 8, FAKE, None) == 3      # xq 16 B
+    assert q(None, 0, 256, 0, 256, None, None, None) == 0          # M == 0
+    f = lib.tern_linear_i8
+    assert f(FAKE, FAKE, FAKE, 1, 64, 200, FAKE, 64, 0, FAKE, 1 << 20, None) == 2
+    assert f(FAKE, FAKE, FAKE, 1, 64, 256, FAKE, 64, 7, FAKE, 1 << 20, None) == 2
+    assert f(FAKE, None, FAKE, 1, 64, 256, FAKE, 64, 0, FAKE, 1 << 20, None) == 1
+    assert f(FAKE, FAKE, FAKE, 1, 64, 256, FAKE + 2, 64, 0, FAKE, 1 << 20, None) == 3
+    assert f(FAKE, FAKE, FAKE, 1, 64, 256, FAKE, 63, 0, FAKE, 1 << 20, None) == 2
+    assert binding.tern_i8_workspace_bytes(1, 64, 256) >= 256

@@ -441,3 +441,48 @@ def test_swiglu_of_the_layer_by_hand():
     gv, uv = 0.75, -0.75
     assert g[0, 0] == gv and u[0, 0] == uv
     assert abs(h[0, 0] - gv / (1 + math.exp(-gv)) * uv) < 1e-15
+
+
+# ------------------------------------------------------- int8 activations
+
+def _bf16(vals):
+    x = np.array(vals, dtype=np.float32).reshape(1, -1)
+    return (x.view(np.uint32) >> 16).astype(np.uint16)
+
+
+def test_quantize_x_hand_worked():
+    # absmax 2 -> 127/2 = 63.5 per unit; 1.0 -> 63.5 -> 64 (tie to even),
+    # -2 -> -127, 0.5 -> 31.75 -> 32, 0.25 -> 15.875 -> 16; a = 2/127
+    q, a = oracle.quantize_x(_bf16([1.0, -2.0, 0.5, 0.25] + [0.0] * 124))
+    assert q[0, :4].tolist() == [64, -127, 32, 16] and not q[0, 4:].any()
+    assert a[0] == np.float32(2.0) / np.float32(127.0)
+    # absmax 127: the scale is exactly 1 and ties go to even
+    q, a = oracle.quantize_x(_bf16([127.0, 0.5, 1.5, 2.5, -0.5, -1.5, 126.0, -127.0] + [0.0] * 120))
+    assert q[0, :8].tolist() == [127, 0, 2, 2, 0, -2, 126, -127] and a[0] == 1.0
+    # a row of zeros: a = 0, q = 0
+    q, a = oracle.quantize_x(np.zeros((1, 128), dtype=np.uint16))
+    assert a[0] == 0.0 and not q.any()
+    # fp16 bits are read as fp16
+    xh = np.array([[3.0, -1.5] + [0.0] * 126], dtype=np.float16)
+    q, a = oracle.quantize_x(xh.view(np.uint16), x_f16=True)
+    assert q[0, :2].tolist() == [127, -64] and a[0] == np.float32(3.0) / np.float32(127.0)
+
+
+def test_linear_i8_matches_integer_matmul():
+    rng = np.random.default_rng(8)
+    M, N, K = 3, 7, 384
+    t = rng.integers(-1, 2, (N, K)).astype(np.int8)
+    q = rng.integers(-127, 128, (M, K)).astype(np.int8)
+    a = rng.uniform(0.001, 0.1, M).astype(np.float32)
+    s = rng.uniform(0.005, 0.05, (N, K // 128)).astype(np.float16)
+    packed, _ = oracle.pack(t)
+    y, b = oracle.linear_i8(q, a, packed, s.view(np.uint16), K)
+    G = K // 128
+    # integer group sums from numpy's int64 matmul, then the scales
+    isum = np.stack([q[:, 128 * g:128 * g + 128].astype(np.int64) @ t[:, 128 * g:128 * g + 128].T.astype(np.int64)
+                     for g in range(G)], axis=-1)                      # [M, N, G]
+    ref = a.astype(np.float64)[:, None] * np.einsum("mng,ng->mn", isum.astype(np.float64), s.astype(np.float64))
+    assert np.allclose(y, ref, rtol=1e-13, atol=0)
+    w = t.astype(np.float64) * np.repeat(s.astype(np.float64), 128, axis=1)
+    mag = a.astype(np.float64)[:, None] * (np.abs(q.astype(np.float64)) @ np.abs(w).T)
+    assert np.allclose(b, mag, rtol=1e-13)
