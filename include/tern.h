@@ -263,6 +263,38 @@ tern_status tern_linear_swiglu(const void* d_X, int x_type, int64_t ldx, const v
                                int out_type, void* d_ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * INT8 group scales ([EMB] §6, outlook: compress the FP16 scales to INT8).
+ * The page gives no format; this library's reading: one fp32 factor per
+ * row and one int8 per group,
+ *   s8[n, g] = q8[n, g] * f[n],   f[n] = max_g |s[n,g]| / 127,
+ *   q8[n, g] = rint(s[n,g] * (127 / max_g |s[n,g]|))  (fp32, ties to even)
+ * and the layer becomes Y = X . (s8 (.) T)^T with the same error bound.
+ *
+ * INT8-scale tile layout: the codes of the tiled layout (R*G units of 4096
+ * bytes), then per unit (b, g) the 128 int8 q8[128b + r][g] (r = 0..127),
+ * then per row tile b the 128 fp32 factors f[128b + r] (0 for padding).
+ * ---------------------------------------------------------------------- */
+
+/* Bytes of the INT8-scale layout: ceil(N/128) * (K/128) * 4224 + ceil(N/128) * 512. */
+size_t tern_tiled_s8_bytes(int64_t N, int64_t K);
+
+/* FP16 scales [N, K/128] -> d_q8 int8 [N, K/128] and d_f fp32 [N] (device).
+ * A row of zero scales gives f = 0, q8 = 0. */
+tern_status tern_quantize_scales(const uint16_t* d_scales, int64_t N, int64_t K, int8_t* d_q8,
+                                 float* d_f, void* stream);
+
+/* (packed [N, K/4], q8, f) -> INT8-scale tile layout; otherwise as tern_repack. */
+tern_status tern_repack_s8(const uint8_t* d_packed, const int8_t* d_q8, const float* d_f,
+                           int64_t N, int64_t K, void* d_tiled, size_t tiled_bytes,
+                           int32_t* d_err, void* stream);
+
+/* tern_linear_ex over INT8-scale weights (workspace: tern_workspace_bytes). */
+tern_status tern_linear_s8(const void* d_X, int x_type, int64_t ldx, const void* d_tiled_s8,
+                           int64_t M, int64_t K, int n_out, const int64_t* n_sizes,
+                           void* const* d_Ys, const int64_t* ldys, int out_type,
+                           void* d_ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * int8-activation variant ([EMB] §4.1-§4.3: the page's third route, signs
  * accumulated as integers inside each 128-wide group and the float scale
  * applied once at the group boundary).  The page does not define how the

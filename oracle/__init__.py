@@ -72,6 +72,10 @@ def _load():
             lib.orc_linear_x.restype = None
             lib.orc_linear_cols_x.argtypes = [vp, ctypes.c_int, i64, vp, vp, i64, i64, i64, vp, i64, vp, vp]
             lib.orc_linear_cols_x.restype = None
+            lib.orc_quantize_scales.argtypes = [vp, i64, i64, vp, vp]
+            lib.orc_quantize_scales.restype = None
+            lib.orc_linear_s8.argtypes = [vp, i64, vp, vp, vp, i64, i64, i64, vp, vp]
+            lib.orc_linear_s8.restype = None
             lib.orc_quantize_x.argtypes = [vp, ctypes.c_int, i64, i64, i64, vp, vp]
             lib.orc_quantize_x.restype = None
             lib.orc_linear_i8.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp]
@@ -169,6 +173,56 @@ def linear_cols(x_bits: np.ndarray, packed: np.ndarray, scales: np.ndarray, K: i
     b = np.empty((M, cols.size), dtype=np.float64)
     _load().orc_linear_cols_x(x.ctypes.data, int(x_f16), K, packed.ctypes.data, scales.ctypes.data,
                               M, N, K, cols.ctypes.data, cols.size, y.ctypes.data, b.ctypes.data)
+    return y, b
+
+
+def quantize_scales(scales: np.ndarray, K: int):
+    """FP16 scale bits [N, K/128] -> (q8 int8 [N, K/128], f fp32 [N])."""
+    scales = _c(scales, np.uint16)
+    N = scales.shape[0]
+    q8 = np.empty((N, K // 128), dtype=np.int8)
+    f = np.empty(N, dtype=np.float32)
+    _load().orc_quantize_scales(scales.ctypes.data, N, K, q8.ctypes.data, f.ctypes.data)
+    return q8, f
+
+
+def tiled_s8_bytes(N: int, K: int) -> int:
+    R, G = (N + 127) // 128, K // 128
+    return R * G * (4096 + 128) + R * 128 * 4
+
+
+def repack_s8(packed: np.ndarray, q8: np.ndarray, f: np.ndarray, K: int) -> np.ndarray:
+    """INT8-scale tile layout: the tiled layout's code units, then per unit
+    (b, g) the bytes q8[128b + r][g], then per row tile the fp32 f[128b + r]
+    (padding rows 0)."""
+    packed = _c(packed, np.uint8)
+    N = packed.shape[0]
+    R, G = (N + 127) // 128, K // 128
+    zero_scales = np.zeros((N, G), dtype=np.uint16)
+    tiled, _ = repack(packed, zero_scales, K)
+    codes = tiled[:R * G * 4096]
+    q = np.zeros((R * 128, G), dtype=np.int8)
+    q[:N] = q8
+    units = np.empty((R, G, 128), dtype=np.int8)
+    for b in range(R):
+        for g in range(G):
+            units[b, g] = q[128 * b:128 * b + 128, g]
+    fac = np.zeros(R * 128, dtype=np.float32)
+    fac[:N] = f
+    return np.concatenate([codes, units.reshape(-1).view(np.uint8), fac.view(np.uint8)])
+
+
+def linear_s8(x_bits: np.ndarray, packed: np.ndarray, q8: np.ndarray, f: np.ndarray, K: int):
+    """Y = X . (q8 * f (.) T)^T in fp64 and its bound."""
+    x = _c(x_bits, np.uint16)
+    packed = _c(packed, np.uint8)
+    q8 = _c(q8, np.int8)
+    f = _c(f, np.float32)
+    M, N = x.shape[0], packed.shape[0]
+    y = np.empty((M, N), dtype=np.float64)
+    b = np.empty((M, N), dtype=np.float64)
+    _load().orc_linear_s8(x.ctypes.data, K, packed.ctypes.data, q8.ctypes.data, f.ctypes.data, M, N, K,
+                          y.ctypes.data, b.ctypes.data)
     return y, b
 
 

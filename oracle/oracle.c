@@ -283,6 +283,52 @@ void orc_linear_cols(const uint16_t* X, int64_t ldx, const uint8_t* packed,
     orc_linear_cols_x(X, 0, ldx, packed, scales, M, N, K, cols, ncols, Y, bound);
 }
 
+/* ------------------------------------------------------ INT8 group scales */
+
+/* The reading taken for "compress the FP16 scales to INT8" ("Ternary
+   embedding model in vLLM" §6, an outlook without a format): per row one
+   fp32 factor f = max_g |s| / 127 and per group q = rint(s * (127 / max_g |s|))
+   in [-127, 127], in fp32 with ties to even. */
+void orc_quantize_scales(const uint16_t* scales, int64_t N, int64_t K, int8_t* q8, float* f) {
+    int64_t G = K / 128;
+    for (int64_t n = 0; n < N; ++n) {
+        float mx = 0.0f;
+        for (int64_t g = 0; g < G; ++g) {
+            float v = (float)orc_fp16_to_double(scales[n * G + g]);
+            if (fabsf(v) > mx) mx = fabsf(v);
+        }
+        float inv = mx > 0.0f ? 127.0f / mx : 0.0f;
+        f[n] = mx / 127.0f;
+        for (int64_t g = 0; g < G; ++g) {
+            float r = rintf((float)orc_fp16_to_double(scales[n * G + g]) * inv);
+            if (r > 127.0f) r = 127.0f;
+            if (r < -127.0f) r = -127.0f;
+            q8[n * G + g] = (int8_t)r;
+        }
+    }
+}
+
+/* Y[m,n] = sum_k x[m,k] * t[n,k] * q8[n,k/128] * f[n] in fp64 (X bf16 bits),
+   and the bound sum_k |x t q8 f|. */
+void orc_linear_s8(const uint16_t* X, int64_t ldx, const uint8_t* packed, const int8_t* q8,
+                   const float* f, int64_t M, int64_t N, int64_t K, double* Y, double* bound) {
+    int64_t G = K / 128;
+    #pragma omp parallel for schedule(dynamic, 16) collapse(2)
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0, mag = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double x = orc_bf16_to_double(X[m * ldx + k]);
+                double w = (double)orc_code_to_ternary(packed_code(packed, K, n, k))
+                         * (double)q8[n * G + k / 128] * (double)f[n];
+                acc += x * w;
+                mag += fabs(x * w);
+            }
+            Y[m * N + n] = acc;
+            bound[m * N + n] = mag;
+        }
+}
+
 /* --------------------------------------------------- int8 activations */
 
 /* Per-token absmax quantisation (the reading taken for the page's third

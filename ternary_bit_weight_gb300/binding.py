@@ -26,7 +26,8 @@ EXPORTED = ("tern_status_string", "tern_version", "tern_pack", "tern_unpack", "t
             "tern_linear_multi", "tern_linear_noalloc", "tern_linear_ex", "tern_tiled_glu_bytes",
             "tern_repack_glu", "tern_swiglu_workspace_bytes", "tern_linear_swiglu",
             "tern_workspace_error", "tern_workspace_reset", "tern_xq_bytes", "tern_quantize_x",
-            "tern_i8_workspace_bytes", "tern_linear_i8")
+            "tern_i8_workspace_bytes", "tern_linear_i8", "tern_tiled_s8_bytes", "tern_quantize_scales",
+            "tern_repack_s8", "tern_linear_s8")
 
 
 class TernError(RuntimeError):
@@ -87,6 +88,14 @@ def _load():
     lib.tern_i8_workspace_bytes.restype = sz
     lib.tern_linear_i8.argtypes = [vp, vp, vp, i64, i64, i64, vp, i64, i32, vp, sz, vp]
     lib.tern_linear_i8.restype = i32
+    lib.tern_tiled_s8_bytes.argtypes = [i64, i64]
+    lib.tern_tiled_s8_bytes.restype = sz
+    lib.tern_quantize_scales.argtypes = [vp, i64, i64, vp, vp, vp]
+    lib.tern_quantize_scales.restype = i32
+    lib.tern_repack_s8.argtypes = [vp, vp, vp, i64, i64, vp, sz, vp, vp]
+    lib.tern_repack_s8.restype = i32
+    lib.tern_linear_s8.argtypes = list(lib.tern_linear_ex.argtypes)
+    lib.tern_linear_s8.restype = i32
     return lib
 
 
@@ -264,3 +273,30 @@ def tern_linear_i8(xq, a, tiled, M: int, N: int, K: int, Y, ldy: int, out_type: 
         ws_bytes = _nbytes(ws)
     _check(_lib.tern_linear_i8(_p(xq), _p(a), _p(tiled), M, N, K, _p(Y), ldy, out_type, _p(ws), ws_bytes,
                                _s(stream)), "tern_linear_i8")
+
+
+def tern_tiled_s8_bytes(N: int, K: int) -> int:
+    return int(_lib.tern_tiled_s8_bytes(N, K))
+
+
+def tern_quantize_scales(scales, N: int, K: int, q8, f, stream=None):
+    _check(_lib.tern_quantize_scales(_p(scales), N, K, _p(q8), _p(f), _s(stream)), "tern_quantize_scales")
+
+
+def tern_repack_s8(packed, q8, f, N: int, K: int, tiled, tiled_bytes: int | None = None, err=None, stream=None):
+    if tiled_bytes is None:
+        tiled_bytes = _nbytes(tiled)
+    _check(_lib.tern_repack_s8(_p(packed), _p(q8), _p(f), N, K, _p(tiled), tiled_bytes, _p(err), _s(stream)),
+           "tern_repack_s8")
+
+
+def tern_linear_s8(X, x_type: int, ldx: int, tiled_s8, M: int, K: int, n_sizes, Ys, ldys, out_type: int,
+                   ws=None, ws_bytes: int | None = None, stream=None):
+    n_out = len(n_sizes)
+    sizes = (ctypes.c_int64 * n_out)(*[int(v) for v in n_sizes])
+    ptrs = (ctypes.c_void_p * n_out)(*[_p(y) for y in Ys])
+    lds = (ctypes.c_int64 * n_out)(*[int(v) for v in ldys])
+    if ws_bytes is None:
+        ws_bytes = _nbytes(ws)
+    _check(_lib.tern_linear_s8(_p(X), x_type, ldx, _p(tiled_s8), M, K, n_out, sizes, ptrs, lds, out_type,
+                               _p(ws), ws_bytes, _s(stream)), "tern_linear_s8")

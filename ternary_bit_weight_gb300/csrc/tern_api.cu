@@ -20,7 +20,7 @@ inline bool valid_group_shape(int64_t N, int64_t K) { return N >= 0 && K > 0 && 
 
 tern_status run_linear(const uint16_t* X, bool x_f16, int64_t ldx, const void* tiled, int64_t M, int64_t N,
                        int64_t K, const tern::OutputSplit& out, void* ws, size_t ws_bytes,
-                       cudaStream_t stream) {
+                       cudaStream_t stream, bool s8 = false) {
     const int sms = tern::device_sm_count();
     if (sms <= 0) return TERN_ERR_UNSUPPORTED;
     if (ws == nullptr) return TERN_ERR_NULL;
@@ -30,11 +30,11 @@ tern_status run_linear(const uint16_t* X, bool x_f16, int64_t ldx, const void* t
     if (M <= tern::kStreamMaxM) {
         const tern::StreamPlan plan = tern::plan_stream(M, N, K, sms);
         if (ws_bytes < plan.ws_bytes) return TERN_ERR_SIZE;
-        e = tern::launch_stream(X, x_f16, ldx, w, M, N, K, out, ws, plan, stream);
+        e = tern::launch_stream(X, x_f16, ldx, w, s8, M, N, K, out, ws, plan, stream);
     } else {
         const tern::GemmPlan plan = tern::plan_gemm(M, N, K, sms);
         if (ws_bytes < plan.ws_bytes) return TERN_ERR_SIZE;
-        e = tern::launch_gemm(X, x_f16, ldx, w, M, N, K, out, ws, plan, stream);
+        e = tern::launch_gemm(X, x_f16, ldx, w, s8, M, N, K, out, ws, plan, stream);
     }
     return e == cudaSuccess ? TERN_OK : TERN_ERR_CUDA;
 }
@@ -162,9 +162,10 @@ tern_status tern_linear_multi(const uint16_t* d_X, int64_t ldx, const void* d_ti
                           reinterpret_cast<void* const*>(d_Ys), ldys, TERN_OUT_F32, d_ws, ws_bytes, stream);
 }
 
-tern_status tern_linear_ex(const void* d_X, int x_type, int64_t ldx, const void* d_tiled, int64_t M,
-                           int64_t K, int n_out, const int64_t* n_sizes, void* const* d_Ys,
-                           const int64_t* ldys, int out_type, void* d_ws, size_t ws_bytes, void* stream) {
+static tern_status linear_ex(const void* d_X, int x_type, int64_t ldx, const void* d_tiled, int64_t M,
+                             int64_t K, int n_out, const int64_t* n_sizes, void* const* d_Ys,
+                             const int64_t* ldys, int out_type, void* d_ws, size_t ws_bytes, void* stream,
+                             bool s8) {
     if (x_type != TERN_X_BF16 && x_type != TERN_X_F16) return TERN_ERR_SHAPE;
     if (out_type != TERN_OUT_F32 && out_type != TERN_OUT_BF16 && out_type != TERN_OUT_F16) return TERN_ERR_SHAPE;
     if (n_out < 1 || n_out > tern::kMaxOutputs) return TERN_ERR_SHAPE;
@@ -193,7 +194,48 @@ tern_status tern_linear_ex(const void* d_X, int x_type, int64_t ldx, const void*
         out.y[j] = d_Ys[j];
         out.ldy[j] = ldys[j];
     }
-    return run_linear(X, x_type == TERN_X_F16, ldx, d_tiled, M, N, K, out, d_ws, ws_bytes, as_stream(stream));
+    return run_linear(X, x_type == TERN_X_F16, ldx, d_tiled, M, N, K, out, d_ws, ws_bytes, as_stream(stream), s8);
+}
+
+tern_status tern_linear_ex(const void* d_X, int x_type, int64_t ldx, const void* d_tiled, int64_t M,
+                           int64_t K, int n_out, const int64_t* n_sizes, void* const* d_Ys,
+                           const int64_t* ldys, int out_type, void* d_ws, size_t ws_bytes, void* stream) {
+    return linear_ex(d_X, x_type, ldx, d_tiled, M, K, n_out, n_sizes, d_Ys, ldys, out_type, d_ws, ws_bytes, stream,
+                     false);
+}
+
+size_t tern_tiled_s8_bytes(int64_t N, int64_t K) {
+    if (!valid_group_shape(N, K)) return 0;
+    const size_t R = (size_t)ceil_div(N, tern::kTileRows), G = (size_t)(K / tern::kGroup);
+    return R * G * (size_t)(tern::kUnitCodeBytes + tern::kUnitScaleBytesS8) + R * tern::kTileRows * sizeof(float);
+}
+
+tern_status tern_quantize_scales(const uint16_t* d_scales, int64_t N, int64_t K, int8_t* d_q8, float* d_f,
+                                 void* stream) {
+    if (!valid_group_shape(N, K)) return TERN_ERR_SHAPE;
+    if (N == 0) return TERN_OK;
+    if (d_scales == nullptr || d_q8 == nullptr || d_f == nullptr) return TERN_ERR_NULL;
+    if (!aligned(d_scales, 2) || !aligned(d_f, 4)) return TERN_ERR_ALIGN;
+    return from_cuda(tern::launch_quantize_scales(d_scales, N, K, d_q8, d_f, as_stream(stream)));
+}
+
+tern_status tern_repack_s8(const uint8_t* d_packed, const int8_t* d_q8, const float* d_f, int64_t N, int64_t K,
+                           void* d_tiled, size_t tiled_bytes, int32_t* d_err, void* stream) {
+    if (!valid_group_shape(N, K)) return TERN_ERR_SHAPE;
+    if (N == 0) return TERN_OK;
+    if (d_packed == nullptr || d_q8 == nullptr || d_f == nullptr || d_tiled == nullptr) return TERN_ERR_NULL;
+    if (!aligned(d_packed, 4) || !aligned(d_f, 4) || !aligned(d_tiled, 16)) return TERN_ERR_ALIGN;
+    if (d_err != nullptr && !aligned(d_err, 4)) return TERN_ERR_ALIGN;
+    if (tiled_bytes < tern_tiled_s8_bytes(N, K)) return TERN_ERR_SIZE;
+    return from_cuda(tern::launch_repack_s8(d_packed, d_q8, d_f, N, K, static_cast<uint8_t*>(d_tiled), d_err,
+                                            as_stream(stream)));
+}
+
+tern_status tern_linear_s8(const void* d_X, int x_type, int64_t ldx, const void* d_tiled_s8, int64_t M,
+                           int64_t K, int n_out, const int64_t* n_sizes, void* const* d_Ys,
+                           const int64_t* ldys, int out_type, void* d_ws, size_t ws_bytes, void* stream) {
+    return linear_ex(d_X, x_type, ldx, d_tiled_s8, M, K, n_out, n_sizes, d_Ys, ldys, out_type, d_ws, ws_bytes,
+                     stream, true);
 }
 
 size_t tern_tiled_glu_bytes(int64_t I, int64_t K) {

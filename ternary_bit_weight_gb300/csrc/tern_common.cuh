@@ -15,6 +15,7 @@ constexpr int kTileRows = 128;         // rows per tile of the tiled layout
 constexpr int kUnitCodeBytes = 4096;   // 128 rows x 128 weights x 2 bits
 constexpr int kUnitScaleBytes = 256;   // 128 FP16 scales
 constexpr int kUnitBytes = kUnitCodeBytes + kUnitScaleBytes;
+constexpr int kUnitScaleBytesS8 = 128;   // 128 int8 scales (INT8-scale layout)
 
 __host__ __device__ constexpr int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 __host__ __device__ constexpr int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }

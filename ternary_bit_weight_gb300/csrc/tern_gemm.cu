@@ -82,7 +82,10 @@ static_assert(kAbort + 4 <= kCtrlBytes, "control block");
 
 struct GemmArgs {
     const uint8_t* codes;
-    const uint8_t* scales;
+    const uint8_t* scales;     // per unit: 128 FP16 scales, or (s8) 128 int8 scales
+    const float* row_factor;   // s8: per row, the factor of its int8 scales
+    int s8;
+    int scale_unit;            // 256 or 128 (s8)
     const float* inv_scale;    // [M]: 2^-c_m
     int M;
     int NT;                    // tokens per tile
@@ -222,7 +225,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
                 const int cnt = g1 - g < kWG ? g1 - g : kWG;
                 const uint32_t st = wring + ws * kWStage;
                 if (elect_one()) {
-                    mbar_arrive_expect_tx(cb + kBarWFull + 8 * ws, (two ? 2 : 1) * cnt * kUnitBytes);
+                    mbar_arrive_expect_tx(cb + kBarWFull + 8 * ws, (two ? 2 : 1) * cnt * (kUnitCodeBytes + a.scale_unit));
 #pragma unroll
                     for (int rt = 0; rt < 2; ++rt) {
                         if (rt == 1 && !two) break;
@@ -230,7 +233,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
                         bulk_load(st + rt * kWG * kUnitCodeBytes, a.codes + u * kUnitCodeBytes, cnt * kUnitCodeBytes,
                                   cb + kBarWFull + 8 * ws);
                         bulk_load(st + 2 * kWG * kUnitCodeBytes + rt * kWG * kUnitScaleBytes,
-                                  a.scales + u * kUnitScaleBytes, cnt * kUnitScaleBytes, cb + kBarWFull + 8 * ws);
+                                  a.scales + u * a.scale_unit, cnt * a.scale_unit, cb + kBarWFull + 8 * ws);
                     }
                 }
                 __syncwarp();
@@ -376,8 +379,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
                     const uint8_t* st = wring_ptr + ws * kWStage;
                     c0 = lds_v4(st + rt * kWG * kUnitCodeBytes + wg * kUnitCodeBytes + 16 * r);
                     c1 = lds_v4(st + rt * kWG * kUnitCodeBytes + wg * kUnitCodeBytes + 2048 + 16 * r);
-                    const uint32_t sb = *reinterpret_cast<const uint16_t*>(
-                        st + 2 * kWG * kUnitCodeBytes + rt * kWG * kUnitScaleBytes + wg * kUnitScaleBytes + 2 * r);
+                    const uint8_t* sp = st + 2 * kWG * kUnitCodeBytes + rt * kWG * kUnitScaleBytes + wg * a.scale_unit;
+                    // int8 scale q: t * q is exact in fp16 (|q| <= 127); the row's factor comes at the end
+                    const uint32_t sb = a.s8 ? __half_as_ushort(__int2half_rn(*reinterpret_cast<const int8_t*>(sp + r)))
+                                             : *reinterpret_cast<const uint16_t*>(sp + 2 * r);
                     s2 = sb | (sb << 16);
                 }
                 if (acount >= kAU) {
@@ -439,9 +444,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
                     const int64_t row = (int64_t)(2 * it.bp + rt) * kTileRows + r;
                     const bool live = row < a.N;
                     const RowOut o = row_out(a.out, live ? row : 0);
+                    const float f = a.s8 ? a.row_factor[row] : 1.0f;
                     for (int c = 0; c < NT; c += 32) {
                         float inv[32];
                         load_inv(a.inv_scale + m0 + c, inv);
+#pragma unroll
+                        for (int m = 0; m < 32; ++m) inv[m] *= f;
                         uint32_t d[32];
                         if (c + 32 <= NT)
                             tmem_ld32_sync(tm + rt * NT + c, d);
@@ -493,6 +501,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
                         const int64_t row = (int64_t)(2 * it.bp + rt) * kTileRows + r;
                         const bool live = row < a.N;
                         const RowOut o = row_out(a.out, live ? row : 0);
+                        const float f = a.s8 ? a.row_factor[row] : 1.0f;
                         for (int c = 0; c < mvalid; c += 16) {
                             float v[16];
 #pragma unroll
@@ -504,6 +513,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
                             }
                             float inv[16];
                             load_inv(a.inv_scale + m0 + c, inv);
+#pragma unroll
+                            for (int m = 0; m < 16; ++m) inv[m] *= f;
 #pragma unroll
                             for (int m = 0; m < 16; ++m)
                                 if (c + m < mvalid) store_out(a.out, o, m0 + c + m, row, v[m] * inv[m], live);
@@ -646,8 +657,9 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sm_count) {
     return p;
 }
 
-cudaError_t launch_gemm(const uint16_t* X, bool x_f16, int64_t ldx, const uint8_t* tiled, int64_t M, int64_t N,
-                        int64_t K, const OutputSplit& out, void* ws, const GemmPlan& plan, cudaStream_t stream) {
+cudaError_t launch_gemm(const uint16_t* X, bool x_f16, int64_t ldx, const uint8_t* tiled, bool s8, int64_t M,
+                        int64_t N, int64_t K, const OutputSplit& out, void* ws, const GemmPlan& plan,
+                        cudaStream_t stream) {
     uint8_t* w = static_cast<uint8_t*>(ws);
     __half* x16 = reinterpret_cast<__half*>(w + plan.off_x16);
     float* inv = reinterpret_cast<float*>(w + plan.off_inv);
@@ -682,6 +694,10 @@ cudaError_t launch_gemm(const uint16_t* X, bool x_f16, int64_t ldx, const uint8_
     GemmArgs a = {};
     a.codes = tiled;
     a.scales = tiled + plan.R * plan.G * kUnitCodeBytes;
+    a.s8 = s8 ? 1 : 0;
+    a.scale_unit = s8 ? kUnitScaleBytesS8 : kUnitScaleBytes;
+    a.row_factor = s8 ? reinterpret_cast<const float*>(tiled + plan.R * plan.G * (kUnitCodeBytes + kUnitScaleBytesS8))
+                      : nullptr;
     a.inv_scale = inv;
     a.M = static_cast<int>(M);
     a.NT = plan.NT;

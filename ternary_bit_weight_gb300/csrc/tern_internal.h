@@ -22,6 +22,12 @@ constexpr int64_t glu_rows(int64_t I) { return 2 * ((I + 15) / 16) * 16; }
 cudaError_t launch_repack_glu(const uint8_t* packed_gate, const uint16_t* scales_gate, const uint8_t* packed_up,
                               const uint16_t* scales_up, int64_t I, int64_t K, uint8_t* tiled, int32_t* err,
                               cudaStream_t stream);
+// INT8-scale layout: codes as the tiled layout, then per unit 128 int8
+// scales, then per row tile 128 fp32 row factors.
+cudaError_t launch_repack_s8(const uint8_t* packed, const int8_t* q8, const float* f, int64_t N, int64_t K,
+                             uint8_t* tiled, int32_t* err, cudaStream_t stream);
+cudaError_t launch_quantize_scales(const uint16_t* scales, int64_t N, int64_t K, int8_t* q8, float* f,
+                                   cudaStream_t stream);
 cudaError_t launch_unrepack(const uint8_t* tiled, int64_t N, int64_t K, uint8_t* packed,
                             uint16_t* scales, int32_t* err, cudaStream_t stream);
 
@@ -67,7 +73,8 @@ struct StreamPlan {
 StreamPlan plan_stream(int64_t M, int64_t N, int64_t K, int sm_count);
 
 // x_f16: X holds fp16 rather than bf16 bits.
-cudaError_t launch_stream(const uint16_t* X, bool x_f16, int64_t ldx, const uint8_t* tiled, int64_t M,
+// s8: the tiled weights carry int8 scales and per-row factors (INT8-scale layout).
+cudaError_t launch_stream(const uint16_t* X, bool x_f16, int64_t ldx, const uint8_t* tiled, bool s8, int64_t M,
                           int64_t N, int64_t K, const OutputSplit& out, void* ws, const StreamPlan& plan,
                           cudaStream_t stream);
 
@@ -88,8 +95,9 @@ struct GemmPlan {
 
 GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sm_count);
 
-cudaError_t launch_gemm(const uint16_t* X, bool x_f16, int64_t ldx, const uint8_t* tiled, int64_t M, int64_t N,
-                        int64_t K, const OutputSplit& out, void* ws, const GemmPlan& plan, cudaStream_t stream);
+cudaError_t launch_gemm(const uint16_t* X, bool x_f16, int64_t ldx, const uint8_t* tiled, bool s8, int64_t M,
+                        int64_t N, int64_t K, const OutputSplit& out, void* ws, const GemmPlan& plan,
+                        cudaStream_t stream);
 
 // int8-activation variant: quantised activations in the code words' field
 // order, one CTA per (row tile, K split).

@@ -175,8 +175,11 @@ __device__ __forceinline__ void tiled_scale_coords(int64_t j, int64_t G, int64_t
 struct RepackSrc {
     const uint8_t* packed[2];
     const uint16_t* scales[2];
+    const int8_t* q8;   // s8: int8 scales [rows, G] and per-row factors [rows]
+    const float* f;
     int64_t rows;   // rows per source
     int glu;
+    int s8;
 };
 
 __device__ __forceinline__ bool source_row(const RepackSrc& s, int64_t n, int& which, int64_t& row) {
@@ -201,6 +204,8 @@ repack_kernel(const RepackSrc src, int64_t K, int64_t units, uint8_t* __restrict
     const int64_t G = K / kGroup;
     const int64_t row_bytes = K / 4;
     uint16_t* tscales = reinterpret_cast<uint16_t*>(tiled + units * kUnitCodeBytes);
+    int8_t* tscales8 = reinterpret_cast<int8_t*>(tiled + units * kUnitCodeBytes);
+    float* tfactor = reinterpret_cast<float*>(tiled + units * (kUnitCodeBytes + kUnitScaleBytesS8));
     int bad = 0;
     for (int64_t i = blockIdx.x * (int64_t)kThreads + threadIdx.x; i < units * kTileRows;
          i += (int64_t)gridDim.x * kThreads) {
@@ -223,14 +228,19 @@ repack_kernel(const RepackSrc src, int64_t K, int64_t units, uint8_t* __restrict
 #pragma unroll
                 for (int q = 0; q < 8; ++q) w[q] = __ldg(reinterpret_cast<const uint32_t*>(p) + q);
             }
-            sc = __ldg((which ? src.scales[1] : src.scales[0]) + row * G + g);
+            if (!src.s8) sc = __ldg((which ? src.scales[1] : src.scales[0]) + row * G + g);
         }
         uint8_t* u = tiled + unit * kUnitCodeBytes + 16 * r;
         *reinterpret_cast<uint4*>(u) = make_uint4(disk_to_tiled_word(w[0], bad), disk_to_tiled_word(w[1], bad),
                                                   disk_to_tiled_word(w[2], bad), disk_to_tiled_word(w[3], bad));
         *reinterpret_cast<uint4*>(u + 2048) = make_uint4(disk_to_tiled_word(w[4], bad), disk_to_tiled_word(w[5], bad),
                                                          disk_to_tiled_word(w[6], bad), disk_to_tiled_word(w[7], bad));
-        tscales[unit * kTileRows + r] = sc;
+        if (src.s8) {
+            tscales8[unit * kTileRows + r] = valid ? src.q8[row * G + g] : int8_t(0);
+            if (g == 0) tfactor[b * kTileRows + r] = valid ? src.f[row] : 0.f;
+        } else {
+            tscales[unit * kTileRows + r] = sc;
+        }
     }
     __threadfence();   // writes visible GPU-wide before exit (early-starting successors)
     count_errors(err, bad);
@@ -320,6 +330,44 @@ cudaError_t launch_repack(const uint8_t* packed, const uint16_t* scales, int64_t
     const bool vec = (reinterpret_cast<uintptr_t>(packed) & 15) == 0;
     return vec ? launch_flat(repack_kernel<true>, units * kTileRows, stream, src, K, units, tiled, err)
                : launch_flat(repack_kernel<false>, units * kTileRows, stream, src, K, units, tiled, err);
+}
+
+cudaError_t launch_repack_s8(const uint8_t* packed, const int8_t* q8, const float* f, int64_t N, int64_t K,
+                             uint8_t* tiled, int32_t* err, cudaStream_t stream) {
+    RepackSrc src = {};
+    src.packed[0] = src.packed[1] = packed;
+    src.q8 = q8;
+    src.f = f;
+    src.rows = N;
+    src.s8 = 1;
+    const int64_t units = ceil_div(N, kTileRows) * (K / kGroup);
+    const bool vec = (reinterpret_cast<uintptr_t>(packed) & 15) == 0;
+    return vec ? launch_flat(repack_kernel<true>, units * kTileRows, stream, src, K, units, tiled, err)
+               : launch_flat(repack_kernel<false>, units * kTileRows, stream, src, K, units, tiled, err);
+}
+
+// FP16 scales -> int8 scales and per-row factors, in fp32 with ties to
+// even: f = max_g |s| / 127, q = rint(s * (127 / max_g |s|)).
+__global__ void __launch_bounds__(kThreads)
+quantize_scales_kernel(const uint16_t* __restrict__ scales, int64_t N, int64_t G, int8_t* __restrict__ q8,
+                       float* __restrict__ f) {
+    for (int64_t n = blockIdx.x * (int64_t)kThreads + threadIdx.x; n < N; n += (int64_t)gridDim.x * kThreads) {
+        float mx = 0.f;
+        for (int64_t g = 0; g < G; ++g) mx = fmaxf(mx, fabsf(fp16_bits_to_float(scales[n * G + g])));
+        const float inv = mx > 0.f ? 127.0f / mx : 0.f;
+        f[n] = mx / 127.0f;
+        for (int64_t g = 0; g < G; ++g) {
+            float q = rintf(fp16_bits_to_float(scales[n * G + g]) * inv);
+            q = fminf(fmaxf(q, -127.f), 127.f);
+            q8[n * G + g] = static_cast<int8_t>(q);
+        }
+    }
+    __threadfence();
+}
+
+cudaError_t launch_quantize_scales(const uint16_t* scales, int64_t N, int64_t K, int8_t* q8, float* f,
+                                   cudaStream_t stream) {
+    return launch_flat(quantize_scales_kernel, N, stream, scales, N, K / kGroup, q8, f);
 }
 
 cudaError_t launch_repack_glu(const uint8_t* packed_gate, const uint16_t* scales_gate, const uint8_t* packed_up,

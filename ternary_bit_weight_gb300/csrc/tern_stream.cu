@@ -124,7 +124,10 @@ __host__ __device__ constexpr int64_t x_smem_bytes(int64_t K) { return round_up(
 
 struct StreamArgs {
     const uint8_t* codes;
-    const uint8_t* scales;
+    const uint8_t* scales;     // per unit: 128 FP16 scales, or (s8) 128 int8 scales
+    const float* row_factor;   // s8: per row, the factor of its int8 scales ([R * 128])
+    int s8;
+    int scale_unit;            // bytes of one unit's scales: 256, or 128 (s8)
     const uint16_t* x;         // M == 1: the activation row
     int M;
     int G;                     // groups per row
@@ -156,6 +159,12 @@ __device__ __forceinline__ void flush_tile(const StreamArgs& a, int64_t v, int64
     const int lane = r & 31, quad = r >> 5;
     const int64_t row = b * kTileRows + r;
     const int mvalid = a.M < NCOL ? a.M : NCOL;
+    if (a.s8) {
+        // int8 scales: the group sums were weighted by q; the row's factor once
+        const float f = a.row_factor[b * kTileRows + r];
+#pragma unroll
+        for (int m = 0; m < NCOL; ++m) acc[m] *= f;
+    }
     const bool live = row < a.N;
     const RowOut o = row_out(a.out, live ? row : 0);
     if (whole) {
@@ -282,9 +291,9 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
             const int64_t uf = u0 + (int64_t)f * kPS;
             const int32_t cnt = n - f * kPS < kPS ? n - f * kPS : kPS;
             if (elect_one()) {
-                mbar_arrive_expect_tx(bar, cnt * (kUnitBytes + C::XUnit));
+                mbar_arrive_expect_tx(bar, cnt * (kUnitCodeBytes + a.scale_unit + C::XUnit));
                 bulk_load(st + C::OffCodes, a.codes + uf * kUnitCodeBytes, cnt * kUnitCodeBytes, bar);
-                bulk_load(st + C::OffScales, a.scales + uf * kUnitScaleBytes, cnt * kUnitScaleBytes, bar);
+                bulk_load(st + C::OffScales, a.scales + uf * a.scale_unit, cnt * a.scale_unit, bar);
             }
             __syncwarp();
         };
@@ -482,7 +491,7 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
         // ------------------------------------------------------- promotion
         const int r = threadIdx.x & 127;   // weight row in the tile = tensor-memory lane
         const uint32_t tm = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + kDCol0;
-        const int scale_off = C::OffScales + 2 * r;   // + unit in stage * 256
+        const int scale_off = C::OffScales + (a.s8 ? 1 : 2) * r;   // + unit in stage * scale_unit
         const int64_t first_tile = u0 / G;
         const int32_t first_g = static_cast<int32_t>(u0 - first_tile * G);
         int64_t pb = first_tile;
@@ -508,9 +517,15 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
                 tmem_ld_32x32b_x16(tm + 2 * dp * kNtok, *reinterpret_cast<uint32_t(*)[16]>(d));
                 tmem_ld_32x32b_x16(tm + (2 * dp + 1) * kNtok, *reinterpret_cast<uint32_t(*)[16]>(d + NCOL));
             }
-            const uint8_t* sp = ring_ptr + s * C::StageBytes + scale_off + us * kUnitScaleBytes;
-            const float sc0 = fp16_bits_to_float(*reinterpret_cast<const uint16_t*>(sp));
-            const float sc1 = two ? fp16_bits_to_float(*reinterpret_cast<const uint16_t*>(sp + kUnitScaleBytes)) : 0.f;
+            const uint8_t* sp = ring_ptr + s * C::StageBytes + scale_off + us * a.scale_unit;
+            float sc0, sc1;
+            if (a.s8) {
+                sc0 = static_cast<float>(*reinterpret_cast<const int8_t*>(sp));
+                sc1 = two ? static_cast<float>(*reinterpret_cast<const int8_t*>(sp + a.scale_unit)) : 0.f;
+            } else {
+                sc0 = fp16_bits_to_float(*reinterpret_cast<const uint16_t*>(sp));
+                sc1 = two ? fp16_bits_to_float(*reinterpret_cast<const uint16_t*>(sp + a.scale_unit)) : 0.f;
+            }
             tmem_ld_wait();
             tc_fence_before_sync();
             __syncwarp();
@@ -651,12 +666,15 @@ StreamPlan plan_stream(int64_t M, int64_t N, int64_t K, int sm_count) {
     return p;
 }
 
-cudaError_t launch_stream(const uint16_t* X, bool x_f16, int64_t ldx, const uint8_t* tiled, int64_t M,
+cudaError_t launch_stream(const uint16_t* X, bool x_f16, int64_t ldx, const uint8_t* tiled, bool s8, int64_t M,
                           int64_t N, int64_t K, const OutputSplit& out, void* ws, const StreamPlan& plan,
                           cudaStream_t stream) {
     StreamArgs a = {};
     a.codes = tiled;
     a.scales = tiled + plan.U * kUnitCodeBytes;
+    a.s8 = s8 ? 1 : 0;
+    a.scale_unit = s8 ? kUnitScaleBytesS8 : kUnitScaleBytes;
+    a.row_factor = s8 ? reinterpret_cast<const float*>(tiled + plan.U * (kUnitCodeBytes + kUnitScaleBytesS8)) : nullptr;
     a.x = X;
     a.M = static_cast<int>(M);
     a.G = static_cast<int>(plan.G);

@@ -203,3 +203,16 @@ def test_i8_argument_errors():
     assert f(FAKE, FAKE, FAKE, 1, 64, 256, FAKE + 2, 64, 0, FAKE, 1 << 20, None) == 3
     assert f(FAKE, FAKE, FAKE, 1, 64, 256, FAKE, 63, 0, FAKE, 1 << 20, None) == 2
     assert binding.tern_i8_workspace_bytes(1, 64, 256) >= 256
+
+
+def test_s8_sizes_and_argument_errors():
+    for N, K in [(1, 128), (130, 256), (55296, 5120)]:
+        R, G = (N + 127) // 128, K // 128
+        assert binding.tern_tiled_s8_bytes(N, K) == oracle.tiled_s8_bytes(N, K) == R * G * 4224 + R * 512
+    lib = binding.library()
+    need = binding.tern_tiled_s8_bytes(32, 256)
+    assert lib.tern_repack_s8(FAKE, FAKE, FAKE, 32, 200, FAKE, need, None, None) == 2
+    assert lib.tern_repack_s8(FAKE, None, FAKE, 32, 256, FAKE, need, None, None) == 1
+    assert lib.tern_repack_s8(FAKE, FAKE, FAKE, 32, 256, FAKE, need - 1, None, None) == 4
+    assert lib.tern_quantize_scales(FAKE, 32, 256, FAKE, FAKE + 2, None) == 3
+    assert lib.tern_quantize_scales(FAKE, 32, 100, FAKE, FAKE, None) == 2

@@ -486,3 +486,58 @@ def test_linear_i8_matches_integer_matmul():
     w = t.astype(np.float64) * np.repeat(s.astype(np.float64), 128, axis=1)
     mag = a.astype(np.float64)[:, None] * (np.abs(q.astype(np.float64)) @ np.abs(w).T)
     assert np.allclose(b, mag, rtol=1e-13)
+
+
+# ------------------------------------------------------ INT8 group scales
+
+def test_quantize_scales_hand_worked():
+    # row max 0.05 -> f = 0.05/127; 0.025 -> 63.5 -> 64 (tie to even)
+    s = np.array([[0.05, 0.025, 0.0125, -0.05]], dtype=np.float16)
+    q8, f = oracle.quantize_scales(s.view(np.uint16), 512)
+    m = np.float32(np.float16(0.05))
+    assert f[0] == m / np.float32(127.0)
+    inv = np.float32(127.0) / m
+    want = [int(np.rint(np.float32(np.float16(v)) * inv)) for v in (0.05, 0.025, 0.0125, -0.05)]
+    assert q8[0].tolist() == want and want[0] == 127 and want[3] == -127
+    # exactly representable case: scales 1, 0.5, 0.25 with max 1 -> f = 1/127
+    s = np.array([[1.0, 0.5, 0.25, -1.0]], dtype=np.float16)
+    q8, f = oracle.quantize_scales(s.view(np.uint16), 512)
+    assert q8[0].tolist() == [127, 64, 32, -127]          # 63.5 -> 64, 31.75 -> 32
+    q8, f = oracle.quantize_scales(np.zeros((1, 2), dtype=np.uint16), 256)
+    assert f[0] == 0.0 and not q8.any()
+
+
+def test_repack_s8_layout_by_hand():
+    rng = np.random.default_rng(2)
+    N, K = 130, 256                                      # two row tiles, the second ragged
+    t = rng.integers(-1, 2, (N, K)).astype(np.int8)
+    packed, _ = oracle.pack(t)
+    q8 = rng.integers(-127, 128, (N, K // 128)).astype(np.int8)
+    f = rng.uniform(1e-4, 1e-3, N).astype(np.float32)
+    tiled = oracle.repack_s8(packed, q8, f, K)
+    R, G = 2, 2
+    assert tiled.size == oracle.tiled_s8_bytes(N, K) == R * G * 4224 + R * 512
+    base = R * G * 4096
+    # unit (b=1, g=0) starts at base + (1*2 + 0)*128; its row 1 is weight row 129
+    assert tiled.view(np.int8)[base + 2 * 128 + 1] == q8[129, 0]
+    assert tiled.view(np.int8)[base + 1 * 128 + 5] == q8[5, 1]
+    assert not tiled[base + 2 * 128 + 2:base + 3 * 128].any()    # rows 130..255: padding
+    fac = tiled[base + R * G * 128:].view(np.float32)
+    assert fac[129] == f[129] and fac[0] == f[0] and not fac[130:].any()
+    # the code units are those of the plain tiled layout
+    plain, _ = oracle.repack(packed, np.zeros((N, 2), dtype=np.uint16), K)
+    assert np.array_equal(tiled[:base], plain[:base])
+
+
+def test_linear_s8_matches_dense_matmul():
+    rng = np.random.default_rng(12)
+    M, N, K = 2, 5, 256
+    t = rng.integers(-1, 2, (N, K)).astype(np.int8)
+    q8 = rng.integers(-127, 128, (N, K // 128)).astype(np.int8)
+    f = rng.uniform(1e-4, 1e-3, N).astype(np.float32)
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    xb = (x.view(np.uint32) >> 16).astype(np.uint16)
+    y, _ = oracle.linear_s8(xb, oracle.pack(t)[0], q8, f, K)
+    w = t.astype(np.float64) * np.repeat(q8.astype(np.float64), 128, axis=1) * f.astype(np.float64)[:, None]
+    xd = (xb.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    assert np.allclose(y, xd @ w.T, rtol=1e-12, atol=1e-15)
