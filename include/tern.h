@@ -263,6 +263,29 @@ tern_status tern_linear_swiglu(const void* d_X, int x_type, int64_t ldx, const v
                                int out_type, void* d_ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Zero-block skipping ([EMB] §6, outlook: skip blocks that are all zero
+ * with a sparse mask).  A unit (128 rows x 128 weights of the tiled
+ * layout) whose weights are all 0 contributes nothing: with its flag set
+ * the linear kernels neither copy, decode nor multiply it.
+ * ---------------------------------------------------------------------- */
+
+/* Units of the tiled layout: ceil(N/128) * (K/128); unit (b, g) has index b*G + g. */
+size_t tern_unit_count(int64_t N, int64_t K);
+
+/* d_flags[u] (device uint8, tern_unit_count entries) = 1 if every weight of
+ * unit u is 0, else 0.  Reads only the code units, so it serves the plain,
+ * GLU and INT8-scale layouts alike. */
+tern_status tern_zero_units(const void* d_tiled, int64_t N, int64_t K, uint8_t* d_flags, void* stream);
+
+/* tern_linear_ex (plain tiled layout) skipping the units flagged in d_flags
+ * (as written by tern_zero_units; a flag set on a unit that is not all
+ * zero drops that unit's contribution). */
+tern_status tern_linear_sparse(const void* d_X, int x_type, int64_t ldx, const void* d_tiled,
+                               const uint8_t* d_flags, int64_t M, int64_t K, int n_out,
+                               const int64_t* n_sizes, void* const* d_Ys, const int64_t* ldys,
+                               int out_type, void* d_ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * INT8 group scales ([EMB] §6, outlook: compress the FP16 scales to INT8).
  * The page gives no format; this library's reading: one fp32 factor per
  * row and one int8 per group,

@@ -250,6 +250,18 @@ def linear_i8(q: np.ndarray, a: np.ndarray, packed: np.ndarray, scales: np.ndarr
     return y, b
 
 
+def zero_units(packed: np.ndarray, K: int) -> np.ndarray:
+    """Per unit (128 rows x 128 weights, rows padded to a multiple of 128
+    with zeros, index b*G + g): 1 if every weight is 0 (codes 00 or 11)."""
+    t, _ = unpack(packed, K)
+    N = t.shape[0]
+    R, G = (N + 127) // 128, K // 128
+    pad = np.zeros((R * 128, K), dtype=np.int8)
+    pad[:N] = t
+    blocks = pad.reshape(R, 128, G, 128)
+    return (~blocks.any(axis=(1, 3))).astype(np.uint8).reshape(-1)
+
+
 def swiglu(g: np.ndarray, u: np.ndarray) -> np.ndarray:
     """silu(g) * u elementwise in fp64 (silu(g) = g / (1 + e^-g))."""
     g = _c(g, np.float64)

@@ -27,7 +27,7 @@ EXPORTED = ("tern_status_string", "tern_version", "tern_pack", "tern_unpack", "t
             "tern_repack_glu", "tern_swiglu_workspace_bytes", "tern_linear_swiglu",
             "tern_workspace_error", "tern_workspace_reset", "tern_xq_bytes", "tern_quantize_x",
             "tern_i8_workspace_bytes", "tern_linear_i8", "tern_tiled_s8_bytes", "tern_quantize_scales",
-            "tern_repack_s8", "tern_linear_s8")
+            "tern_repack_s8", "tern_linear_s8", "tern_unit_count", "tern_zero_units", "tern_linear_sparse")
 
 
 class TernError(RuntimeError):
@@ -96,6 +96,13 @@ def _load():
     lib.tern_repack_s8.restype = i32
     lib.tern_linear_s8.argtypes = list(lib.tern_linear_ex.argtypes)
     lib.tern_linear_s8.restype = i32
+    lib.tern_unit_count.argtypes = [i64, i64]
+    lib.tern_unit_count.restype = sz
+    lib.tern_zero_units.argtypes = [vp, i64, i64, vp, vp]
+    lib.tern_zero_units.restype = i32
+    lib.tern_linear_sparse.argtypes = [vp, i32, i64, vp, vp, i64, i64, i32, ctypes.POINTER(i64),
+                                       ctypes.POINTER(vp), ctypes.POINTER(i64), i32, vp, sz, vp]
+    lib.tern_linear_sparse.restype = i32
     return lib
 
 
@@ -300,3 +307,23 @@ def tern_linear_s8(X, x_type: int, ldx: int, tiled_s8, M: int, K: int, n_sizes, 
         ws_bytes = _nbytes(ws)
     _check(_lib.tern_linear_s8(_p(X), x_type, ldx, _p(tiled_s8), M, K, n_out, sizes, ptrs, lds, out_type,
                                _p(ws), ws_bytes, _s(stream)), "tern_linear_s8")
+
+
+def tern_unit_count(N: int, K: int) -> int:
+    return int(_lib.tern_unit_count(N, K))
+
+
+def tern_zero_units(tiled, N: int, K: int, flags, stream=None):
+    _check(_lib.tern_zero_units(_p(tiled), N, K, _p(flags), _s(stream)), "tern_zero_units")
+
+
+def tern_linear_sparse(X, x_type: int, ldx: int, tiled, flags, M: int, K: int, n_sizes, Ys, ldys, out_type: int,
+                       ws=None, ws_bytes: int | None = None, stream=None):
+    n_out = len(n_sizes)
+    sizes = (ctypes.c_int64 * n_out)(*[int(v) for v in n_sizes])
+    ptrs = (ctypes.c_void_p * n_out)(*[_p(y) for y in Ys])
+    lds = (ctypes.c_int64 * n_out)(*[int(v) for v in ldys])
+    if ws_bytes is None:
+        ws_bytes = _nbytes(ws)
+    _check(_lib.tern_linear_sparse(_p(X), x_type, ldx, _p(tiled), _p(flags), M, K, n_out, sizes, ptrs, lds,
+                                   out_type, _p(ws), ws_bytes, _s(stream)), "tern_linear_sparse")

@@ -20,7 +20,7 @@ inline bool valid_group_shape(int64_t N, int64_t K) { return N >= 0 && K > 0 && 
 
 tern_status run_linear(const uint16_t* X, bool x_f16, int64_t ldx, const void* tiled, int64_t M, int64_t N,
                        int64_t K, const tern::OutputSplit& out, void* ws, size_t ws_bytes,
-                       cudaStream_t stream, bool s8 = false) {
+                       cudaStream_t stream, bool s8 = false, const uint8_t* zflags = nullptr) {
     const int sms = tern::device_sm_count();
     if (sms <= 0) return TERN_ERR_UNSUPPORTED;
     if (ws == nullptr) return TERN_ERR_NULL;
@@ -30,11 +30,11 @@ tern_status run_linear(const uint16_t* X, bool x_f16, int64_t ldx, const void* t
     if (M <= tern::kStreamMaxM) {
         const tern::StreamPlan plan = tern::plan_stream(M, N, K, sms);
         if (ws_bytes < plan.ws_bytes) return TERN_ERR_SIZE;
-        e = tern::launch_stream(X, x_f16, ldx, w, s8, M, N, K, out, ws, plan, stream);
+        e = tern::launch_stream(X, x_f16, ldx, w, s8, zflags, M, N, K, out, ws, plan, stream);
     } else {
         const tern::GemmPlan plan = tern::plan_gemm(M, N, K, sms);
         if (ws_bytes < plan.ws_bytes) return TERN_ERR_SIZE;
-        e = tern::launch_gemm(X, x_f16, ldx, w, s8, M, N, K, out, ws, plan, stream);
+        e = tern::launch_gemm(X, x_f16, ldx, w, s8, zflags, M, N, K, out, ws, plan, stream);
     }
     return e == cudaSuccess ? TERN_OK : TERN_ERR_CUDA;
 }
@@ -165,7 +165,7 @@ tern_status tern_linear_multi(const uint16_t* d_X, int64_t ldx, const void* d_ti
 static tern_status linear_ex(const void* d_X, int x_type, int64_t ldx, const void* d_tiled, int64_t M,
                              int64_t K, int n_out, const int64_t* n_sizes, void* const* d_Ys,
                              const int64_t* ldys, int out_type, void* d_ws, size_t ws_bytes, void* stream,
-                             bool s8) {
+                             bool s8, const uint8_t* zflags = nullptr) {
     if (x_type != TERN_X_BF16 && x_type != TERN_X_F16) return TERN_ERR_SHAPE;
     if (out_type != TERN_OUT_F32 && out_type != TERN_OUT_BF16 && out_type != TERN_OUT_F16) return TERN_ERR_SHAPE;
     if (n_out < 1 || n_out > tern::kMaxOutputs) return TERN_ERR_SHAPE;
@@ -194,7 +194,8 @@ static tern_status linear_ex(const void* d_X, int x_type, int64_t ldx, const voi
         out.y[j] = d_Ys[j];
         out.ldy[j] = ldys[j];
     }
-    return run_linear(X, x_type == TERN_X_F16, ldx, d_tiled, M, N, K, out, d_ws, ws_bytes, as_stream(stream), s8);
+    return run_linear(X, x_type == TERN_X_F16, ldx, d_tiled, M, N, K, out, d_ws, ws_bytes, as_stream(stream), s8,
+                      zflags);
 }
 
 tern_status tern_linear_ex(const void* d_X, int x_type, int64_t ldx, const void* d_tiled, int64_t M,
@@ -202,6 +203,29 @@ tern_status tern_linear_ex(const void* d_X, int x_type, int64_t ldx, const void*
                            const int64_t* ldys, int out_type, void* d_ws, size_t ws_bytes, void* stream) {
     return linear_ex(d_X, x_type, ldx, d_tiled, M, K, n_out, n_sizes, d_Ys, ldys, out_type, d_ws, ws_bytes, stream,
                      false);
+}
+
+size_t tern_unit_count(int64_t N, int64_t K) {
+    if (!valid_group_shape(N, K)) return 0;
+    return (size_t)ceil_div(N, tern::kTileRows) * (size_t)(K / tern::kGroup);
+}
+
+tern_status tern_zero_units(const void* d_tiled, int64_t N, int64_t K, uint8_t* d_flags, void* stream) {
+    if (!valid_group_shape(N, K)) return TERN_ERR_SHAPE;
+    if (N == 0) return TERN_OK;
+    if (d_tiled == nullptr || d_flags == nullptr) return TERN_ERR_NULL;
+    if (!aligned(d_tiled, 16)) return TERN_ERR_ALIGN;
+    return from_cuda(tern::launch_zero_units(static_cast<const uint8_t*>(d_tiled), (int64_t)tern_unit_count(N, K),
+                                             d_flags, as_stream(stream)));
+}
+
+tern_status tern_linear_sparse(const void* d_X, int x_type, int64_t ldx, const void* d_tiled,
+                               const uint8_t* d_flags, int64_t M, int64_t K, int n_out, const int64_t* n_sizes,
+                               void* const* d_Ys, const int64_t* ldys, int out_type, void* d_ws, size_t ws_bytes,
+                               void* stream) {
+    if (d_flags == nullptr) return TERN_ERR_NULL;
+    return linear_ex(d_X, x_type, ldx, d_tiled, M, K, n_out, n_sizes, d_Ys, ldys, out_type, d_ws, ws_bytes, stream,
+                     false, d_flags);
 }
 
 size_t tern_tiled_s8_bytes(int64_t N, int64_t K) {

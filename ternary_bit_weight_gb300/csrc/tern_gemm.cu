@@ -86,6 +86,7 @@ struct GemmArgs {
     const float* row_factor;   // s8: per row, the factor of its int8 scales
     int s8;
     int scale_unit;            // 256 or 128 (s8)
+    const uint8_t* zflags;     // optional, per unit: 1 = every weight of the unit is 0 (skipped)
     const float* inv_scale;    // [M]: 2^-c_m
     int M;
     int NT;                    // tokens per tile
@@ -140,6 +141,18 @@ __device__ __forceinline__ void load_inv(const float* p, float (&inv)[C]) {
         inv[4 * i + 2] = v.z;
         inv[4 * i + 3] = v.w;
     }
+}
+
+__device__ __forceinline__ bool unit_zero(const GemmArgs& a, int64_t tile, int g) {
+    return a.zflags != nullptr && a.zflags[tile * a.G + g] != 0;
+}
+
+// Whether row tile `tile` has a non-zero unit among groups [g0, g1).
+__device__ __forceinline__ bool tile_has_data(const GemmArgs& a, int64_t tile, int g0, int g1) {
+    if (a.zflags == nullptr) return true;
+    for (int g = g0; g < g1; ++g)
+        if (a.zflags[tile * a.G + g] == 0) return true;
+    return false;
 }
 
 // Item i -> (row-tile pair, token tile, K split), token tile slowest so that
@@ -300,8 +313,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
             int g0, g1;
             group_range(a, it.ks, g0, g1);
             const bool two = 2 * it.bp + 1 < a.R;
+            bool started0 = false, started1 = false;   // accumulators written this item
             for (int g = g0; g < g1; ++g) {
                 const int xg = (g - g0) % kXG;
+                const bool z0 = unit_zero(a, 2 * it.bp, g), z1 = !two || unit_zero(a, 2 * it.bp + 1, g);
                 uint32_t bar = 0, par = 0;
                 bool act = false;
                 if (lane == 1) {
@@ -325,15 +340,20 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint64_t bdesc = b0 + (uint32_t)((kk >> 2) * (NT * 128 / 16)) + 2 * (kk & 3);
-                        const uint32_t acc = (g > g0 || kk > 0) ? 1u : 0u;
-                        umma_bf16_tmem_a(tmem + kDCol0, tmem + al * kACols + 8 * kk, bdesc, idesc, acc);
-                        if (two) umma_bf16_tmem_a(tmem + kDCol0 + NT, tmem + (kAU + al) * kACols + 8 * kk, bdesc, idesc, acc);
+                        if (!z0)
+                            umma_bf16_tmem_a(tmem + kDCol0, tmem + al * kACols + 8 * kk, bdesc, idesc,
+                                             (started0 || kk > 0) ? 1u : 0u);
+                        if (!z1)
+                            umma_bf16_tmem_a(tmem + kDCol0 + NT, tmem + (kAU + al) * kACols + 8 * kk, bdesc, idesc,
+                                             (started1 || kk > 0) ? 1u : 0u);
                     }
                     umma_commit(cb + kBarAEmpty + 8 * al);
                     if (xg == kXG - 1 || g == g1 - 1) umma_commit(cb + kBarXEmpty + 8 * xs);
                     if (g == g1 - 1) umma_commit(cb + kBarDFull);
                 }
                 __syncwarp();
+                started0 |= !z0;
+                started1 |= !z1;
                 if (++al == kAU) {
                     al = 0;
                     a_ph ^= 1u;
@@ -369,10 +389,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
             const Item it = item_of(a, i);
             int g0, g1;
             group_range(a, it.ks, g0, g1);
-            const bool mine = rt == 0 || 2 * it.bp + 1 < a.R;
+            const bool tile_exists = rt == 0 || 2 * it.bp + 1 < a.R;
             for (int g = g0; g < g1; ++g) {
                 const int wg = (g - g0) % kWG;
                 if (wg == 0 && !(ok = warp_wait(cb + kBarWFull + 8 * ws, w_ph, abort_flag))) break;
+                const bool mine = tile_exists && !unit_zero(a, 2 * it.bp + rt, g);   // a zero unit needs no A
                 uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0;
                 uint32_t s2 = 0;
                 if (mine) {
@@ -445,16 +466,20 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
                     const bool live = row < a.N;
                     const RowOut o = row_out(a.out, live ? row : 0);
                     const float f = a.s8 ? a.row_factor[row] : 1.0f;
+                    const bool data = tile_has_data(a, 2 * it.bp + rt, 0, a.G);   // else the accumulators are stale
                     for (int c = 0; c < NT; c += 32) {
                         float inv[32];
                         load_inv(a.inv_scale + m0 + c, inv);
 #pragma unroll
-                        for (int m = 0; m < 32; ++m) inv[m] *= f;
+                        for (int m = 0; m < 32; ++m) inv[m] *= data ? f : 0.f;
                         uint32_t d[32];
                         if (c + 32 <= NT)
                             tmem_ld32_sync(tm + rt * NT + c, d);
                         else
                             tmem_ld16_sync(tm + rt * NT + c, d);
+                        if (!data)
+#pragma unroll
+                            for (int m = 0; m < 32; ++m) d[m] = 0u;
 #pragma unroll
                         for (int m = 0; m < 32; ++m)
                             if (c + m < mvalid) store_out(a.out, o, m0 + c + m, row, __uint_as_float(d[m]) * inv[m], live);
@@ -467,14 +492,20 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
                 // publish this split's partial; the last split of the tile sums
                 // all partials in split order
                 float* base = a.partial + (tile * a.KS + it.ks) * (2 * (int64_t)NT * kTileRows);
+                int g0, g1;
+                group_range(a, it.ks, g0, g1);
                 for (int rt = 0; rt < 2; ++rt) {
                     if (rt == 1 && !two) break;
+                    const bool data = tile_has_data(a, 2 * it.bp + rt, g0, g1);
                     for (int c = 0; c < NT; c += 32) {
                         uint32_t d[32];
                         if (c + 32 <= NT)
                             tmem_ld32_sync(tm + rt * NT + c, d);
                         else
                             tmem_ld16_sync(tm + rt * NT + c, d);
+                        if (!data)
+#pragma unroll
+                            for (int m = 0; m < 32; ++m) d[m] = 0u;
 #pragma unroll
                         for (int m = 0; m < 32; ++m)
                             if (c + m < NT) base[((int64_t)rt * NT + c + m) * kTileRows + r] = __uint_as_float(d[m]);
@@ -657,9 +688,9 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sm_count) {
     return p;
 }
 
-cudaError_t launch_gemm(const uint16_t* X, bool x_f16, int64_t ldx, const uint8_t* tiled, bool s8, int64_t M,
-                        int64_t N, int64_t K, const OutputSplit& out, void* ws, const GemmPlan& plan,
-                        cudaStream_t stream) {
+cudaError_t launch_gemm(const uint16_t* X, bool x_f16, int64_t ldx, const uint8_t* tiled, bool s8,
+                        const uint8_t* zflags, int64_t M, int64_t N, int64_t K, const OutputSplit& out, void* ws,
+                        const GemmPlan& plan, cudaStream_t stream) {
     uint8_t* w = static_cast<uint8_t*>(ws);
     __half* x16 = reinterpret_cast<__half*>(w + plan.off_x16);
     float* inv = reinterpret_cast<float*>(w + plan.off_inv);
@@ -695,6 +726,7 @@ cudaError_t launch_gemm(const uint16_t* X, bool x_f16, int64_t ldx, const uint8_
     a.codes = tiled;
     a.scales = tiled + plan.R * plan.G * kUnitCodeBytes;
     a.s8 = s8 ? 1 : 0;
+    a.zflags = zflags;
     a.scale_unit = s8 ? kUnitScaleBytesS8 : kUnitScaleBytes;
     a.row_factor = s8 ? reinterpret_cast<const float*>(tiled + plan.R * plan.G * (kUnitCodeBytes + kUnitScaleBytesS8))
                       : nullptr;

@@ -28,6 +28,9 @@ cudaError_t launch_repack_s8(const uint8_t* packed, const int8_t* q8, const floa
                              uint8_t* tiled, int32_t* err, cudaStream_t stream);
 cudaError_t launch_quantize_scales(const uint16_t* scales, int64_t N, int64_t K, int8_t* q8, float* f,
                                    cudaStream_t stream);
+// Per unit of the tiled codes: 1 if every weight is zero (every code word
+// holds the biased value 1 in all sixteen fields).
+cudaError_t launch_zero_units(const uint8_t* tiled, int64_t units, uint8_t* flags, cudaStream_t stream);
 cudaError_t launch_unrepack(const uint8_t* tiled, int64_t N, int64_t K, uint8_t* packed,
                             uint16_t* scales, int32_t* err, cudaStream_t stream);
 
@@ -74,9 +77,10 @@ StreamPlan plan_stream(int64_t M, int64_t N, int64_t K, int sm_count);
 
 // x_f16: X holds fp16 rather than bf16 bits.
 // s8: the tiled weights carry int8 scales and per-row factors (INT8-scale layout).
-cudaError_t launch_stream(const uint16_t* X, bool x_f16, int64_t ldx, const uint8_t* tiled, bool s8, int64_t M,
-                          int64_t N, int64_t K, const OutputSplit& out, void* ws, const StreamPlan& plan,
-                          cudaStream_t stream);
+// zflags (optional): per unit, 1 = all its weights are zero; such units are skipped.
+cudaError_t launch_stream(const uint16_t* X, bool x_f16, int64_t ldx, const uint8_t* tiled, bool s8,
+                          const uint8_t* zflags, int64_t M, int64_t N, int64_t K, const OutputSplit& out, void* ws,
+                          const StreamPlan& plan, cudaStream_t stream);
 
 // Tensor-core GEMM plan for M > kStreamMaxM: items of 256 weight rows x NT
 // tokens x a range of groups along K, persistent CTAs.
@@ -95,9 +99,9 @@ struct GemmPlan {
 
 GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sm_count);
 
-cudaError_t launch_gemm(const uint16_t* X, bool x_f16, int64_t ldx, const uint8_t* tiled, bool s8, int64_t M,
-                        int64_t N, int64_t K, const OutputSplit& out, void* ws, const GemmPlan& plan,
-                        cudaStream_t stream);
+cudaError_t launch_gemm(const uint16_t* X, bool x_f16, int64_t ldx, const uint8_t* tiled, bool s8,
+                        const uint8_t* zflags, int64_t M, int64_t N, int64_t K, const OutputSplit& out, void* ws,
+                        const GemmPlan& plan, cudaStream_t stream);
 
 // int8-activation variant: quantised activations in the code words' field
 // order, one CTA per (row tile, K split).

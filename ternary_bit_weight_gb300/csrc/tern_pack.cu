@@ -332,6 +332,29 @@ cudaError_t launch_repack(const uint8_t* packed, const uint16_t* scales, int64_t
                : launch_flat(repack_kernel<false>, units * kTileRows, stream, src, K, units, tiled, err);
 }
 
+// One warp per unit: 1024 code words, 32 per lane, one vote.
+__global__ void __launch_bounds__(kThreads)
+zero_units_kernel(const uint4* __restrict__ codes, int64_t units, uint8_t* __restrict__ flags) {
+    const int lane = threadIdx.x & 31;
+    for (int64_t u = (blockIdx.x * (int64_t)kThreads + threadIdx.x) >> 5; u < units;
+         u += ((int64_t)gridDim.x * kThreads) >> 5) {
+        const uint4* p = codes + u * (kUnitCodeBytes / 16);
+        bool zero = true;
+#pragma unroll
+        for (int i = 0; i < kUnitCodeBytes / 16 / 32; ++i) {
+            const uint4 v = __ldg(p + i * 32 + lane);
+            zero = zero && v.x == 0x55555555u && v.y == 0x55555555u && v.z == 0x55555555u && v.w == 0x55555555u;
+        }
+        zero = __all_sync(0xffffffffu, zero);
+        if (lane == 0) flags[u] = zero ? 1 : 0;
+    }
+    __threadfence();
+}
+
+cudaError_t launch_zero_units(const uint8_t* tiled, int64_t units, uint8_t* flags, cudaStream_t stream) {
+    return launch_flat(zero_units_kernel, units * 32, stream, reinterpret_cast<const uint4*>(tiled), units, flags);
+}
+
 cudaError_t launch_repack_s8(const uint8_t* packed, const int8_t* q8, const float* f, int64_t N, int64_t K,
                              uint8_t* tiled, int32_t* err, cudaStream_t stream) {
     RepackSrc src = {};

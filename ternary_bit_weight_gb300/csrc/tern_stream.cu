@@ -128,6 +128,7 @@ struct StreamArgs {
     const float* row_factor;   // s8: per row, the factor of its int8 scales ([R * 128])
     int s8;
     int scale_unit;            // bytes of one unit's scales: 256, or 128 (s8)
+    const uint8_t* zflags;     // optional, per unit: 1 = every weight of the unit is 0 (skipped)
     const uint16_t* x;         // M == 1: the activation row
     int M;
     int G;                     // groups per row
@@ -291,9 +292,29 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
             const int64_t uf = u0 + (int64_t)f * kPS;
             const int32_t cnt = n - f * kPS < kPS ? n - f * kPS : kPS;
             if (elect_one()) {
-                mbar_arrive_expect_tx(bar, cnt * (kUnitCodeBytes + a.scale_unit + C::XUnit));
-                bulk_load(st + C::OffCodes, a.codes + uf * kUnitCodeBytes, cnt * kUnitCodeBytes, bar);
-                bulk_load(st + C::OffScales, a.scales + uf * a.scale_unit, cnt * a.scale_unit, bar);
+                if (a.zflags == nullptr) {
+                    mbar_arrive_expect_tx(bar, cnt * (kUnitCodeBytes + a.scale_unit + C::XUnit));
+                    bulk_load(st + C::OffCodes, a.codes + uf * kUnitCodeBytes, cnt * kUnitCodeBytes, bar);
+                    bulk_load(st + C::OffScales, a.scales + uf * a.scale_unit, cnt * a.scale_unit, bar);
+                } else {
+                    // zero units are not copied: one copy per run of non-zero units
+                    uint32_t live = 0;
+                    for (int32_t i = 0; i < cnt; ++i) live |= (a.zflags[uf + i] ? 0u : 1u) << i;
+                    mbar_arrive_expect_tx(bar, __popc(live) * (kUnitCodeBytes + a.scale_unit) + cnt * C::XUnit);
+                    for (int32_t i = 0; i < cnt;) {
+                        if (!((live >> i) & 1u)) {
+                            ++i;
+                            continue;
+                        }
+                        int32_t e = i;
+                        while (e < cnt && ((live >> e) & 1u)) ++e;
+                        bulk_load(st + C::OffCodes + i * kUnitCodeBytes, a.codes + (uf + i) * kUnitCodeBytes,
+                                  (e - i) * kUnitCodeBytes, bar);
+                        bulk_load(st + C::OffScales + i * a.scale_unit, a.scales + (uf + i) * a.scale_unit,
+                                  (e - i) * a.scale_unit, bar);
+                        i = e;
+                    }
+                }
             }
             __syncwarp();
         };
@@ -394,13 +415,16 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
             const uint32_t d_tm = tmem + kDCol0 + (2 * dp + q) * kNtok;
             const uint64_t b0 = ONE ? bdesc_x + 16u * (uint32_t)g
                                     : bdesc_ring + ((uint32_t)(s * C::StageBytes + us * C::XUnit) >> 4);
+            const bool zero = a.zflags != nullptr && a.zflags[u0 + j] != 0;
             if (elect_one()) {
+                if (!zero) {
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    // M == 1: +32 bytes per K-step; else +32 bytes within a
-                    // 64-wide box and +2048 bytes to the second box
-                    const uint32_t step = ONE ? 2 * kk : (kk >> 2) * (kNtok * 128 / 16) + 2 * (kk & 3);
-                    umma_bf16_tmem_a(d_tm, a_tm + 8 * kk, b0 + step, idesc, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < 8; ++kk) {
+                        // M == 1: +32 bytes per K-step; else +32 bytes within a
+                        // 64-wide box and +2048 bytes to the second box
+                        const uint32_t step = ONE ? 2 * kk : (kk >> 2) * (kNtok * 128 / 16) + 2 * (kk & 3);
+                        umma_bf16_tmem_a(d_tm, a_tm + 8 * kk, b0 + step, idesc, kk > 0 ? 1u : 0u);
+                    }
                 }
                 umma_commit(cb + kBarAEmpty + 8 * (kAQ * q + al));
                 umma_commit(cb + kBarDFull + 8 * dp);
@@ -451,9 +475,13 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
         for (int32_t j = q; j < n; j += 2) {
             const int us = j % kPS;
             if (us < 2 && !warp_wait(bar_full + 8 * s, full_ph, abort_flag)) break;   // first unit of the stage
+            const bool zero = a.zflags != nullptr && a.zflags[u0 + j] != 0;   // nothing to decode
             const uint8_t* cp = ring_ptr + s * C::StageBytes + codes_off + us * kUnitCodeBytes;
-            const uint4 c0 = lds_v4(cp);
-            const uint4 c1 = lds_v4(cp + 2048);
+            uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0;
+            if (!zero) {
+                c0 = lds_v4(cp);
+                c1 = lds_v4(cp + 2048);
+            }
             if (us >= kPS - 2 || j + 2 >= n) {   // this stream's last unit of the stage
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_empty + 8 * s);
@@ -466,7 +494,7 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
                 if (!warp_wait(bar_aempty + 8 * al, a_ph ^ 1u, abort_flag)) break;
                 tc_fence_after_sync();
             }
-            {
+            if (!zero) {
                 uint32_t p[64];
                 const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
@@ -547,9 +575,10 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
             for (int i = 0; i < 2; ++i) {
                 if (i == 1 && !two) break;
                 const float sc = i == 0 ? sc0 : sc1;
-#pragma unroll
-                for (int m = 0; m < NCOL; ++m) acc[m] = fmaf(sc, __uint_as_float(d[i * NCOL + m]), acc[m]);
                 const int32_t u = f + i;
+                if (a.zflags == nullptr || a.zflags[u0 + u] == 0)
+#pragma unroll
+                    for (int m = 0; m < NCOL; ++m) acc[m] = fmaf(sc, __uint_as_float(d[i * NCOL + m]), acc[m]);
                 if (pg == G - 1 || u == n - 1) {
                     const bool whole = (pb != first_tile || first_g == 0) && pg == G - 1;
                     flush_tile<NCOL>(a, v, pb, first_tile, whole, acc, r);
@@ -666,10 +695,11 @@ StreamPlan plan_stream(int64_t M, int64_t N, int64_t K, int sm_count) {
     return p;
 }
 
-cudaError_t launch_stream(const uint16_t* X, bool x_f16, int64_t ldx, const uint8_t* tiled, bool s8, int64_t M,
-                          int64_t N, int64_t K, const OutputSplit& out, void* ws, const StreamPlan& plan,
-                          cudaStream_t stream) {
+cudaError_t launch_stream(const uint16_t* X, bool x_f16, int64_t ldx, const uint8_t* tiled, bool s8,
+                          const uint8_t* zflags, int64_t M, int64_t N, int64_t K, const OutputSplit& out, void* ws,
+                          const StreamPlan& plan, cudaStream_t stream) {
     StreamArgs a = {};
+    a.zflags = zflags;
     a.codes = tiled;
     a.scales = tiled + plan.U * kUnitCodeBytes;
     a.s8 = s8 ? 1 : 0;

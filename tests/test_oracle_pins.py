@@ -541,3 +541,18 @@ def test_linear_s8_matches_dense_matmul():
     w = t.astype(np.float64) * np.repeat(q8.astype(np.float64), 128, axis=1) * f.astype(np.float64)[:, None]
     xd = (xb.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     assert np.allclose(y, xd @ w.T, rtol=1e-12, atol=1e-15)
+
+
+# ---------------------------------------------------------- zero units
+
+def test_zero_units_by_hand():
+    K = 256
+    t = np.zeros((130, K), dtype=np.int8)          # 2 row tiles x 2 groups, second tile ragged
+    t[5, 200] = -1                                  # unit (0, 1)
+    t[129, 3] = 1                                   # unit (1, 0)
+    packed, _ = oracle.pack(t)
+    assert oracle.zero_units(packed, K).tolist() == [1, 0, 0, 1]
+    # a reserved code 11 reads as 0, so it leaves a unit zero
+    packed[0, 0] = 0b11
+    assert oracle.zero_units(packed, K).tolist() == [1, 0, 0, 1]
+    assert oracle.zero_units(oracle.pack(np.ones((1, 128), dtype=np.int8))[0], 128).tolist() == [0]
