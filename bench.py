@@ -543,6 +543,110 @@ def leg_swiglu(wl, layers, dev, tb, torch, Ms, local):
     return out
 
 
+def leg_variants(wl, layers, dev, tb, torch, local):
+    """The layer's variants on the 27B-class shapes, one launch per layer back
+    to back (distinct weights): INT8 group scales (tern_linear_s8) and int8
+    activations (tern_quantize_x + tern_linear_i8) at M = 1 and 16 per
+    linear, and zero-block skipping (tern_linear_sparse) on gate+up weights
+    with half of the 128x128 units zero (structured sparsity) against the
+    same weights run dense."""
+    import synth
+    out = {"s8": {}, "i8": {}, "sparse_gate_up": {}}
+    for lin in wl.linears:
+        K, N = lin.K, lin.N
+        s8w, tiled = [], []
+        for layer in range(layers):
+            t, s = synth.weights(wl, layer, lin)
+            t_d = torch.from_numpy(t).to(dev)
+            packed = torch.empty((N, K // 4), dtype=torch.uint8, device=dev)
+            tb.tern_pack(t_d, N, K, packed)
+            del t_d
+            sc = torch.from_numpy(s.view(np.int16)).to(dev)
+            q8 = torch.empty((N, K // 128), dtype=torch.int8, device=dev)
+            f = torch.empty(N, dtype=torch.float32, device=dev)
+            tb.tern_quantize_scales(sc, N, K, q8, f)
+            w8 = torch.empty(tb.tern_tiled_s8_bytes(N, K), dtype=torch.uint8, device=dev)
+            tb.tern_repack_s8(packed, q8, f, N, K, w8)
+            s8w.append(w8)
+            w = torch.empty(tb.tern_tiled_bytes(N, K), dtype=torch.uint8, device=dev)
+            tb.tern_repack(packed, sc, N, K, w)
+            tiled.append(w)
+        for M in (1, 16):
+            xs = [torch.from_numpy(synth.activations(wl, l, lin, M).view(np.int16)).to(dev) for l in range(layers)]
+            Y = torch.empty((M, N), dtype=torch.float32, device=dev)
+            ws = torch.zeros(max(tb.tern_workspace_bytes(M, N, K), tb.tern_i8_workspace_bytes(M, N, K), 256),
+                             dtype=torch.uint8, device=dev)
+            xq = torch.empty(tb.tern_xq_bytes(M, K), dtype=torch.int8, device=dev)
+            a = torch.empty(M, dtype=torch.float32, device=dev)
+
+            def pass_s8():
+                for l in range(layers):
+                    tb.tern_linear_s8(xs[l], tb.TERN_X_BF16, K, s8w[l], M, K, [N], [Y], [N], tb.TERN_OUT_F32, ws)
+
+            def pass_i8():
+                for l in range(layers):
+                    tb.tern_quantize_x(xs[l], tb.TERN_X_BF16, K, M, K, xq, a)
+                    tb.tern_linear_i8(xq, a, tiled[l], M, N, K, Y, N, tb.TERN_OUT_F32, ws)
+            for name, fn, unit_bytes in (("s8", pass_s8, 4096 + 128), ("i8", pass_i8, 4096 + 256)):
+                fn()
+                ms, clocks = timed_region(torch, fn, 1, local, min_ms=60.0)
+                us = ms * 1e3 / layers
+                nbytes = ((N + 127) // 128) * (K // 128) * unit_bytes + M * K * 2 + 4 * M * N
+                out[name].setdefault(str(M), {})[lin.name] = {"us": us, "gbs": nbytes / (us * 1e-6) / 1e9,
+                                                              "clocks": clocks}
+            del xs, Y, ws, xq, a
+        del s8w, tiled
+        torch.cuda.empty_cache()
+    # zero-block skipping on gate+up with half of the units zero
+    lin = next(l for l in wl.linears if l.name == "gate_up")
+    K, N = lin.K, lin.N
+    rng = np.random.default_rng(0)
+    sp, flags = [], []
+    for layer in range(layers):
+        t, s = synth.weights(wl, layer, lin)
+        R, G = (N + 127) // 128, K // 128
+        keep = rng.random((R, G)) < 0.5
+        t = t.reshape(R, 128, G, 128)
+        t[~keep[:, None, :, None].repeat(128, 1).repeat(128, 3)] = 0
+        t = t.reshape(N, K)
+        t_d = torch.from_numpy(t).to(dev)
+        packed = torch.empty((N, K // 4), dtype=torch.uint8, device=dev)
+        tb.tern_pack(t_d, N, K, packed)
+        del t_d
+        w = torch.empty(tb.tern_tiled_bytes(N, K), dtype=torch.uint8, device=dev)
+        tb.tern_repack(packed, torch.from_numpy(s.view(np.int16)).to(dev), N, K, w)
+        fl = torch.empty(tb.tern_unit_count(N, K), dtype=torch.uint8, device=dev)
+        tb.tern_zero_units(w, N, K, fl)
+        sp.append(w)
+        flags.append(fl)
+    for M in (1, 1024):
+        xs = [torch.from_numpy(synth.activations(wl, l, lin, M).view(np.int16)).to(dev) for l in range(layers)]
+        Y = torch.empty((M, N), dtype=torch.float32, device=dev)
+        ws = torch.zeros(tb.tern_workspace_bytes(M, N, K), dtype=torch.uint8, device=dev)
+
+        def dense():
+            for l in range(layers):
+                tb.tern_linear_ex(xs[l], tb.TERN_X_BF16, K, sp[l], M, K, [N], [Y], [N], tb.TERN_OUT_F32, ws)
+
+        def sparse():
+            for l in range(layers):
+                tb.tern_linear_sparse(xs[l], tb.TERN_X_BF16, K, sp[l], flags[l], M, K, [N], [Y], [N],
+                                      tb.TERN_OUT_F32, ws)
+        row = {}
+        for name, fn in (("dense", dense), ("skipping", sparse)):
+            fn()
+            ms, clocks = timed_region(torch, fn, 1, local, min_ms=60.0)
+            row[name + "_us"] = ms * 1e3 / layers
+            row[name + "_clocks"] = clocks
+        row["speedup"] = row["dense_us"] / row["skipping_us"]
+        out["sparse_gate_up"][str(M)] = row
+        del xs, Y, ws
+    del sp, flags
+    torch.cuda.empty_cache()
+    out["sparse_gate_up"]["note"] = "half of the 128x128 weight units zero, chosen at random per layer"
+    return out
+
+
 def run_profile(args):
     """A few calls of one layer-0 linear (or its repack) for an ncu capture."""
     import torch
@@ -707,6 +811,7 @@ def main():
         for v in legs["prefill27b_bf16_out"].values():
             v["frac_of_bf16_peak"] = v["tflops"] / bf16_peak
         legs["swiglu27b"] = leg_swiglu(wl, min(layers, 8), dev, tb, torch, [1, 64, 1024], local)
+        legs["variants27b"] = leg_variants(wl, min(layers, 8), dev, tb, torch, local)
         del tiled
         torch.cuda.empty_cache()
         legs["embed06b"] = leg_workload("embed06b", [1, 32, 512], dev, tb, torch, local)

@@ -196,6 +196,13 @@ __device__ __forceinline__ void store_row(const RowOut& o, int m, float v) {
     store_elem(o.base, (int64_t)m * o.ld, o.otype, v);
 }
 
+// C final values v[0..C) of tokens m0 .. m0+C-1 of one output row, those
+// below the token bound `mend` stored; the whole warp calls together, and
+// the output form is decided once for the C stores instead of per element.
+template <int C>
+__device__ __forceinline__ void store_run(const OutputSplit& out, const RowOut& o, int m0, int mend, int64_t row,
+                                          const float (&v)[C], bool live);
+
 // Final value v of output (m, row), the row being lane (row mod 32) of the
 // calling warp; every lane of the warp calls with the same m.  `live`: the
 // row exists (row < N).  With the GLU layout the partner lane (lane ^ 16)
@@ -212,6 +219,34 @@ __device__ __forceinline__ void store_out(const OutputSplit& out, const RowOut& 
         }
     } else if (live) {
         store_row(o, m, v);
+    }
+}
+
+template <int C>
+__device__ __forceinline__ void store_run(const OutputSplit& out, const RowOut& o, int m0, int mend, int64_t row,
+                                          const float (&v)[C], bool live) {
+    if (out.glu) {
+#pragma unroll
+        for (int m = 0; m < C; ++m)
+            if (m0 + m < mend) store_out(out, o, m0 + m, row, v[m], live);
+        return;
+    }
+    if (!live) return;
+    if (o.otype == 0) {
+        float* p = reinterpret_cast<float*>(o.base) + (int64_t)m0 * o.ld;
+#pragma unroll
+        for (int m = 0; m < C; ++m)
+            if (m0 + m < mend) p[(int64_t)m * o.ld] = v[m];
+    } else if (o.otype == 1) {
+        __nv_bfloat16* p = reinterpret_cast<__nv_bfloat16*>(o.base) + (int64_t)m0 * o.ld;
+#pragma unroll
+        for (int m = 0; m < C; ++m)
+            if (m0 + m < mend) p[(int64_t)m * o.ld] = __float2bfloat16_rn(v[m]);
+    } else {
+        __half* p = reinterpret_cast<__half*>(o.base) + (int64_t)m0 * o.ld;
+#pragma unroll
+        for (int m = 0; m < C; ++m)
+            if (m0 + m < mend) p[(int64_t)m * o.ld] = __float2half_rn(v[m]);
     }
 }
 

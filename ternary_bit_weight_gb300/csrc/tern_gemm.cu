@@ -143,15 +143,15 @@ __device__ __forceinline__ void load_inv(const float* p, float (&inv)[C]) {
     }
 }
 
-__device__ __forceinline__ bool unit_zero(const GemmArgs& a, int64_t tile, int g) {
-    return a.zflags != nullptr && a.zflags[tile * a.G + g] != 0;
+__device__ __forceinline__ bool unit_zero(const uint8_t* zflags, int G, int64_t tile, int g) {
+    return zflags != nullptr && zflags[tile * G + g] != 0;
 }
 
 // Whether row tile `tile` has a non-zero unit among groups [g0, g1).
-__device__ __forceinline__ bool tile_has_data(const GemmArgs& a, int64_t tile, int g0, int g1) {
-    if (a.zflags == nullptr) return true;
+__device__ __forceinline__ bool tile_has_data(const uint8_t* zflags, int G, int64_t tile, int g0, int g1) {
+    if (zflags == nullptr) return true;
     for (int g = g0; g < g1; ++g)
-        if (a.zflags[tile * a.G + g] == 0) return true;
+        if (zflags[tile * G + g] == 0) return true;
     return false;
 }
 
@@ -173,8 +173,14 @@ __device__ __forceinline__ void group_range(const GemmArgs& a, int ks, int& g0, 
     g1 = static_cast<int>((int64_t)a.G * (ks + 1) / a.KS);
 }
 
+// EXT: the weights may carry int8 scales (a.s8) or zero-unit flags
+// (a.zflags); the plain instantiation has neither check on its hot paths.
+template <bool EXT>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
+    const bool s8 = EXT && a.s8 != 0;
+    const uint8_t* const zflags = EXT ? a.zflags : nullptr;
+    const int scale_unit = EXT ? a.scale_unit : kUnitScaleBytes;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);
@@ -238,7 +244,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
                 const int cnt = g1 - g < kWG ? g1 - g : kWG;
                 const uint32_t st = wring + ws * kWStage;
                 if (elect_one()) {
-                    mbar_arrive_expect_tx(cb + kBarWFull + 8 * ws, (two ? 2 : 1) * cnt * (kUnitCodeBytes + a.scale_unit));
+                    mbar_arrive_expect_tx(cb + kBarWFull + 8 * ws, (two ? 2 : 1) * cnt * (kUnitCodeBytes + scale_unit));
 #pragma unroll
                     for (int rt = 0; rt < 2; ++rt) {
                         if (rt == 1 && !two) break;
@@ -246,7 +252,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
                         bulk_load(st + rt * kWG * kUnitCodeBytes, a.codes + u * kUnitCodeBytes, cnt * kUnitCodeBytes,
                                   cb + kBarWFull + 8 * ws);
                         bulk_load(st + 2 * kWG * kUnitCodeBytes + rt * kWG * kUnitScaleBytes,
-                                  a.scales + u * a.scale_unit, cnt * a.scale_unit, cb + kBarWFull + 8 * ws);
+                                  a.scales + u * scale_unit, cnt * scale_unit, cb + kBarWFull + 8 * ws);
                     }
                 }
                 __syncwarp();
@@ -316,7 +322,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
             bool started0 = false, started1 = false;   // accumulators written this item
             for (int g = g0; g < g1; ++g) {
                 const int xg = (g - g0) % kXG;
-                const bool z0 = unit_zero(a, 2 * it.bp, g), z1 = !two || unit_zero(a, 2 * it.bp + 1, g);
+                const bool z0 = unit_zero(zflags, a.G, 2 * it.bp, g), z1 = !two || unit_zero(zflags, a.G, 2 * it.bp + 1, g);
                 uint32_t bar = 0, par = 0;
                 bool act = false;
                 if (lane == 1) {
@@ -393,16 +399,16 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
             for (int g = g0; g < g1; ++g) {
                 const int wg = (g - g0) % kWG;
                 if (wg == 0 && !(ok = warp_wait(cb + kBarWFull + 8 * ws, w_ph, abort_flag))) break;
-                const bool mine = tile_exists && !unit_zero(a, 2 * it.bp + rt, g);   // a zero unit needs no A
+                const bool mine = tile_exists && !unit_zero(zflags, a.G, 2 * it.bp + rt, g);   // a zero unit needs no A
                 uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0;
                 uint32_t s2 = 0;
                 if (mine) {
                     const uint8_t* st = wring_ptr + ws * kWStage;
                     c0 = lds_v4(st + rt * kWG * kUnitCodeBytes + wg * kUnitCodeBytes + 16 * r);
                     c1 = lds_v4(st + rt * kWG * kUnitCodeBytes + wg * kUnitCodeBytes + 2048 + 16 * r);
-                    const uint8_t* sp = st + 2 * kWG * kUnitCodeBytes + rt * kWG * kUnitScaleBytes + wg * a.scale_unit;
+                    const uint8_t* sp = st + 2 * kWG * kUnitCodeBytes + rt * kWG * kUnitScaleBytes + wg * scale_unit;
                     // int8 scale q: t * q is exact in fp16 (|q| <= 127); the row's factor comes at the end
-                    const uint32_t sb = a.s8 ? __half_as_ushort(__int2half_rn(*reinterpret_cast<const int8_t*>(sp + r)))
+                    const uint32_t sb = s8 ? __half_as_ushort(__int2half_rn(*reinterpret_cast<const int8_t*>(sp + r)))
                                              : *reinterpret_cast<const uint16_t*>(sp + 2 * r);
                     s2 = sb | (sb << 16);
                 }
@@ -465,8 +471,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
                     const int64_t row = (int64_t)(2 * it.bp + rt) * kTileRows + r;
                     const bool live = row < a.N;
                     const RowOut o = row_out(a.out, live ? row : 0);
-                    const float f = a.s8 ? a.row_factor[row] : 1.0f;
-                    const bool data = tile_has_data(a, 2 * it.bp + rt, 0, a.G);   // else the accumulators are stale
+                    const float f = s8 ? a.row_factor[row] : 1.0f;
+                    const bool data = tile_has_data(zflags, a.G, 2 * it.bp + rt, 0, a.G);   // else the accumulators are stale
                     for (int c = 0; c < NT; c += 32) {
                         float inv[32];
                         load_inv(a.inv_scale + m0 + c, inv);
@@ -480,9 +486,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
                         if (!data)
 #pragma unroll
                             for (int m = 0; m < 32; ++m) d[m] = 0u;
+                        float v[32];
 #pragma unroll
-                        for (int m = 0; m < 32; ++m)
-                            if (c + m < mvalid) store_out(a.out, o, m0 + c + m, row, __uint_as_float(d[m]) * inv[m], live);
+                        for (int m = 0; m < 32; ++m) v[m] = __uint_as_float(d[m]) * inv[m];
+                        store_run(a.out, o, m0 + c, m0 + mvalid, row, v, live);
                     }
                 }
                 tc_fence_before_sync();
@@ -496,7 +503,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
                 group_range(a, it.ks, g0, g1);
                 for (int rt = 0; rt < 2; ++rt) {
                     if (rt == 1 && !two) break;
-                    const bool data = tile_has_data(a, 2 * it.bp + rt, g0, g1);
+                    const bool data = tile_has_data(zflags, a.G, 2 * it.bp + rt, g0, g1);
                     for (int c = 0; c < NT; c += 32) {
                         uint32_t d[32];
                         if (c + 32 <= NT)
@@ -532,7 +539,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
                         const int64_t row = (int64_t)(2 * it.bp + rt) * kTileRows + r;
                         const bool live = row < a.N;
                         const RowOut o = row_out(a.out, live ? row : 0);
-                        const float f = a.s8 ? a.row_factor[row] : 1.0f;
+                        const float f = s8 ? a.row_factor[row] : 1.0f;
                         for (int c = 0; c < mvalid; c += 16) {
                             float v[16];
 #pragma unroll
@@ -547,8 +554,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
 #pragma unroll
                             for (int m = 0; m < 16; ++m) inv[m] *= f;
 #pragma unroll
-                            for (int m = 0; m < 16; ++m)
-                                if (c + m < mvalid) store_out(a.out, o, m0 + c + m, row, v[m] * inv[m], live);
+                            for (int m = 0; m < 16; ++m) v[m] *= inv[m];
+                            store_run(a.out, o, m0 + c, m0 + mvalid, row, v, live);
                         }
                     }
                     if (r == 0) a.counters[tile] = 0;   // leave the workspace zeroed
@@ -646,11 +653,12 @@ EncodeTiledFn encode_tiled_fn() {
     return fn;
 }
 
+template <bool EXT>
 cudaError_t set_smem_limit() {
     static cudaError_t status = cudaErrorUnknown;
     static std::once_flag once;
     std::call_once(once, [] {
-        status = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        status = cudaFuncSetAttribute(gemm_kernel<EXT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     });
     return status;
 }
@@ -720,7 +728,8 @@ cudaError_t launch_gemm(const uint16_t* X, bool x_f16, int64_t ldx, const uint8_
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
         CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-    cudaError_t e = set_smem_limit();
+    const bool ext = s8 || zflags != nullptr;
+    cudaError_t e = ext ? set_smem_limit<true>() : set_smem_limit<false>();
     if (e != cudaSuccess) return e;
     GemmArgs a = {};
     a.codes = tiled;
@@ -754,7 +763,7 @@ cudaError_t launch_gemm(const uint16_t* X, bool x_f16, int64_t ldx, const uint8_
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemm_kernel, map, a);
+    return ext ? cudaLaunchKernelEx(&cfg, gemm_kernel<true>, map, a) : cudaLaunchKernelEx(&cfg, gemm_kernel<false>, map, a);
 }
 
 }  // namespace tern

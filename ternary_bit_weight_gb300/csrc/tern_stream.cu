@@ -156,11 +156,11 @@ __device__ __forceinline__ int64_t owner_worker(int64_t u, int64_t U, int64_t V)
 // that row quarter sums all partials in CTA order.
 template <int NCOL>
 __device__ __forceinline__ void flush_tile(const StreamArgs& a, int64_t v, int64_t b, int64_t first_tile,
-                                           bool whole, float (&acc)[NCOL], int r) {
+                                           bool whole, float (&acc)[NCOL], int r, bool s8) {
     const int lane = r & 31, quad = r >> 5;
     const int64_t row = b * kTileRows + r;
     const int mvalid = a.M < NCOL ? a.M : NCOL;
-    if (a.s8) {
+    if (s8) {
         // int8 scales: the group sums were weighted by q; the row's factor once
         const float f = a.row_factor[b * kTileRows + r];
 #pragma unroll
@@ -227,10 +227,15 @@ __device__ __forceinline__ bool vote_wait(uint32_t bar, uint32_t parity, bool ac
     return __all_sync(0xffffffffu, got);
 }
 
-template <bool ONE, bool XF16>
+// EXT: the weights may carry int8 scales (a.s8) or zero-unit flags
+// (a.zflags); the plain instantiation has neither check on its hot paths.
+template <bool ONE, bool XF16, bool EXT>
 __global__ void __launch_bounds__(kThreads, 1)
 stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
     using C = SCfg<ONE>;
+    const bool s8 = EXT && a.s8 != 0;
+    const uint8_t* const zflags = EXT ? a.zflags : nullptr;
+    const int scale_unit = EXT ? a.scale_unit : kUnitScaleBytes;
     constexpr int NCOL = C::NCOL;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base (swizzle atoms)
@@ -292,15 +297,15 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
             const int64_t uf = u0 + (int64_t)f * kPS;
             const int32_t cnt = n - f * kPS < kPS ? n - f * kPS : kPS;
             if (elect_one()) {
-                if (a.zflags == nullptr) {
-                    mbar_arrive_expect_tx(bar, cnt * (kUnitCodeBytes + a.scale_unit + C::XUnit));
+                if (zflags == nullptr) {
+                    mbar_arrive_expect_tx(bar, cnt * (kUnitCodeBytes + scale_unit + C::XUnit));
                     bulk_load(st + C::OffCodes, a.codes + uf * kUnitCodeBytes, cnt * kUnitCodeBytes, bar);
-                    bulk_load(st + C::OffScales, a.scales + uf * a.scale_unit, cnt * a.scale_unit, bar);
+                    bulk_load(st + C::OffScales, a.scales + uf * scale_unit, cnt * scale_unit, bar);
                 } else {
                     // zero units are not copied: one copy per run of non-zero units
                     uint32_t live = 0;
-                    for (int32_t i = 0; i < cnt; ++i) live |= (a.zflags[uf + i] ? 0u : 1u) << i;
-                    mbar_arrive_expect_tx(bar, __popc(live) * (kUnitCodeBytes + a.scale_unit) + cnt * C::XUnit);
+                    for (int32_t i = 0; i < cnt; ++i) live |= (zflags[uf + i] ? 0u : 1u) << i;
+                    mbar_arrive_expect_tx(bar, __popc(live) * (kUnitCodeBytes + scale_unit) + cnt * C::XUnit);
                     for (int32_t i = 0; i < cnt;) {
                         if (!((live >> i) & 1u)) {
                             ++i;
@@ -310,8 +315,8 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
                         while (e < cnt && ((live >> e) & 1u)) ++e;
                         bulk_load(st + C::OffCodes + i * kUnitCodeBytes, a.codes + (uf + i) * kUnitCodeBytes,
                                   (e - i) * kUnitCodeBytes, bar);
-                        bulk_load(st + C::OffScales + i * a.scale_unit, a.scales + (uf + i) * a.scale_unit,
-                                  (e - i) * a.scale_unit, bar);
+                        bulk_load(st + C::OffScales + i * scale_unit, a.scales + (uf + i) * scale_unit,
+                                  (e - i) * scale_unit, bar);
                         i = e;
                     }
                 }
@@ -415,7 +420,7 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
             const uint32_t d_tm = tmem + kDCol0 + (2 * dp + q) * kNtok;
             const uint64_t b0 = ONE ? bdesc_x + 16u * (uint32_t)g
                                     : bdesc_ring + ((uint32_t)(s * C::StageBytes + us * C::XUnit) >> 4);
-            const bool zero = a.zflags != nullptr && a.zflags[u0 + j] != 0;
+            const bool zero = zflags != nullptr && zflags[u0 + j] != 0;
             if (elect_one()) {
                 if (!zero) {
 #pragma unroll
@@ -475,7 +480,7 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
         for (int32_t j = q; j < n; j += 2) {
             const int us = j % kPS;
             if (us < 2 && !warp_wait(bar_full + 8 * s, full_ph, abort_flag)) break;   // first unit of the stage
-            const bool zero = a.zflags != nullptr && a.zflags[u0 + j] != 0;   // nothing to decode
+            const bool zero = zflags != nullptr && zflags[u0 + j] != 0;   // nothing to decode
             const uint8_t* cp = ring_ptr + s * C::StageBytes + codes_off + us * kUnitCodeBytes;
             uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0;
             if (!zero) {
@@ -519,7 +524,7 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
         // ------------------------------------------------------- promotion
         const int r = threadIdx.x & 127;   // weight row in the tile = tensor-memory lane
         const uint32_t tm = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + kDCol0;
-        const int scale_off = C::OffScales + (a.s8 ? 1 : 2) * r;   // + unit in stage * scale_unit
+        const int scale_off = C::OffScales + (s8 ? 1 : 2) * r;   // + unit in stage * scale_unit
         const int64_t first_tile = u0 / G;
         const int32_t first_g = static_cast<int32_t>(u0 - first_tile * G);
         int64_t pb = first_tile;
@@ -545,14 +550,14 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
                 tmem_ld_32x32b_x16(tm + 2 * dp * kNtok, *reinterpret_cast<uint32_t(*)[16]>(d));
                 tmem_ld_32x32b_x16(tm + (2 * dp + 1) * kNtok, *reinterpret_cast<uint32_t(*)[16]>(d + NCOL));
             }
-            const uint8_t* sp = ring_ptr + s * C::StageBytes + scale_off + us * a.scale_unit;
+            const uint8_t* sp = ring_ptr + s * C::StageBytes + scale_off + us * scale_unit;
             float sc0, sc1;
-            if (a.s8) {
+            if (s8) {
                 sc0 = static_cast<float>(*reinterpret_cast<const int8_t*>(sp));
-                sc1 = two ? static_cast<float>(*reinterpret_cast<const int8_t*>(sp + a.scale_unit)) : 0.f;
+                sc1 = two ? static_cast<float>(*reinterpret_cast<const int8_t*>(sp + scale_unit)) : 0.f;
             } else {
                 sc0 = fp16_bits_to_float(*reinterpret_cast<const uint16_t*>(sp));
-                sc1 = two ? fp16_bits_to_float(*reinterpret_cast<const uint16_t*>(sp + a.scale_unit)) : 0.f;
+                sc1 = two ? fp16_bits_to_float(*reinterpret_cast<const uint16_t*>(sp + scale_unit)) : 0.f;
             }
             tmem_ld_wait();
             tc_fence_before_sync();
@@ -576,12 +581,12 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
                 if (i == 1 && !two) break;
                 const float sc = i == 0 ? sc0 : sc1;
                 const int32_t u = f + i;
-                if (a.zflags == nullptr || a.zflags[u0 + u] == 0)
+                if (zflags == nullptr || zflags[u0 + u] == 0)
 #pragma unroll
                     for (int m = 0; m < NCOL; ++m) acc[m] = fmaf(sc, __uint_as_float(d[i * NCOL + m]), acc[m]);
                 if (pg == G - 1 || u == n - 1) {
                     const bool whole = (pb != first_tile || first_g == 0) && pg == G - 1;
-                    flush_tile<NCOL>(a, v, pb, first_tile, whole, acc, r);
+                    flush_tile<NCOL>(a, v, pb, first_tile, whole, acc, r, s8);
 #pragma unroll
                     for (int m = 0; m < NCOL; ++m) acc[m] = 0.f;
                 }
@@ -624,18 +629,18 @@ EncodeTiledFn encode_tiled_fn() {
     return fn;
 }
 
-template <bool ONE, bool XF16>
+template <bool ONE, bool XF16, bool EXT>
 cudaError_t set_smem_limit() {
     static cudaError_t status = cudaErrorUnknown;
     static std::once_flag once;
     std::call_once(once, [] {
-        status = cudaFuncSetAttribute(stream_kernel<ONE, XF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        status = cudaFuncSetAttribute(stream_kernel<ONE, XF16, EXT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       kSmemLimit);
     });
     return status;
 }
 
-template <bool ONE, bool XF16>
+template <bool ONE, bool XF16, bool EXT>
 cudaError_t launch_one(const uint16_t* X, int64_t ldx, const StreamArgs& a, const StreamPlan& plan,
                        cudaStream_t stream) {
     CUtensorMap map;
@@ -653,7 +658,7 @@ cudaError_t launch_one(const uint16_t* X, int64_t ldx, const StreamArgs& a, cons
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    cudaError_t e = set_smem_limit<ONE, XF16>();
+    cudaError_t e = set_smem_limit<ONE, XF16, EXT>();
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(plan.grid));
@@ -665,7 +670,7 @@ cudaError_t launch_one(const uint16_t* X, int64_t ldx, const StreamArgs& a, cons
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, stream_kernel<ONE, XF16>, map, a);
+    return cudaLaunchKernelEx(&cfg, stream_kernel<ONE, XF16, EXT>, map, a);
 }
 
 }  // namespace
@@ -720,11 +725,19 @@ cudaError_t launch_stream(const uint16_t* X, bool x_f16, int64_t ldx, const uint
     a.err = reinterpret_cast<int*>(w);
     a.counters = reinterpret_cast<int*>(w + kWorkspaceErrBytes);
     a.slots = reinterpret_cast<float*>(w + kWorkspaceErrBytes + static_cast<size_t>(round_up(plan.R * 4 * 4, 256)));
+    const bool ext = s8 || zflags != nullptr;
+    if (ext) {
+        if (x_f16)
+            return plan.one ? launch_one<true, true, true>(X, ldx, a, plan, stream)
+                            : launch_one<false, true, true>(X, ldx, a, plan, stream);
+        return plan.one ? launch_one<true, false, true>(X, ldx, a, plan, stream)
+                        : launch_one<false, false, true>(X, ldx, a, plan, stream);
+    }
     if (x_f16)
-        return plan.one ? launch_one<true, true>(X, ldx, a, plan, stream)
-                        : launch_one<false, true>(X, ldx, a, plan, stream);
-    return plan.one ? launch_one<true, false>(X, ldx, a, plan, stream)
-                    : launch_one<false, false>(X, ldx, a, plan, stream);
+        return plan.one ? launch_one<true, true, false>(X, ldx, a, plan, stream)
+                        : launch_one<false, true, false>(X, ldx, a, plan, stream);
+    return plan.one ? launch_one<true, false, false>(X, ldx, a, plan, stream)
+                    : launch_one<false, false, false>(X, ldx, a, plan, stream);
 }
 
 }  // namespace tern
