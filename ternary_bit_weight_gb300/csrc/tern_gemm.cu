@@ -43,12 +43,18 @@
 namespace tern {
 namespace {
 
+// The MMA warp and the producers come first: a scheduler choosing among
+// ready warps favours the older ones, and the decode warps are always
+// ready with long runs of integer and FMA work.  Warp w reaches
+// tensor-memory lanes 32 (w mod 4) .. +31, so the decode and epilogue
+// warpgroups start at multiples of 4.
+constexpr int kMmaWarp = 0;
+constexpr int kProducerWarp = 1;                // weights
+constexpr int kXWarp0 = 2;                      // 2 warps: activation stages, alternately
+constexpr int kDecWarp0 = 4;
 constexpr int kDecWarps = 8;                    // warpgroup r decodes row tile r of the pair
-constexpr int kEpiWarp0 = kDecWarps;            // 4 warps
-constexpr int kProducerWarp = kEpiWarp0 + 4;    // weights
-constexpr int kXWarp0 = kProducerWarp + 1;      // 2 warps: activation stages, alternately
-constexpr int kMmaWarp = kXWarp0 + 2;
-constexpr int kThreads = (kMmaWarp + 1) * 32;
+constexpr int kEpiWarp0 = kDecWarp0 + kDecWarps;   // 4 warps
+constexpr int kThreads = (kEpiWarp0 + 4) * 32;
 constexpr int kMaxNT = 128;                     // tokens per tile (UMMA N)
 constexpr int kTmemCols = 512;
 constexpr int kACols = 64;                      // one unit of fp16 A (128 per row)
@@ -377,11 +383,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
         __syncwarp();
         volatile int no_abort = 0;
         (void)mbar_wait(cb + kBarDrain, 0, &no_abort);
-    } else if (warp < kDecWarps) {
+    } else if (warp >= kDecWarp0 && warp < kDecWarp0 + kDecWarps) {
         // ------------------------------------------------------------ decode
         // both warpgroups keep the A ring's phases even when an item has no
         // second row tile (they then arrive without decoding)
-        const int rt = warp >> 2;                       // row tile of the pair
+        const int rt = (warp - kDecWarp0) >> 2;         // row tile of the pair
         const int r = threadIdx.x & 127;                // weight row in the tile = tensor-memory lane
         const uint32_t tm = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + rt * kAU * kACols;
         const uint32_t bar_afull = cb + kBarAFull;
@@ -447,7 +453,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
                 }
             }
         }
-    } else if (warp < kEpiWarp0 + 4) {
+    } else if (warp >= kEpiWarp0) {
         // ---------------------------------------------------------- epilogue
         const int r = threadIdx.x & 127;
         const uint32_t tm = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + kDCol0;
