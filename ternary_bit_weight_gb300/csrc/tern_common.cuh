@@ -232,21 +232,22 @@ __device__ __forceinline__ void store_run(const OutputSplit& out, const RowOut& 
         return;
     }
     if (!live) return;
+    // streaming stores (evict first): the outputs are not read again here,
+    // and L2 is better spent on weights and activation tiles
     if (o.otype == 0) {
         float* p = reinterpret_cast<float*>(o.base) + (int64_t)m0 * o.ld;
 #pragma unroll
         for (int m = 0; m < C; ++m)
-            if (m0 + m < mend) p[(int64_t)m * o.ld] = v[m];
-    } else if (o.otype == 1) {
-        __nv_bfloat16* p = reinterpret_cast<__nv_bfloat16*>(o.base) + (int64_t)m0 * o.ld;
-#pragma unroll
-        for (int m = 0; m < C; ++m)
-            if (m0 + m < mend) p[(int64_t)m * o.ld] = __float2bfloat16_rn(v[m]);
+            if (m0 + m < mend) __stcs(p + (int64_t)m * o.ld, v[m]);
     } else {
-        __half* p = reinterpret_cast<__half*>(o.base) + (int64_t)m0 * o.ld;
+        unsigned short* p = reinterpret_cast<unsigned short*>(o.base) + (int64_t)m0 * o.ld;
 #pragma unroll
         for (int m = 0; m < C; ++m)
-            if (m0 + m < mend) p[(int64_t)m * o.ld] = __float2half_rn(v[m]);
+            if (m0 + m < mend) {
+                const unsigned short b = o.otype == 1 ? __bfloat16_as_ushort(__float2bfloat16_rn(v[m]))
+                                                      : __half_as_ushort(__float2half_rn(v[m]));
+                asm volatile("st.global.cs.b16 [%0], %1;" ::"l"(p + (int64_t)m * o.ld), "h"(b) : "memory");
+            }
     }
 }
 
