@@ -68,7 +68,9 @@ constexpr int kXS = 4;                          // activation stages; producer w
 constexpr int kXStageMax = kXG * 2 * kMaxNT * 128;          // 2 chunks of 64 per group
 constexpr int kWStage = 2 * kWG * kUnitBytes;              // both row tiles
 constexpr int kCtrlBytes = 1024;
-constexpr int kSmemBytes = 1024 + kXS * kXStageMax + kWS * kWStage + kCtrlBytes;
+constexpr int kYTok = 16;                       // tokens per output staging buffer
+constexpr int kYStage = kYTok * kTileRows * 4;  // one buffer: 16 tokens x 128 rows, up to 4 bytes each
+constexpr int kSmemBytes = 1024 + kXS * kXStageMax + kWS * kWStage + 2 * kYStage + kCtrlBytes;
 static_assert(kSmemBytes <= 232448, "shared-memory budget");
 static_assert(kXS % 2 == 0, "each activation stage has one producer warp");
 
@@ -107,6 +109,13 @@ struct GemmArgs {
     int* err;
     int* counters;             // [RP * T]
     float* partial;            // [RP * T][KS][2][NT][128]
+    int tma_store;             // outputs written through ymaps (see launch_gemm)
+};
+
+// Tensor maps of the outputs (inner dimension: the output's rows n, outer:
+// tokens m; box 128 x kYTok) for stores by TMA.
+struct YMaps {
+    CUtensorMap map[kMaxOutputs];
 };
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
@@ -183,7 +192,7 @@ __device__ __forceinline__ void group_range(const GemmArgs& a, int ks, int& g0, 
 // (a.zflags); the plain instantiation has neither check on its hot paths.
 template <bool EXT>
 __global__ void __launch_bounds__(kThreads, 1)
-gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
+gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ YMaps ymaps, const GemmArgs a) {
     const bool s8 = EXT && a.s8 != 0;
     const uint8_t* const zflags = EXT ? a.zflags : nullptr;
     const int scale_unit = EXT ? a.scale_unit : kUnitScaleBytes;
@@ -196,7 +205,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
     const uint32_t xring = sbase;
     const uint32_t wring = sbase + kXS * kXStageMax;
     uint8_t* wring_ptr = smem + kXS * kXStageMax;
-    uint8_t* ctrl = smem + kXS * kXStageMax + kWS * kWStage;
+    uint8_t* ystage = smem + kXS * kXStageMax + kWS * kWStage;   // 2 output staging buffers
+    uint8_t* ctrl = ystage + 2 * kYStage;
     const uint32_t cb = smem_u32(ctrl);
     uint32_t* tmem_base_ptr = reinterpret_cast<uint32_t*>(ctrl + kTmemPtr);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(ctrl + kAbort);
@@ -459,6 +469,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
         const uint32_t tm = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + kDCol0;
         grid_dependency_wait();   // outputs and workspace belong to earlier kernels until now
         uint32_t d_ph = 0;
+        uint32_t ybuf = 0;        // output staging buffers used so far
         for (int64_t i = blockIdx.x; i < a.items; i += gridDim.x) {
             const Item it = item_of(a, i);
             // the four warps decide together (they meet at barrier 1 below)
@@ -470,7 +481,53 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
             const int mvalid = a.M - m0 < NT ? a.M - m0 : NT;
             const bool two = 2 * it.bp + 1 < a.R;
             const int64_t tile = (int64_t)it.n * a.RP + it.bp;
-            if (a.KS == 1) {
+            if (a.KS == 1 && a.tma_store) {
+                // Through shared memory and TMA: the stores of the plain load
+                // and store path hold back the whole kernel.  16 tokens at a
+                // time into one of two staging buffers ([token][row]), one TMA
+                // store per buffer by thread 0 of the warpgroup.
+                const int nchunk = (mvalid + kYTok - 1) / kYTok;
+                const int ebytes = a.out.bf16 ? 2 : 4;
+                for (int rt = 0; rt < 2; ++rt) {
+                    if (rt == 1 && !two) break;
+                    const int64_t row0 = (int64_t)(2 * it.bp + rt) * kTileRows;
+                    const int j = output_of(a.out, row0);
+                    const int32_t n0 = static_cast<int32_t>(row0 - a.out.offset[j]);
+                    const float f = s8 ? a.row_factor[row0 + r] : 1.0f;
+                    const bool data = tile_has_data(zflags, a.G, 2 * it.bp + rt, 0, a.G);
+                    for (int q = 0; q < nchunk; ++q) {
+                        const int c = q * kYTok;
+                        uint32_t d[16];
+                        tmem_ld16_sync(tm + rt * NT + c, d);
+                        float inv[16];
+                        load_inv(a.inv_scale + m0 + c, inv);
+                        // the buffer written two chunks ago has been read by its store
+                        if (r == 0) bulk_wait_group_read<1>();
+                        asm volatile("bar.sync 2, 128;" ::: "memory");
+                        uint8_t* buf = ystage + (ybuf & 1) * kYStage;
+#pragma unroll
+                        for (int m = 0; m < 16; ++m) {
+                            const float v = data ? __uint_as_float(d[m]) * (inv[m] * f) : 0.f;
+                            if (ebytes == 4)
+                                reinterpret_cast<float*>(buf)[m * kTileRows + r] = v;
+                            else if (a.out.bf16 == 1)
+                                reinterpret_cast<__nv_bfloat16*>(buf)[m * kTileRows + r] = __float2bfloat16_rn(v);
+                            else
+                                reinterpret_cast<__half*>(buf)[m * kTileRows + r] = __float2half_rn(v);
+                        }
+                        fence_proxy_async_smem();
+                        asm volatile("bar.sync 2, 128;" ::: "memory");
+                        if (r == 0) {
+                            tma_store_2d(&ymaps.map[j], n0, m0 + c, smem_u32(buf));
+                            bulk_commit_group();
+                        }
+                        ++ybuf;
+                    }
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(cb + kBarDEmpty);
+            } else if (a.KS == 1) {
                 // final values straight from tensor memory, 32 tokens per load
                 for (int rt = 0; rt < 2; ++rt) {
                     if (rt == 1 && !two) break;
@@ -571,6 +628,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const GemmArgs a) {
     }
 
     // ------------------------------------------------------------ teardown
+    if (threadIdx.x == kEpiWarp0 * 32) bulk_wait_group_all();   // output stores complete
     tc_fence_before_sync();
     __syncthreads();
     if (*abort_flag && threadIdx.x == 0) atomicOr(a.err, 1);
@@ -759,6 +817,32 @@ cudaError_t launch_gemm(const uint16_t* X, bool x_f16, int64_t ldx, const uint8_
     a.err = reinterpret_cast<int*>(w);
     a.counters = reinterpret_cast<int*>(w + plan.off_counters);
     a.partial = reinterpret_cast<float*>(w + plan.off_partial);
+    // outputs by TMA when every row tile falls in one output and the
+    // outputs meet TMA's alignment (else the plain stores)
+    YMaps ymaps;
+    memset(&ymaps, 0, sizeof(ymaps));
+    {
+        const int eb = out.bf16 ? 2 : 4;
+        bool ok = plan.KS == 1 && !out.glu;
+        for (int j = 0; j < out.n_out && ok; ++j) {
+            const int64_t nj = out.offset[j + 1] - out.offset[j];
+            if (nj == 0) continue;
+            ok = out.offset[j] % kTileRows == 0 && (reinterpret_cast<uintptr_t>(out.y[j]) & 15) == 0 &&
+                 (out.ldy[j] * eb) % 16 == 0;
+            if (!ok) break;
+            const cuuint64_t ydims[2] = {static_cast<cuuint64_t>(nj), static_cast<cuuint64_t>(M)};
+            const cuuint64_t ystrides[1] = {static_cast<cuuint64_t>(out.ldy[j]) * eb};
+            const cuuint32_t ybox[2] = {static_cast<cuuint32_t>(kTileRows), static_cast<cuuint32_t>(kYTok)};
+            const cuuint32_t yestr[2] = {1, 1};
+            const CUtensorMapDataType dt = out.bf16 == 1   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                           : out.bf16 == 2 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                           : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+            ok = enc(&ymaps.map[j], dt, 2, out.y[j], ydims, ystrides, ybox, yestr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+        }
+        a.tma_store = ok ? 1 : 0;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(plan.grid));
     cfg.blockDim = dim3(kThreads);
@@ -769,7 +853,8 @@ cudaError_t launch_gemm(const uint16_t* X, bool x_f16, int64_t ldx, const uint8_
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return ext ? cudaLaunchKernelEx(&cfg, gemm_kernel<true>, map, a) : cudaLaunchKernelEx(&cfg, gemm_kernel<false>, map, a);
+    return ext ? cudaLaunchKernelEx(&cfg, gemm_kernel<true>, map, ymaps, a)
+               : cudaLaunchKernelEx(&cfg, gemm_kernel<false>, map, ymaps, a);
 }
 
 }  // namespace tern

@@ -243,3 +243,29 @@ def test_workspace_error_word_and_reset():
     tb.tern_workspace_reset(ws)
     torch.cuda.synchronize()
     assert int(ws.count_nonzero()) == 0
+
+
+@pytest.mark.parametrize("M", [17, 200, 300])
+@pytest.mark.parametrize("out_type", [tb.TERN_OUT_F32, tb.TERN_OUT_BF16, tb.TERN_OUT_F16])
+def test_linear_ex_tile_aligned_outputs(M, out_type):
+    # outputs cut at multiples of 128 rows (the fused-QKV shape class), the
+    # last one ragged, with padded row strides: the GEMM writes these by TMA
+    K = 512
+    splits = [256, 128, 300]
+    N = sum(splits)
+    rng = np.random.default_rng(M + out_type)
+    t, s = rand_ternary(rng, N, K), rand_scales(rng, N, K)
+    x = rand_x(rng, M, K, False)
+    tiled = tiled_from_ternary(t, s)
+    pad = 8 if out_type == tb.TERN_OUT_F32 else 16     # rows stay 16-byte aligned
+    Ys = [out_tensor(M, n, out_type, pad=pad) for n in splits]
+    ws = torch.zeros(tb.tern_workspace_bytes(M, N, K), dtype=torch.uint8, device=DEV)
+    tb.tern_linear_ex(dev(x.view(np.int16)), tb.TERN_X_BF16, K, tiled, M, K, splits, Ys, [n + pad for n in splits],
+                      out_type, ws)
+    y_ref, bound = oracle.linear(x, oracle.pack(t)[0], s, K)
+    off = 0
+    for Y, n in zip(Ys, splits):
+        y = host(Y.float())
+        assert np.all(np.isnan(y[:, n:])), "padding written"
+        check(y[:, :n], y_ref[:, off:off + n], bound[:, off:off + n], out_type, f"M={M} split {n}")
+        off += n
