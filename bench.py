@@ -6,7 +6,10 @@ with the fused QKV (5120 -> 5120+1024+1024), O (5120 -> 5120), fused
 gate+up (5120 -> 2x27648) and down (27648 -> 5120) projections, ternary
 weights resident in HBM in the tiled layout (6.2 GB), one token per step
 (M = 1).  A step is one pass over all 192 linears; it is captured once in a
-CUDA graph and replayed.
+CUDA graph and replayed.  Every linear has its own synthetic X, so the four
+linears of a layer are independent problems: the step issues one
+tern_linear_grouped launch per layer (`per_call` times the same step with
+one launch per linear, as a chain of dependent linears would need).
 
 Reported (one JSON line on rank 0):
   value      effective weight GB/s = algorithmic bytes / step time, where a
@@ -174,9 +177,11 @@ def build_stack(wl, layers, dev, tb, torch):
 class Step:
     """All linears of the stack at batch M, with X/Y arenas on the device.
     out_type: the outputs' element type (fp32 by default; bf16 through
-    tern_linear_ex)."""
+    tern_linear_ex).  grouped (M <= 16): each layer's linears -- independent
+    problems here, every one with its own synthetic X -- in one
+    tern_linear_grouped launch instead of one launch each."""
 
-    def __init__(self, wl, layers, M, tiled, dev, tb, torch, host_copies=True, out_type=0):
+    def __init__(self, wl, layers, M, tiled, dev, tb, torch, host_copies=True, out_type=0, grouped=False):
         import synth
         self.tb, self.torch = tb, torch
         self.M = M
@@ -204,6 +209,10 @@ class Step:
             ws_need = max(ws_need, tb.tern_workspace_bytes(M, lin.N, lin.K))
             self.bytes += linear_bytes(M, lin.N, lin.K) - (4 - out_size) * M * lin.N
             self.flops += 2 * M * lin.N * lin.K
+        self.grouped = grouped and M <= 16
+        if self.grouped:
+            ws_need = max(ws_need, tb.tern_grouped_workspace_bytes(M, [l.N for l in wl.linears],
+                                                                   [l.K for l in wl.linears]))
         self.ws = torch.zeros(max(ws_need, 256), dtype=torch.uint8, device=dev)
         self.ws_bytes = ws_need
         for layer, lin, xo, yo in plan:
@@ -211,6 +220,13 @@ class Step:
             Yp = self.y_dev.data_ptr() + out_size * yo
             self.calls.append((lin, X, tiled[(layer, lin.name)], Yp))
         self.launches_per_call = 1
+        self.groups = []
+        if self.grouped:
+            per = len(wl.linears)
+            for i in range(0, len(self.calls), per):
+                cs = self.calls[i:i + per]
+                self.groups.append(([c[1] for c in cs], [c[2] for c in cs], [c[0].N for c in cs],
+                                    [c[0].K for c in cs], [c[3] for c in cs]))
 
     def run_call(self, call, stream=None):
         tb, M = self.tb, self.M
@@ -233,11 +249,19 @@ class Step:
                                  self.ws, self.ws_bytes, stream)
 
     def run(self, stream=None):
+        if self.grouped:
+            tb = self.tb
+            for Xs, Ws, Ns, Ks, Ys in self.groups:
+                tb.tern_linear_grouped(tb.TERN_X_BF16, self.M, Xs, Ks, Ws, Ns, Ks, Ys, Ns, self.out_type, self.ws,
+                                       self.ws_bytes, stream)
+            return
         for call in self.calls:
             self.run_call(call, stream)
 
     @property
     def launches(self):
+        if self.grouped:
+            return len(self.groups)
         return len(self.calls) * self.launches_per_call
 
 
@@ -740,8 +764,9 @@ def main():
     del disk
     torch.cuda.empty_cache()
 
-    # ---- headline: all linears of the stack at batch M, one CUDA graph per step
-    step = Step(wl, layers, args.M, tiled, dev, tb, torch)
+    # ---- headline: all linears of the stack at batch M, one CUDA graph per
+    # step; each layer's linears (independent inputs) in one grouped launch
+    step = Step(wl, layers, args.M, tiled, dev, tb, torch, grouped=True)
     graph = capture(torch, step.run)
     sampler = ClockSampler(local)
     sampler.start()
@@ -762,6 +787,15 @@ def main():
     e2e = {"value": step.bytes / (ms_e2e / 1e3) / 1e9 * world, "unit": "GB/s",
            "h2d_bytes_per_step": step.x_host.numel() * 2, "d2h_bytes_per_step": step.y_host.numel() * 4}
     del graph
+
+    # ---- the same step with one launch per linear (a dependent chain of
+    # linears cannot be grouped)
+    step1 = Step(wl, layers, args.M, tiled, dev, tb, torch, host_copies=False)
+    graph1 = capture(torch, step1.run)
+    ms1 = time_graph(torch, graph1, args.steps, args.warmup, world)
+    per_call = {"value": step1.bytes / (ms1 / 1e3) / 1e9 * world, "unit": "GB/s", "ms_per_step": ms1,
+                "launches_per_step": step1.launches}
+    del graph1, step1
 
     # ---- the dominant kernel: the streaming kernel at the gate+up shape,
     # launched once per layer back to back on the current stream; its
@@ -785,12 +819,14 @@ def main():
                    "M": args.M, "tokens_per_step": args.M * world,
                    "weights_gb_per_step": step.bytes / 1e9,
                    "l2": "inputs larger than L2: 6.2 GB of weights streamed per step",
-                   "parallelism": f"replicas x{world}", "graph": "one CUDA graph per step"},
+                   "parallelism": f"replicas x{world}", "graph": "one CUDA graph per step",
+                   "launch": "one tern_linear_grouped launch per layer (its 4 linears)"},
         "hbm_frac": value / world / hbm_peak,
         "tokens_per_s": args.M * world / (ms / 1e3),
         "roofline": roofline,
         "e2e": e2e,
         "gpu_launches": step.launches * args.steps,
+        "per_call": per_call,
         "clocks": clocks,
         "per_linear_M1": {k: {"us": v["us"], "gbs": v["gbs"]} for k, v in per_lin.items()},
         "repack": {"gbs": repack_bytes / repack_s / 1e9, "layers": layers,

@@ -226,6 +226,33 @@ tern_status tern_linear_ex(const void* d_X, int x_type, int64_t ldx, const void*
                            void* const* d_Ys, const int64_t* ldys, int out_type,
                            void* d_ws, size_t ws_bytes, void* stream);
 
+/* A group of independent linears in one launch.  The source pages have no
+ * counterpart: this is a library convenience for problems that do not feed
+ * one another (projections of different sequences or experts, or layers
+ * whose inputs are all known), so that small linears share the fixed costs
+ * of a launch.  Problem i computes
+ *   Y_i[m, n] = sum_k X_i[m, k] * t_i[n, k] * s_i[n, k/128]
+ * exactly as tern_linear_ex with one output: X_i = d_Xs[i] [M, ldxs[i]]
+ * (x_type for all), weights d_tiled[i] for Ns[i] x Ks[i] (plain tiled
+ * layout), output d_Ys[i] [M, ldys[i]] of out_type.  d_Xs, ldxs, d_tiled,
+ * Ns, Ks, d_Ys and ldys are HOST arrays of `count` entries
+ * (1 <= count <= TERN_MAX_GROUP); the pointers in them are device pointers
+ * with the alignment rules of tern_linear_ex.  Problems with Ns[i] == 0 are
+ * skipped; M == 0 is a no-op.  Each result meets the bound of tern_linear;
+ * it may differ from a separate call's in the last bits, as the CTAs split a
+ * problem's groups differently and fp32 partial sums then add in another
+ * order (a given group is still deterministic).  M <= 16 runs as one
+ * launch; larger M as one launch per problem.
+ * The workspace is sized by tern_grouped_workspace_bytes (0 for invalid
+ * shapes) and follows the rules of tern_linear. */
+#define TERN_MAX_GROUP 8
+size_t tern_grouped_workspace_bytes(int64_t M, int count, const int64_t* Ns, const int64_t* Ks);
+
+tern_status tern_linear_grouped(int x_type, int64_t M, int count, const void* const* d_Xs,
+                                const int64_t* ldxs, const void* const* d_tiled, const int64_t* Ns,
+                                const int64_t* Ks, void* const* d_Ys, const int64_t* ldys, int out_type,
+                                void* d_ws, size_t ws_bytes, void* stream);
+
 /* ------------------------------------------------------------------------
  * Fused gate+up projection with SwiGLU ([EMB] §2.2: gate and up are one
  * fused tensor cut by offsets):

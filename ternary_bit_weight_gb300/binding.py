@@ -27,7 +27,10 @@ EXPORTED = ("tern_status_string", "tern_version", "tern_pack", "tern_unpack", "t
             "tern_repack_glu", "tern_swiglu_workspace_bytes", "tern_linear_swiglu",
             "tern_workspace_error", "tern_workspace_reset", "tern_xq_bytes", "tern_quantize_x",
             "tern_i8_workspace_bytes", "tern_linear_i8", "tern_tiled_s8_bytes", "tern_quantize_scales",
-            "tern_repack_s8", "tern_linear_s8", "tern_unit_count", "tern_zero_units", "tern_linear_sparse")
+            "tern_repack_s8", "tern_linear_s8", "tern_unit_count", "tern_zero_units", "tern_linear_sparse",
+            "tern_grouped_workspace_bytes", "tern_linear_grouped")
+
+MAX_GROUP = 8
 
 
 class TernError(RuntimeError):
@@ -68,6 +71,12 @@ def _load():
     lib.tern_linear_ex.argtypes = [vp, i32, i64, vp, i64, i64, i32, ctypes.POINTER(i64),
                                    ctypes.POINTER(vp), ctypes.POINTER(i64), i32, vp, sz, vp]
     lib.tern_linear_ex.restype = i32
+    lib.tern_grouped_workspace_bytes.argtypes = [i64, i32, ctypes.POINTER(i64), ctypes.POINTER(i64)]
+    lib.tern_grouped_workspace_bytes.restype = sz
+    lib.tern_linear_grouped.argtypes = [i32, i64, i32, ctypes.POINTER(vp), ctypes.POINTER(i64), ctypes.POINTER(vp),
+                                        ctypes.POINTER(i64), ctypes.POINTER(i64), ctypes.POINTER(vp),
+                                        ctypes.POINTER(i64), i32, vp, sz, vp]
+    lib.tern_linear_grouped.restype = i32
     lib.tern_tiled_glu_bytes.argtypes = [i64, i64]
     lib.tern_tiled_glu_bytes.restype = sz
     lib.tern_repack_glu.argtypes = [vp, vp, vp, vp, i64, i64, vp, sz, vp, vp]
@@ -223,6 +232,29 @@ def tern_linear_ex(X, x_type: int, ldx: int, tiled, M: int, K: int, n_sizes, Ys,
         ws_bytes = _nbytes(ws)
     _check(_lib.tern_linear_ex(_p(X), x_type, ldx, _p(tiled), M, K, n_out, sizes, ptrs, lds, out_type,
                                _p(ws), ws_bytes, _s(stream)), "tern_linear_ex")
+
+
+def _i64s(vals):
+    return (ctypes.c_int64 * len(vals))(*[int(v) for v in vals])
+
+
+def _ptrs(vals):
+    return (ctypes.c_void_p * len(vals))(*[_p(v) for v in vals])
+
+
+def tern_grouped_workspace_bytes(M: int, Ns, Ks) -> int:
+    return int(_lib.tern_grouped_workspace_bytes(M, len(Ns), _i64s(Ns), _i64s(Ks)))
+
+
+def tern_linear_grouped(x_type: int, M: int, Xs, ldxs, tiled, Ns, Ks, Ys, ldys, out_type: int, ws=None,
+                        ws_bytes: int | None = None, stream=None):
+    """Independent linears (one output each) in one launch (M <= 16)."""
+    count = len(Ns)
+    if ws_bytes is None:
+        ws_bytes = _nbytes(ws)
+    _check(_lib.tern_linear_grouped(x_type, M, count, _ptrs(Xs), _i64s(ldxs), _ptrs(tiled), _i64s(Ns), _i64s(Ks),
+                                    _ptrs(Ys), _i64s(ldys), out_type, _p(ws), ws_bytes, _s(stream)),
+           "tern_linear_grouped")
 
 
 def tern_tiled_glu_bytes(I: int, K: int) -> int:

@@ -6,6 +6,8 @@
 #include "tern_common.cuh"
 #include "tern_internal.h"
 
+static_assert(tern::kMaxGroup == TERN_MAX_GROUP, "group size limit of the C ABI");
+
 namespace {
 
 using tern::ceil_div;
@@ -28,9 +30,10 @@ tern_status run_linear(const uint16_t* X, bool x_f16, int64_t ldx, const void* t
     const uint8_t* w = static_cast<const uint8_t*>(tiled);
     cudaError_t e;
     if (M <= tern::kStreamMaxM) {
-        const tern::StreamPlan plan = tern::plan_stream(M, N, K, sms);
+        const tern::StreamPlan plan = tern::plan_stream(M, &N, &K, 1, sms);
         if (ws_bytes < plan.ws_bytes) return TERN_ERR_SIZE;
-        e = tern::launch_stream(X, x_f16, ldx, w, s8, zflags, M, N, K, out, ws, plan, stream);
+        tern::StreamProblem prob = {X, ldx, w, N, K, out};
+        e = tern::launch_stream(&prob, 1, x_f16, s8, zflags, M, ws, plan, stream);
     } else {
         const tern::GemmPlan plan = tern::plan_gemm(M, N, K, sms);
         if (ws_bytes < plan.ws_bytes) return TERN_ERR_SIZE;
@@ -41,7 +44,7 @@ tern_status run_linear(const uint16_t* X, bool x_f16, int64_t ldx, const void* t
 
 size_t workspace_bytes(int64_t M, int64_t N, int64_t K) {
     const int sms = tern::device_sm_count();
-    if (M <= tern::kStreamMaxM) return tern::plan_stream(M, N, K, sms).ws_bytes;
+    if (M <= tern::kStreamMaxM) return tern::plan_stream(M, &N, &K, 1, sms).ws_bytes;
     return tern::plan_gemm(M, N, K, sms).ws_bytes;
 }
 
@@ -203,6 +206,79 @@ tern_status tern_linear_ex(const void* d_X, int x_type, int64_t ldx, const void*
                            const int64_t* ldys, int out_type, void* d_ws, size_t ws_bytes, void* stream) {
     return linear_ex(d_X, x_type, ldx, d_tiled, M, K, n_out, n_sizes, d_Ys, ldys, out_type, d_ws, ws_bytes, stream,
                      false);
+}
+
+size_t tern_grouped_workspace_bytes(int64_t M, int count, const int64_t* Ns, const int64_t* Ks) {
+    if (M <= 0 || count < 1 || count > tern::kMaxGroup || Ns == nullptr || Ks == nullptr) return 0;
+    int64_t n[tern::kMaxGroup], k[tern::kMaxGroup];
+    int P = 0;
+    size_t most = 0;
+    for (int i = 0; i < count; ++i) {
+        if (!valid_group_shape(Ns[i], Ks[i])) return 0;
+        if (Ns[i] == 0) continue;
+        n[P] = Ns[i];
+        k[P] = Ks[i];
+        ++P;
+        const size_t w = workspace_bytes(M, Ns[i], Ks[i]);
+        if (w > most) most = w;
+    }
+    if (P == 0) return 256;
+    if (M > tern::kStreamMaxM) return most;   // one launch per problem, one after another
+    return tern::plan_stream(M, n, k, P, tern::device_sm_count()).ws_bytes;
+}
+
+tern_status tern_linear_grouped(int x_type, int64_t M, int count, const void* const* d_Xs, const int64_t* ldxs,
+                                const void* const* d_tiled, const int64_t* Ns, const int64_t* Ks,
+                                void* const* d_Ys, const int64_t* ldys, int out_type, void* d_ws,
+                                size_t ws_bytes, void* stream) {
+    if (x_type != TERN_X_BF16 && x_type != TERN_X_F16) return TERN_ERR_SHAPE;
+    if (out_type != TERN_OUT_F32 && out_type != TERN_OUT_BF16 && out_type != TERN_OUT_F16) return TERN_ERR_SHAPE;
+    if (count < 1 || count > tern::kMaxGroup || M < 0) return TERN_ERR_SHAPE;
+    if (d_Xs == nullptr || ldxs == nullptr || d_tiled == nullptr || Ns == nullptr || Ks == nullptr ||
+        d_Ys == nullptr || ldys == nullptr)
+        return TERN_ERR_NULL;
+    tern::StreamProblem probs[tern::kMaxGroup];
+    int64_t n[tern::kMaxGroup], k[tern::kMaxGroup];
+    int P = 0;
+    const int bf16 = out_type == TERN_OUT_BF16 ? 1 : out_type == TERN_OUT_F16 ? 2 : 0;
+    for (int i = 0; i < count; ++i) {
+        if (!valid_group_shape(Ns[i], Ks[i])) return TERN_ERR_SHAPE;
+        if (Ns[i] == 0 || M == 0) continue;
+        const uint16_t* X = static_cast<const uint16_t*>(d_Xs[i]);
+        tern_status st = check_x_w(X, ldxs[i], d_tiled[i], M, Ks[i]);
+        if (st != TERN_OK) return st;
+        if (d_Ys[i] == nullptr) return TERN_ERR_NULL;
+        if (ldys[i] < Ns[i]) return TERN_ERR_SHAPE;
+        if (!aligned(d_Ys[i], bf16 ? 2 : 4)) return TERN_ERR_ALIGN;
+        tern::OutputSplit out = {};
+        out.n_out = 1;
+        out.bf16 = bf16;
+        out.offset[0] = 0;
+        for (int j = 1; j <= tern::kMaxOutputs; ++j) out.offset[j] = Ns[i];
+        out.y[0] = d_Ys[i];
+        out.ldy[0] = ldys[i];
+        probs[P] = {X, ldxs[i], static_cast<const uint8_t*>(d_tiled[i]), Ns[i], Ks[i], out};
+        n[P] = Ns[i];
+        k[P] = Ks[i];
+        ++P;
+    }
+    if (P == 0) return TERN_OK;
+    if (M > tern::kStreamMaxM) {
+        for (int i = 0; i < P; ++i) {
+            tern_status st = run_linear(probs[i].x, x_type == TERN_X_F16, probs[i].ldx, probs[i].tiled, M, probs[i].N,
+                                        probs[i].K, probs[i].out, d_ws, ws_bytes, as_stream(stream));
+            if (st != TERN_OK) return st;
+        }
+        return TERN_OK;
+    }
+    const int sms = tern::device_sm_count();
+    if (sms <= 0) return TERN_ERR_UNSUPPORTED;
+    if (d_ws == nullptr) return TERN_ERR_NULL;
+    if (!aligned(d_ws, 256)) return TERN_ERR_ALIGN;
+    const tern::StreamPlan plan = tern::plan_stream(M, n, k, P, sms);
+    if (ws_bytes < plan.ws_bytes) return TERN_ERR_SIZE;
+    return from_cuda(tern::launch_stream(probs, P, x_type == TERN_X_F16, false, nullptr, M, d_ws, plan,
+                                         as_stream(stream)));
 }
 
 size_t tern_unit_count(int64_t N, int64_t K) {

@@ -62,10 +62,10 @@ constexpr int64_t kStreamMaxM = 16;
 // Streaming kernel plan (M <= 16): persistent CTAs, one per SM, whose
 // decode workers each own a contiguous range of 128x128 weight units.
 struct StreamPlan {
-    bool one;              // M == 1: X resident in shared memory
-    int64_t R;             // 128-row tiles
-    int64_t G;             // groups per row (K / 128)
-    int64_t U;             // units = R x G
+    bool one;              // M == 1: activation rows resident in shared memory
+    int64_t x_smem;        // shared memory for them (the largest set one CTA needs)
+    int64_t U;             // units of all problems
+    int64_t tiles;         // 128-row tiles of all problems
     int64_t V;             // workers
     int64_t grid;          // CTAs
     int stages;            // shared-memory ring depth
@@ -73,14 +73,28 @@ struct StreamPlan {
     size_t ws_bytes;       // workspace: error word, tile counters, partial slots
 };
 
-StreamPlan plan_stream(int64_t M, int64_t N, int64_t K, int sm_count);
+// Largest group of independent linears one streaming launch serves.
+constexpr int kMaxGroup = 8;
+
+// One linear of a streaming launch: Y = X . W^T with X [M, K] (row stride
+// ldx), W in the tiled layout, N outputs rows.
+struct StreamProblem {
+    const uint16_t* x;
+    int64_t ldx;
+    const uint8_t* tiled;
+    int64_t N;
+    int64_t K;
+    OutputSplit out;
+};
+
+StreamPlan plan_stream(int64_t M, const int64_t* N, const int64_t* K, int P, int sm_count);
 
 // x_f16: X holds fp16 rather than bf16 bits.
 // s8: the tiled weights carry int8 scales and per-row factors (INT8-scale layout).
 // zflags (optional): per unit, 1 = all its weights are zero; such units are skipped.
-cudaError_t launch_stream(const uint16_t* X, bool x_f16, int64_t ldx, const uint8_t* tiled, bool s8,
-                          const uint8_t* zflags, int64_t M, int64_t N, int64_t K, const OutputSplit& out, void* ws,
-                          const StreamPlan& plan, cudaStream_t stream);
+// (s8 and zflags need P == 1.)
+cudaError_t launch_stream(const StreamProblem* probs, int P, bool x_f16, bool s8, const uint8_t* zflags, int64_t M,
+                          void* ws, const StreamPlan& plan, cudaStream_t stream);
 
 // Tensor-core GEMM plan for M > kStreamMaxM: items of 256 weight rows x NT
 // tokens x a range of groups along K, persistent CTAs.

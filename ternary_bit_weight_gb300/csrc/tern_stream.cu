@@ -31,18 +31,25 @@
 // Every hand-off is an mbarrier per unit (A operands) or per pair of units
 // (accumulators), so no role waits for a batch of another's work.
 //
-// M == 1: the activation row (2K bytes) is copied once into shared memory
-// and used as B in the no-swizzle layout: row 0 of every core matrix is the
-// real row, rows 1..15 are whatever bytes follow it (they only feed
-// accumulator columns 1..15, which nobody reads), and only column 0 of each
-// unit's accumulator is promoted.
+// M == 1: the activation row of every problem the CTA's units belong to
+// (2K bytes each) is copied once into shared memory and used as B in the
+// no-swizzle layout: row 0 of every core matrix is the real row, rows
+// 1..15 are whatever bytes follow it (they only feed accumulator columns
+// 1..15, which nobody reads), and only column 0 of each unit's accumulator
+// is promoted.
 // M in 2..16: each stage also carries its units' 16-row X tiles, copied by
 // TMA (128-byte swizzle, rows >= M zero-filled).
 //
-// Work split: CTA v owns the contiguous unit range [U*v/V, U*(v+1)/V) in
-// (row tile, group) order.  A tile whose groups span two or more CTAs is
-// finished by the last of them to arrive (per 32-row quarter), which sums
-// the partials in CTA order (deterministic; no waiting on other CTAs).
+// One launch may serve a group of independent linears (the same M, each
+// with its own X, weights and outputs): their units are concatenated, each
+// problem's in (row tile, group) order, and the CTAs split the whole
+// sequence, so the fixed costs of a launch (start-up, pipeline fill, the
+// last tiles' reductions) are paid once for the group.
+//
+// Work split: CTA v owns the contiguous unit range [U*v/V, U*(v+1)/V) of the
+// sequence.  A tile whose groups span two or more CTAs is finished by the
+// last of them to arrive (per 32-row quarter), which sums the partials in
+// CTA order (deterministic; no waiting on other CTAs).
 // Every mbarrier wait is bounded; on a timeout the kernel raises the
 // workspace error word, drains its own copies and MMAs, frees its tensor
 // memory and returns.
@@ -109,8 +116,8 @@ constexpr int kBarAFull = 0;                                 // [2][kAQ]
 constexpr int kBarAEmpty = kBarAFull + 8 * 2 * kAQ;          // [2][kAQ]
 constexpr int kBarDFull = kBarAEmpty + 8 * 2 * kAQ;          // [kDP]
 constexpr int kBarDEmpty = kBarDFull + 8 * kDP;              // [kDP]
-constexpr int kBarX = kBarDEmpty + 8 * kDP;                  // activation row copied (M == 1)
-constexpr int kBarDrain = kBarX + 8;                         // [kMaxMmaWarps]
+constexpr int kBarX = kBarDEmpty + 8 * kDP;                  // [kMaxGroup] activation rows copied (M == 1)
+constexpr int kBarDrain = kBarX + 8 * kMaxGroup;             // [kMaxMmaWarps]
 constexpr int kTmemPtr = kBarDrain + 8 * kMaxMmaWarps;
 constexpr int kAbort = kTmemPtr + 4;
 constexpr int kBarStages = 256;                              // full[S], empty[S]
@@ -118,32 +125,52 @@ static_assert(kAbort + 4 <= kBarStages, "control block");
 static_assert(kBarStages + 16 * kMaxStages <= kCtrlBytes, "control block");
 static_assert(kPS % 2 == 0, "with activation tiles in the stages, each of the two MMA warps has units in every full stage");
 
-// M == 1 shared-memory layout before the stages: the activation row (2K
-// bytes) and 256 bytes the tensor cores may read past its end.
+// M == 1: shared memory for a problem's activation row (2K bytes) and 256
+// bytes the tensor cores may read past its end.  The rows of the problems a
+// CTA's units belong to lie one after another before the stages.
 __host__ __device__ constexpr int64_t x_smem_bytes(int64_t K) { return round_up(2 * K + 256, 1024); }
 
-struct StreamArgs {
-    const uint8_t* codes;
+// One linear of the launch's group.
+struct StreamProb {
+    const uint8_t* codes;      // its units' codes (tiled layout)
     const uint8_t* scales;     // per unit: 128 FP16 scales, or (s8) 128 int8 scales
+    const uint16_t* x;         // M == 1: the activation row
+    int64_t u_begin;           // its first unit in the launch's unit sequence
+    int64_t tile0;             // its first tile in the launch's tile counters
+    int64_t N;
+    int32_t R;                 // 128-row tiles
+    int32_t G;                 // groups per row
+    OutputSplit out;
+};
+
+struct StreamArgs {
     const float* row_factor;   // s8: per row, the factor of its int8 scales ([R * 128])
-    int s8;
+    int s8;                    // (s8 and zflags: single-problem launches only)
     int scale_unit;            // bytes of one unit's scales: 256, or 128 (s8)
     const uint8_t* zflags;     // optional, per unit: 1 = every weight of the unit is 0 (skipped)
-    const uint16_t* x;         // M == 1: the activation row
     int M;
-    int G;                     // groups per row
+    int P;                     // problems in the group
     int stages;
-    uint32_t x_bytes;          // M == 1: 2K
-    uint32_t x_smem;           // shared memory reserved for X (multiple of 1024)
-    int64_t N;
-    int64_t R;
-    int64_t U;
+    uint32_t x_smem;           // M == 1: shared memory before the stages for the CTA's activation rows
+    int64_t U;                 // units of all problems
     int64_t V;                 // workers = CTAs
-    OutputSplit out;
     int* err;                  // workspace error word
-    int* counters;             // [R][4 row quarters]
+    int* counters;             // [tiles of all problems][4 row quarters]
     float* slots;              // [2V][NCOL][128]
+    StreamProb prob[kMaxGroup];
 };
+
+// Tensor maps of the problems' activations (M > 1).
+struct XMaps {
+    CUtensorMap map[kMaxGroup];
+};
+
+// Problem that holds unit u of the sequence (problems in order, P small).
+__device__ __forceinline__ int problem_of(const StreamArgs& a, int64_t u) {
+    int p = 0;
+    while (p + 1 < a.P && u >= a.prob[p + 1].u_begin) ++p;
+    return p;
+}
 
 __device__ __forceinline__ int64_t owner_worker(int64_t u, int64_t U, int64_t V) {
     return ((u + 1) * V - 1) / U;
@@ -155,8 +182,9 @@ __device__ __forceinline__ int64_t owner_worker(int64_t u, int64_t U, int64_t V)
 // partials in the CTA's slot, and the last contributing CTA to arrive for
 // that row quarter sums all partials in CTA order.
 template <int NCOL>
-__device__ __forceinline__ void flush_tile(const StreamArgs& a, int64_t v, int64_t b, int64_t first_tile,
+__device__ __forceinline__ void flush_tile(const StreamArgs& a, int64_t v, int p, int64_t b, bool first,
                                            bool whole, float (&acc)[NCOL], int r, bool s8) {
+    const StreamProb& pr = a.prob[p];
     const int lane = r & 31, quad = r >> 5;
     const int64_t row = b * kTileRows + r;
     const int mvalid = a.M < NCOL ? a.M : NCOL;
@@ -166,24 +194,24 @@ __device__ __forceinline__ void flush_tile(const StreamArgs& a, int64_t v, int64
 #pragma unroll
         for (int m = 0; m < NCOL; ++m) acc[m] *= f;
     }
-    const bool live = row < a.N;
-    const RowOut o = row_out(a.out, live ? row : 0);
+    const bool live = row < pr.N;
+    const RowOut o = row_out(pr.out, live ? row : 0);
     if (whole) {
 #pragma unroll
         for (int m = 0; m < NCOL; ++m)
-            if (m < mvalid) store_out(a.out, o, m, row, acc[m], live);
+            if (m < mvalid) store_out(pr.out, o, m, row, acc[m], live);
         return;
     }
-    const int64_t slot = 2 * v + (b == first_tile ? 0 : 1);
+    const int64_t slot = 2 * v + (first ? 0 : 1);
     float* sp = a.slots + slot * (kTileRows * NCOL) + r;
 #pragma unroll
     for (int m = 0; m < NCOL; ++m)
         if (m < mvalid) sp[m * kTileRows] = acc[m];
     __syncwarp();
-    const int64_t t0 = b * a.G;
+    const int64_t t0 = pr.u_begin + b * pr.G;   // the tile's first unit in the sequence
     const int64_t w_first = owner_worker(t0, a.U, a.V);
-    const int64_t w_last = owner_worker(t0 + a.G - 1, a.U, a.V);
-    int* counter = a.counters + b * 4 + quad;
+    const int64_t w_last = owner_worker(t0 + pr.G - 1, a.U, a.V);
+    int* counter = a.counters + (pr.tile0 + b) * 4 + quad;
     int last = 0;
     if (lane == 0) {
         __threadfence();   // publish the warp's slot writes (ordered by the warp barrier)
@@ -208,7 +236,7 @@ __device__ __forceinline__ void flush_tile(const StreamArgs& a, int64_t v, int64
     }
 #pragma unroll
     for (int m = 0; m < NCOL; ++m)
-        if (m < mvalid) store_out(a.out, o, m, row, sum[m], live);
+        if (m < mvalid) store_out(pr.out, o, m, row, sum[m], live);
     if (lane == 0) *counter = 0;   // leave the workspace zeroed
 }
 
@@ -231,7 +259,7 @@ __device__ __forceinline__ bool vote_wait(uint32_t bar, uint32_t parity, bool ac
 // (a.zflags); the plain instantiation has neither check on its hot paths.
 template <bool ONE, bool XF16, bool EXT>
 __global__ void __launch_bounds__(kThreads, 1)
-stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
+stream_kernel(const __grid_constant__ XMaps xmaps, const StreamArgs a) {
     using C = SCfg<ONE>;
     const bool s8 = EXT && a.s8 != 0;
     const uint8_t* const zflags = EXT ? a.zflags : nullptr;
@@ -253,7 +281,6 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
     volatile int* abort_flag = reinterpret_cast<volatile int*>(ctrl + kAbort);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int G = a.G;
 
     // this CTA's worker: a contiguous unit range
     const int64_t v = blockIdx.x;
@@ -261,11 +288,58 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
     const int32_t n = static_cast<int32_t>(a.U * (v + 1) / a.V - u0);
     const int32_t nst = (n + kPS - 1) / kPS;   // stages of this worker
 
-    if (threadIdx.x == 0) {
+    // the producer's lane 0 starts the weight copies of the first stages at
+    // once (they do not depend on earlier kernels): their memory latency then
+    // overlaps the rest of the setup
+    auto load_weights = [&](int32_t f, uint32_t st, uint32_t bar) {
+        const int64_t uf = u0 + (int64_t)f * kPS;
+        const int32_t cnt = n - f * kPS < kPS ? n - f * kPS : kPS;
+        if (zflags == nullptr) {
+            mbar_arrive_expect_tx(bar, cnt * (kUnitCodeBytes + scale_unit + C::XUnit));
+            // one pair of copies per problem the stage's units belong to
+            int p = problem_of(a, uf);
+            for (int32_t i = 0; i < cnt; ++p) {
+                const StreamProb& pr = a.prob[p];
+                const int64_t l = uf + i - pr.u_begin;
+                const int64_t left = (int64_t)pr.R * pr.G - l;
+                const int32_t run = cnt - i < left ? cnt - i : static_cast<int32_t>(left);
+                bulk_load(st + C::OffCodes + i * kUnitCodeBytes, pr.codes + l * kUnitCodeBytes, run * kUnitCodeBytes,
+                          bar);
+                bulk_load(st + C::OffScales + i * scale_unit, pr.scales + l * scale_unit, run * scale_unit, bar);
+                i += run;
+            }
+        } else {
+            // (single problem)
+            // zero units are not copied: one copy per run of non-zero units
+            uint32_t live = 0;
+            for (int32_t i = 0; i < cnt; ++i) live |= (zflags[uf + i] ? 0u : 1u) << i;
+            mbar_arrive_expect_tx(bar, __popc(live) * (kUnitCodeBytes + scale_unit) + cnt * C::XUnit);
+            for (int32_t i = 0; i < cnt;) {
+                if (!((live >> i) & 1u)) {
+                    ++i;
+                    continue;
+                }
+                int32_t e = i;
+                while (e < cnt && ((live >> e) & 1u)) ++e;
+                bulk_load(st + C::OffCodes + i * kUnitCodeBytes, a.prob[0].codes + (uf + i) * kUnitCodeBytes,
+                          (e - i) * kUnitCodeBytes, bar);
+                bulk_load(st + C::OffScales + i * scale_unit, a.prob[0].scales + (uf + i) * scale_unit,
+                          (e - i) * scale_unit, bar);
+                i = e;
+            }
+        }
+    };
+    const int32_t pre = nst < S ? nst : S;
+    if (threadIdx.x == kProducerWarp * 32) {
         for (int s = 0; s < S; ++s) {
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, C::EmptyCount);
         }
+        mbar_fence_init();
+        fence_proxy_async_smem();   // the copies below complete on these barriers
+        for (int32_t f = 0; f < pre; ++f) load_weights(f, ring + f * C::StageBytes, bar_full + 8 * f);
+    }
+    if (threadIdx.x == 0) {
         for (int i = 0; i < 2 * kAQ; ++i) {
             mbar_init(cb + kBarAFull + 8 * i, kDecWarps / 2);   // the stream's 4 warps
             mbar_init(cb + kBarAEmpty + 8 * i, 1);
@@ -274,7 +348,7 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
             mbar_init(cb + kBarDFull + 8 * i, 2);                // both MMA warps
             mbar_init(cb + kBarDEmpty + 8 * i, 4);               // the promotion warps
         }
-        mbar_init(cb + kBarX, 1);
+        for (int i = 0; i < kMaxGroup; ++i) mbar_init(cb + kBarX + 8 * i, 1);
         for (int i = 0; i < kMaxMmaWarps; ++i) mbar_init(cb + kBarDrain + 8 * i, 1);
         *abort_flag = 0;
         mbar_fence_init();
@@ -283,7 +357,8 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
         tmem_alloc(smem_u32(tmem_base_ptr), kTmemCols);
         tmem_relinquish();
     }
-    if (!ONE && warp == kProducerWarp && lane == 0) prefetch_tensormap(&xmap);
+    if (!ONE && warp == kProducerWarp && lane < a.P) prefetch_tensormap(&xmaps.map[lane]);
+    __syncwarp();
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
@@ -292,67 +367,52 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
 
     if (warp == kProducerWarp) {
         // ---------------------------------------------------------- producer
-        // the whole warp runs the loop; one elected lane issues the copies
-        auto load_weights = [&](int32_t f, uint32_t st, uint32_t bar) {
-            const int64_t uf = u0 + (int64_t)f * kPS;
-            const int32_t cnt = n - f * kPS < kPS ? n - f * kPS : kPS;
-            if (elect_one()) {
-                if (zflags == nullptr) {
-                    mbar_arrive_expect_tx(bar, cnt * (kUnitCodeBytes + scale_unit + C::XUnit));
-                    bulk_load(st + C::OffCodes, a.codes + uf * kUnitCodeBytes, cnt * kUnitCodeBytes, bar);
-                    bulk_load(st + C::OffScales, a.scales + uf * scale_unit, cnt * scale_unit, bar);
-                } else {
-                    // zero units are not copied: one copy per run of non-zero units
-                    uint32_t live = 0;
-                    for (int32_t i = 0; i < cnt; ++i) live |= (zflags[uf + i] ? 0u : 1u) << i;
-                    mbar_arrive_expect_tx(bar, __popc(live) * (kUnitCodeBytes + scale_unit) + cnt * C::XUnit);
-                    for (int32_t i = 0; i < cnt;) {
-                        if (!((live >> i) & 1u)) {
-                            ++i;
-                            continue;
-                        }
-                        int32_t e = i;
-                        while (e < cnt && ((live >> e) & 1u)) ++e;
-                        bulk_load(st + C::OffCodes + i * kUnitCodeBytes, a.codes + (uf + i) * kUnitCodeBytes,
-                                  (e - i) * kUnitCodeBytes, bar);
-                        bulk_load(st + C::OffScales + i * scale_unit, a.scales + (uf + i) * scale_unit,
-                                  (e - i) * scale_unit, bar);
-                        i = e;
-                    }
-                }
-            }
-            __syncwarp();
-        };
-        // the weights of the first stages do not depend on earlier kernels
-        const int32_t pre = nst < S ? nst : S;
-        for (int32_t f = 0; f < pre; ++f) load_weights(f, ring + f * C::StageBytes, bar_full + 8 * f);
+        // the whole warp runs the loop; lane 0 issues the copies
         grid_dependency_wait();
-        if (ONE) {
-            if (elect_one()) {
-                mbar_arrive_expect_tx(cb + kBarX, a.x_bytes);
-                bulk_load(sbase, a.x, a.x_bytes, cb + kBarX);
+        if (ONE && n > 0) {
+            // the activation rows of the problems this CTA's units belong to
+            const int pf = problem_of(a, u0), pl = problem_of(a, u0 + n - 1);
+            uint32_t off = 0;
+            for (int p = pf; p <= pl; ++p) {
+                const uint32_t bytes = static_cast<uint32_t>(a.prob[p].G) * kGroup * 2;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(cb + kBarX + 8 * (p - pf), bytes);
+                    bulk_load(sbase + off, a.prob[p].x, bytes, cb + kBarX + 8 * (p - pf));
+                }
+                off += static_cast<uint32_t>(x_smem_bytes((int64_t)a.prob[p].G * kGroup));
             }
             __syncwarp();
         }
-        int32_t gx = static_cast<int32_t>(u0 % G);           // group of the next X tile
+        // problem and group of the next unit whose activation tile is copied (M > 1)
+        int px = problem_of(a, u0);
+        int32_t gx = static_cast<int32_t>((u0 - a.prob[px].u_begin) % a.prob[px].G);
+        int32_t bx = static_cast<int32_t>((u0 - a.prob[px].u_begin) / a.prob[px].G);
         int s = 0;
         uint32_t round = 0;   // completed passes over the ring
         for (int32_t f = 0; f < nst; ++f) {
             const uint32_t st = ring + s * C::StageBytes;
             if (f >= pre) {
                 if (!warp_wait(bar_empty + 8 * s, (round - 1) & 1u, abort_flag)) break;
-                load_weights(f, st, bar_full + 8 * s);
+                if (lane == 0) load_weights(f, st, bar_full + 8 * s);
+                __syncwarp();
             }
             if (!ONE) {
                 const int32_t cnt = n - f * kPS < kPS ? n - f * kPS : kPS;
                 for (int32_t i = 0; i < cnt; ++i) {
-                    const int32_t k0 = gx * kGroup;
-                    if (elect_one()) {
-                        tma_load_2d(st + i * C::XUnit, &xmap, k0, 0, bar_full + 8 * s);
-                        tma_load_2d(st + i * C::XUnit + kNtok * 128, &xmap, k0 + 64, 0, bar_full + 8 * s);
+                    const StreamProb& pr = a.prob[px];
+                    if (lane == 0) {
+                        tma_load_2d(st + i * C::XUnit, &xmaps.map[px], gx * kGroup, 0, bar_full + 8 * s);
+                        tma_load_2d(st + i * C::XUnit + kNtok * 128, &xmaps.map[px], gx * kGroup + 64, 0,
+                                    bar_full + 8 * s);
                     }
                     __syncwarp();
-                    if (++gx == G) gx = 0;
+                    if (++gx == pr.G) {
+                        gx = 0;
+                        if (++bx == pr.R) {
+                            bx = 0;
+                            ++px;
+                        }
+                    }
                 }
             }
             if (++s == S) {
@@ -367,7 +427,9 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
                 (void)mbar_wait(bar_full + 8 * t, 0, &no_abort);
                 (void)mbar_wait(bar_full + 8 * t, 1, &no_abort);
             }
-            (void)mbar_wait(cb + kBarX, 0, &no_abort);
+            if (ONE && n > 0)
+                for (int p = problem_of(a, u0); p <= problem_of(a, u0 + n - 1); ++p)
+                    (void)mbar_wait(cb + kBarX + 8 * (p - problem_of(a, u0)), 0, &no_abort);
         }
     } else if (mma_index(warp) >= 0 && mma_index(warp) < C::MmaWarps) {
         // --------------------------------------------------------------- MMA
@@ -380,71 +442,86 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
         constexpr int kMmaWarps = C::MmaWarps;
         constexpr uint32_t idesc = XF16 ? idesc_fp16_f32(128, kNtok) : idesc_bf16_f32(128, kNtok);
         bool ok = true;
-        int32_t g = static_cast<int32_t>((u0 + m) % G);   // group of unit j
-        // B descriptors: M == 1 the resident row (+16 per group, +2 per K-step);
-        // else the unit's X tile in the stage
+        // B descriptors: M == 1 the problem's resident row (+16 per group,
+        // +2 per K-step); else the unit's X tile in the stage
         const uint64_t bdesc_x = smem_desc_kmajor_noswz(sbase, 16, 16);
         const uint64_t bdesc_ring = smem_desc_kmajor_sw128(ring);
+        // M == 1: one problem at a time, its row offset and group count
+        // fixed over the inner loop (B comes from the stage otherwise)
+        const int pf = problem_of(a, u0);
+        const int pl = ONE && n > 0 ? problem_of(a, u0 + n - 1) : pf;
+        uint32_t xoff = 0;
         // stage of unit j (M > 1; kMmaWarps divides kPS): tracked, not divided
         int us = m, s = 0;
         uint32_t full_ph = 0;
-        for (int32_t j = m; j < n && ok; j += kMmaWarps) {
-            const int q = j & 1;                 // decode stream
-            const int32_t k = j >> 1;            // pair = the stream's unit index
-            const int al = k % kAQ, dp = k % kDP;
-            const uint32_t a_ph = (k / kAQ) & 1u, d_ph = (k / kDP) & 1u;
-            // one vote: D pair free (lane 1), stage full (lane 2), A slot
-            // full (lane 3), activation row copied (lane 4, first units)
-            uint32_t bar = 0, par = 0;
-            bool act = false;
-            if (lane == 1) {
-                act = k >= kDP;
-                bar = cb + kBarDEmpty + 8 * dp;
-                par = d_ph ^ 1u;
-            } else if (lane == 2) {
-                act = !ONE && us < kMmaWarps;
-                bar = bar_full + 8 * s;
-                par = full_ph;
-            } else if (lane == 3) {
-                act = true;
-                bar = cb + kBarAFull + 8 * (kAQ * q + al);
-                par = a_ph;
-            } else if (lane == 4) {
-                act = ONE && j == m;
-                bar = cb + kBarX;
-                par = 0;
-            }
-            if (!(ok = vote_wait(bar, par, act, abort_flag))) break;
-            tc_fence_after_sync();
-            const uint32_t a_tm = tmem + (q * kAQ + al) * kACols;
-            const uint32_t d_tm = tmem + kDCol0 + (2 * dp + q) * kNtok;
-            const uint64_t b0 = ONE ? bdesc_x + 16u * (uint32_t)g
-                                    : bdesc_ring + ((uint32_t)(s * C::StageBytes + us * C::XUnit) >> 4);
-            const bool zero = zflags != nullptr && zflags[u0 + j] != 0;
-            if (elect_one()) {
-                if (!zero) {
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        // M == 1: +32 bytes per K-step; else +32 bytes within a
-                        // 64-wide box and +2048 bytes to the second box
-                        const uint32_t step = ONE ? 2 * kk : (kk >> 2) * (kNtok * 128 / 16) + 2 * (kk & 3);
-                        umma_bf16_tmem_a(d_tm, a_tm + 8 * kk, b0 + step, idesc, kk > 0 ? 1u : 0u);
+        int32_t j = m;
+        for (int p = pf; p <= pl && ok; ++p) {
+            const int32_t G = a.prob[p].G;
+            const int64_t pend = a.prob[p].u_begin + (int64_t)a.prob[p].R * G - u0;   // the problem's end in this CTA
+            const int32_t jend = p == pl ? n : static_cast<int32_t>(pend < n ? pend : n);
+            int32_t g = static_cast<int32_t>((u0 + j - a.prob[p].u_begin) % G);   // group of unit j
+            const uint64_t bdesc_p = bdesc_x + (xoff >> 4);
+            bool first = true;   // this warp's first unit of the problem: wait for its row
+            for (; j < jend && ok; j += kMmaWarps) {
+                const int q = j & 1;                 // decode stream
+                const int32_t k = j >> 1;            // pair = the stream's unit index
+                const int al = k % kAQ, dp = k % kDP;
+                const uint32_t a_ph = (k / kAQ) & 1u, d_ph = (k / kDP) & 1u;
+                // one vote: D pair free (lane 1), stage full (lane 2), A slot
+                // full (lane 3), the problem's activation row copied (lane 4)
+                uint32_t bar = 0, par = 0;
+                bool act = false;
+                if (lane == 1) {
+                    act = k >= kDP;
+                    bar = cb + kBarDEmpty + 8 * dp;
+                    par = d_ph ^ 1u;
+                } else if (lane == 2) {
+                    act = !ONE && us < kMmaWarps;
+                    bar = bar_full + 8 * s;
+                    par = full_ph;
+                } else if (lane == 3) {
+                    act = true;
+                    bar = cb + kBarAFull + 8 * (kAQ * q + al);
+                    par = a_ph;
+                } else if (lane == 4) {
+                    act = ONE && first;
+                    bar = cb + kBarX + 8 * (p - pf);
+                    par = 0;
+                }
+                if (!(ok = vote_wait(bar, par, act, abort_flag))) break;
+                tc_fence_after_sync();
+                const uint32_t a_tm = tmem + (q * kAQ + al) * kACols;
+                const uint32_t d_tm = tmem + kDCol0 + (2 * dp + q) * kNtok;
+                first = false;
+                const uint64_t b0 = ONE ? bdesc_p + 16u * (uint32_t)g
+                                        : bdesc_ring + ((uint32_t)(s * C::StageBytes + us * C::XUnit) >> 4);
+                const bool zero = zflags != nullptr && zflags[u0 + j] != 0;
+                if (elect_one()) {
+                    if (!zero) {
+    #pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            // M == 1: +32 bytes per K-step; else +32 bytes within a
+                            // 64-wide box and +2048 bytes to the second box
+                            const uint32_t step = ONE ? 2 * kk : (kk >> 2) * (kNtok * 128 / 16) + 2 * (kk & 3);
+                            umma_bf16_tmem_a(d_tm, a_tm + 8 * kk, b0 + step, idesc, kk > 0 ? 1u : 0u);
+                        }
+                    }
+                    umma_commit(cb + kBarAEmpty + 8 * (kAQ * q + al));
+                    umma_commit(cb + kBarDFull + 8 * dp);
+                    if (!ONE && (us + kMmaWarps >= kPS || j + kMmaWarps >= n)) umma_commit(bar_empty + 8 * s);
+                }
+                __syncwarp();
+                g += kMmaWarps;
+                while (g >= G) g -= G;
+                if (!ONE && (us += kMmaWarps) >= kPS) {
+                    us -= kPS;
+                    if (++s == S) {
+                        s = 0;
+                        full_ph ^= 1u;
                     }
                 }
-                umma_commit(cb + kBarAEmpty + 8 * (kAQ * q + al));
-                umma_commit(cb + kBarDFull + 8 * dp);
-                if (!ONE && (us + kMmaWarps >= kPS || j + kMmaWarps >= n)) umma_commit(bar_empty + 8 * s);
             }
-            __syncwarp();
-            g += kMmaWarps;
-            while (g >= G) g -= G;
-            if (!ONE && (us += kMmaWarps) >= kPS) {
-                us -= kPS;
-                if (++s == S) {
-                    s = 0;
-                    full_ph ^= 1u;
-                }
-            }
+            xoff += static_cast<uint32_t>(x_smem_bytes((int64_t)G * kGroup));
         }
         // odd n: the last pair has no stream-1 unit; the warp that would
         // have issued it still signals the pair's accumulators -- after the
@@ -525,8 +602,12 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
         const int r = threadIdx.x & 127;   // weight row in the tile = tensor-memory lane
         const uint32_t tm = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + kDCol0;
         const int scale_off = C::OffScales + (s8 ? 1 : 2) * r;   // + unit in stage * scale_unit
-        const int64_t first_tile = u0 / G;
-        const int32_t first_g = static_cast<int32_t>(u0 - first_tile * G);
+        // problem, tile and group of the next unit
+        int pp = problem_of(a, u0);
+        const int first_p = pp;
+        int32_t G = a.prob[pp].G, R = a.prob[pp].R;
+        const int64_t first_tile = (u0 - a.prob[pp].u_begin) / G;
+        const int32_t first_g = static_cast<int32_t>((u0 - a.prob[pp].u_begin) % G);
         int64_t pb = first_tile;
         int32_t pg = first_g;
         float acc[NCOL];
@@ -585,14 +666,20 @@ stream_kernel(const __grid_constant__ CUtensorMap xmap, const StreamArgs a) {
 #pragma unroll
                     for (int m = 0; m < NCOL; ++m) acc[m] = fmaf(sc, __uint_as_float(d[i * NCOL + m]), acc[m]);
                 if (pg == G - 1 || u == n - 1) {
-                    const bool whole = (pb != first_tile || first_g == 0) && pg == G - 1;
-                    flush_tile<NCOL>(a, v, pb, first_tile, whole, acc, r, s8);
+                    const bool first = pp == first_p && pb == first_tile;
+                    const bool whole = (!first || first_g == 0) && pg == G - 1;
+                    flush_tile<NCOL>(a, v, pp, pb, first, whole, acc, r, s8);
 #pragma unroll
                     for (int m = 0; m < NCOL; ++m) acc[m] = 0.f;
                 }
                 if (++pg == G) {
                     pg = 0;
-                    ++pb;
+                    if (++pb == R && pp + 1 < a.P) {
+                        pb = 0;
+                        ++pp;
+                        G = a.prob[pp].G;
+                        R = a.prob[pp].R;
+                    }
                 }
             }
         }
@@ -641,22 +728,24 @@ cudaError_t set_smem_limit() {
 }
 
 template <bool ONE, bool XF16, bool EXT>
-cudaError_t launch_one(const uint16_t* X, int64_t ldx, const StreamArgs& a, const StreamPlan& plan,
+cudaError_t launch_one(const StreamProblem* probs, const StreamArgs& a, const StreamPlan& plan,
                        cudaStream_t stream) {
-    CUtensorMap map;
-    memset(&map, 0, sizeof(map));
+    XMaps maps;
+    memset(&maps, 0, sizeof(maps));
     if (!ONE) {
         EncodeTiledFn enc = encode_tiled_fn();
         if (enc == nullptr) return cudaErrorNotSupported;
-        const int64_t K = (int64_t)a.G * kGroup;
-        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(a.M)};
-        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldx) * 2};
-        const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kNtok)};
-        const cuuint32_t estr[2] = {1, 1};
-        if (enc(&map, XF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(X), dims, strides, box, estr,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
+        for (int p = 0; p < a.P; ++p) {
+            const cuuint64_t dims[2] = {static_cast<cuuint64_t>(probs[p].K), static_cast<cuuint64_t>(a.M)};
+            const cuuint64_t strides[1] = {static_cast<cuuint64_t>(probs[p].ldx) * 2};
+            const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kNtok)};
+            const cuuint32_t estr[2] = {1, 1};
+            if (enc(&maps.map[p], XF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                    const_cast<uint16_t*>(probs[p].x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                return cudaErrorInvalidValue;
+        }
     }
     cudaError_t e = set_smem_limit<ONE, XF16, EXT>();
     if (e != cudaSuccess) return e;
@@ -670,74 +759,101 @@ cudaError_t launch_one(const uint16_t* X, int64_t ldx, const StreamArgs& a, cons
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, stream_kernel<ONE, XF16, EXT>, map, a);
+    return cudaLaunchKernelEx(&cfg, stream_kernel<ONE, XF16, EXT>, maps, a);
 }
 
 }  // namespace
 
-StreamPlan plan_stream(int64_t M, int64_t N, int64_t K, int sm_count) {
+StreamPlan plan_stream(int64_t M, const int64_t* N, const int64_t* K, int P, int sm_count) {
     StreamPlan p = {};
     if (sm_count <= 0) sm_count = 152;
-    p.R = ceil_div(N, kTileRows);
-    p.G = K / kGroup;
-    p.U = p.R * p.G;
+    p.U = 0;
+    p.tiles = 0;
+    for (int i = 0; i < P; ++i) {
+        const int64_t R = ceil_div(N[i], kTileRows);
+        p.U += R * (K[i] / kGroup);
+        p.tiles += R;
+    }
     p.V = p.U < sm_count ? p.U : sm_count;   // one worker per CTA, one CTA per SM
     p.grid = p.V;
-    // M == 1 keeps the activation row in shared memory when at least three
-    // stages still fit beside it
-    const int64_t x_smem = x_smem_bytes(K);
-    const int64_t avail_one = kSmemLimit - 1024 - kCtrlBytes - x_smem;
-    p.one = (M == 1) && avail_one >= 3 * SCfg<true>::StageBytes;
+    // M == 1 keeps the activation rows of each CTA's problems in shared
+    // memory when at least three stages still fit beside the largest set
+    int64_t x_smem = 0;
+    if (M == 1) {
+        int64_t begin[kMaxGroup + 1];
+        begin[0] = 0;
+        for (int i = 0; i < P; ++i) begin[i + 1] = begin[i] + ceil_div(N[i], kTileRows) * (K[i] / kGroup);
+        for (int64_t v = 0; v < p.V; ++v) {
+            const int64_t u0 = p.U * v / p.V, u1 = p.U * (v + 1) / p.V;
+            int64_t bytes = 0;
+            for (int i = 0; i < P; ++i)
+                if (begin[i] < u1 && begin[i + 1] > u0) bytes += x_smem_bytes(K[i]);
+            if (bytes > x_smem) x_smem = bytes;
+        }
+    }
+    p.one = M == 1 && kSmemLimit - 1024 - kCtrlBytes - x_smem >= 3 * SCfg<true>::StageBytes;
+    p.x_smem = p.one ? x_smem : 0;
     const int64_t stage_bytes = p.one ? SCfg<true>::StageBytes : SCfg<false>::StageBytes;
-    const int64_t avail = p.one ? avail_one : kSmemLimit - 1024 - kCtrlBytes;
-    int64_t stages = avail / stage_bytes;
+    int64_t stages = (kSmemLimit - 1024 - kCtrlBytes - p.x_smem) / stage_bytes;
     if (stages > kMaxStages) stages = kMaxStages;
     p.stages = static_cast<int>(stages);
-    p.smem = static_cast<size_t>(1024 + (p.one ? x_smem : 0) + stages * stage_bytes + kCtrlBytes);
+    p.smem = static_cast<size_t>(1024 + p.x_smem + stages * stage_bytes + kCtrlBytes);
     const int64_t ncol = p.one ? SCfg<true>::NCOL : SCfg<false>::NCOL;
-    const size_t counters = static_cast<size_t>(round_up(p.R * 4 * 4, 256));
+    const size_t counters = static_cast<size_t>(round_up(p.tiles * 4 * 4, 256));
     p.ws_bytes = kWorkspaceErrBytes + counters + static_cast<size_t>(2 * p.V * kTileRows * ncol) * sizeof(float);
     return p;
 }
 
-cudaError_t launch_stream(const uint16_t* X, bool x_f16, int64_t ldx, const uint8_t* tiled, bool s8,
-                          const uint8_t* zflags, int64_t M, int64_t N, int64_t K, const OutputSplit& out, void* ws,
-                          const StreamPlan& plan, cudaStream_t stream) {
+cudaError_t launch_stream(const StreamProblem* probs, int P, bool x_f16, bool s8, const uint8_t* zflags, int64_t M,
+                          void* ws, const StreamPlan& plan, cudaStream_t stream) {
+    if (P < 1 || P > kMaxGroup || ((s8 || zflags != nullptr) && P != 1)) return cudaErrorInvalidValue;
     StreamArgs a = {};
     a.zflags = zflags;
-    a.codes = tiled;
-    a.scales = tiled + plan.U * kUnitCodeBytes;
     a.s8 = s8 ? 1 : 0;
     a.scale_unit = s8 ? kUnitScaleBytesS8 : kUnitScaleBytes;
-    a.row_factor = s8 ? reinterpret_cast<const float*>(tiled + plan.U * (kUnitCodeBytes + kUnitScaleBytesS8)) : nullptr;
-    a.x = X;
     a.M = static_cast<int>(M);
-    a.G = static_cast<int>(plan.G);
+    a.P = P;
     a.stages = plan.stages;
-    a.x_bytes = static_cast<uint32_t>(2 * K);
-    a.x_smem = plan.one ? static_cast<uint32_t>(x_smem_bytes(K)) : 0u;
-    a.N = N;
-    a.R = plan.R;
+    a.x_smem = static_cast<uint32_t>(plan.x_smem);
     a.U = plan.U;
     a.V = plan.V;
-    a.out = out;
+    int64_t u = 0, tile = 0;
+    for (int p = 0; p < P; ++p) {
+        StreamProb& pr = a.prob[p];
+        const int64_t R = ceil_div(probs[p].N, kTileRows), G = probs[p].K / kGroup;
+        pr.codes = probs[p].tiled;
+        pr.scales = probs[p].tiled + R * G * kUnitCodeBytes;
+        pr.x = probs[p].x;
+        pr.u_begin = u;
+        pr.tile0 = tile;
+        pr.N = probs[p].N;
+        pr.R = static_cast<int32_t>(R);
+        pr.G = static_cast<int32_t>(G);
+        pr.out = probs[p].out;
+        u += R * G;
+        tile += R;
+    }
+    if (s8) {
+        const int64_t U0 = a.prob[0].R * (int64_t)a.prob[0].G;
+        a.row_factor = reinterpret_cast<const float*>(probs[0].tiled + U0 * (kUnitCodeBytes + kUnitScaleBytesS8));
+    }
     uint8_t* w = static_cast<uint8_t*>(ws);
     a.err = reinterpret_cast<int*>(w);
     a.counters = reinterpret_cast<int*>(w + kWorkspaceErrBytes);
-    a.slots = reinterpret_cast<float*>(w + kWorkspaceErrBytes + static_cast<size_t>(round_up(plan.R * 4 * 4, 256)));
+    a.slots = reinterpret_cast<float*>(w + kWorkspaceErrBytes + static_cast<size_t>(round_up(plan.tiles * 4 * 4, 256)));
     const bool ext = s8 || zflags != nullptr;
     if (ext) {
         if (x_f16)
-            return plan.one ? launch_one<true, true, true>(X, ldx, a, plan, stream)
-                            : launch_one<false, true, true>(X, ldx, a, plan, stream);
-        return plan.one ? launch_one<true, false, true>(X, ldx, a, plan, stream)
-                        : launch_one<false, false, true>(X, ldx, a, plan, stream);
+            return plan.one ? launch_one<true, true, true>(probs, a, plan, stream)
+                            : launch_one<false, true, true>(probs, a, plan, stream);
+        return plan.one ? launch_one<true, false, true>(probs, a, plan, stream)
+                        : launch_one<false, false, true>(probs, a, plan, stream);
     }
     if (x_f16)
-        return plan.one ? launch_one<true, true, false>(X, ldx, a, plan, stream)
-                        : launch_one<false, true, false>(X, ldx, a, plan, stream);
-    return plan.one ? launch_one<true, false, false>(X, ldx, a, plan, stream)
-                    : launch_one<false, false, false>(X, ldx, a, plan, stream);
+        return plan.one ? launch_one<true, true, false>(probs, a, plan, stream)
+                        : launch_one<false, true, false>(probs, a, plan, stream);
+    return plan.one ? launch_one<true, false, false>(probs, a, plan, stream)
+                    : launch_one<false, false, false>(probs, a, plan, stream);
 }
 
 }  // namespace tern

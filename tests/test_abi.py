@@ -216,3 +216,39 @@ def test_s8_sizes_and_argument_errors():
     assert lib.tern_repack_s8(FAKE, FAKE, FAKE, 32, 256, FAKE, need - 1, None, None) == 4
     assert lib.tern_quantize_scales(FAKE, 32, 256, FAKE, FAKE + 2, None) == 3
     assert lib.tern_quantize_scales(FAKE, 32, 100, FAKE, FAKE, None) == 2
+
+
+def test_grouped_sizes_and_argument_errors():
+    lib = binding.library()
+    i64 = ctypes.c_int64
+    vp = ctypes.c_void_p
+
+    def arr(t, vals):
+        return (t * len(vals))(*vals)
+
+    Ns, Ks = arr(i64, [256, 512]), arr(i64, [256, 1024])
+    ws_fn = lib.tern_grouped_workspace_bytes
+    assert ws_fn(1, 2, Ns, Ks) > 0
+    assert ws_fn(1, 2, Ns, Ks) >= binding.tern_workspace_bytes(1, 512, 1024)
+    assert ws_fn(40, 2, Ns, Ks) == max(binding.tern_workspace_bytes(40, 256, 256),
+                                       binding.tern_workspace_bytes(40, 512, 1024))
+    assert ws_fn(1, 0, Ns, Ks) == 0
+    assert ws_fn(1, binding.MAX_GROUP + 1, Ns, Ks) == 0
+    assert ws_fn(1, 1, arr(i64, [256]), arr(i64, [200])) == 0     # K % 128
+    assert ws_fn(0, 2, Ns, Ks) == 0
+    f = lib.tern_linear_grouped
+    X, W, Y = arr(vp, [FAKE, FAKE]), arr(vp, [FAKE, FAKE]), arr(vp, [FAKE, FAKE])
+    ld = arr(i64, [1024, 1024])
+    assert f(2, 1, 2, X, ld, W, Ns, Ks, Y, ld, 0, None, 0, None) == 2            # x_type
+    assert f(0, 1, 2, X, ld, W, Ns, Ks, Y, ld, 3, None, 0, None) == 2            # out_type
+    assert f(0, 1, 0, X, ld, W, Ns, Ks, Y, ld, 0, None, 0, None) == 2            # count
+    assert f(0, 1, binding.MAX_GROUP + 1, X, ld, W, Ns, Ks, Y, ld, 0, None, 0, None) == 2
+    assert f(0, 1, 2, None, ld, W, Ns, Ks, Y, ld, 0, None, 0, None) == 1         # host arrays
+    assert f(0, 1, 2, X, ld, W, Ns, arr(i64, [256, 100]), Y, ld, 0, None, 0, None) == 2
+    assert f(0, 1, 2, X, arr(i64, [255, 1024]), W, Ns, Ks, Y, ld, 0, None, 0, None) == 2   # ldx < K
+    assert f(0, 1, 2, arr(vp, [FAKE + 2, FAKE]), ld, W, Ns, Ks, Y, ld, 0, None, 0, None) == 3
+    assert f(0, 1, 2, X, ld, W, Ns, Ks, arr(vp, [FAKE, None]), ld, 0, None, 0, None) == 1
+    assert f(0, 1, 2, X, ld, W, Ns, Ks, Y, arr(i64, [1024, 511]), 0, None, 0, None) == 2  # ldy < N
+    assert f(0, 1, 2, X, ld, W, Ns, Ks, arr(vp, [FAKE + 2, FAKE]), ld, 0, None, 0, None) == 3   # fp32 Y
+    assert f(0, 0, 2, X, ld, W, Ns, Ks, Y, ld, 0, None, 0, None) == 0            # M == 0
+    assert f(0, 1, 1, X, ld, W, arr(i64, [0]), Ks, Y, ld, 0, None, 0, None) == 0  # N == 0 only
