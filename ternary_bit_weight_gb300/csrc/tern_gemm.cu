@@ -433,16 +433,21 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ YM
                     tc_fence_after_sync();
                 }
                 if (mine) {
+                    // two stores of 32 columns: the first runs while the
+                    // second half decodes (the empty asm keeps that decode
+                    // after the first store)
                     uint32_t p[64];
                     decode_word_fp16_scaled(c0.x, s2, dk, p);
                     decode_word_fp16_scaled(c0.y, s2, dk, p + 8);
                     decode_word_fp16_scaled(c0.z, s2, dk, p + 16);
                     decode_word_fp16_scaled(c0.w, s2, dk, p + 24);
+                    tmem_st_32x32b_x32(tm + al * kACols, p);
+                    asm volatile("" : "+r"(c1.x), "+r"(c1.y), "+r"(c1.z), "+r"(c1.w));
                     decode_word_fp16_scaled(c1.x, s2, dk, p + 32);
                     decode_word_fp16_scaled(c1.y, s2, dk, p + 40);
                     decode_word_fp16_scaled(c1.z, s2, dk, p + 48);
                     decode_word_fp16_scaled(c1.w, s2, dk, p + 56);
-                    tmem_st_32x32b_x64(tm + al * kACols, p);
+                    tmem_st_32x32b_x32(tm + al * kACols + 32, p + 32);
                     tmem_st_wait();
                 }
                 tc_fence_before_sync();

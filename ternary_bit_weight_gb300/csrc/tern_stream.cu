@@ -18,7 +18,9 @@
 //     thread per weight row = one tensor-memory lane): each 16-weight code
 //     word becomes eight exact bf16 pairs t in {-1,0,+1} (one LOP3 + one
 //     bf16x2 FMA per pair, balanced between the integer and FMA pipes)
-//     stored with tcgen05.st into the stream's 3-unit ring of A operands;
+//     stored with tcgen05.st (two stores of 32 columns, the first running
+//     while the second half decodes) into the stream's 3-unit ring of A
+//     operands;
 //   * two MMA warps, one per stream: eight tcgen05.mma (M = 128, N = 16,
 //     K = 16, bf16 -> fp32) per unit, A from tensor memory, B = X from
 //     shared memory, into one of 8 accumulator slots; the whole warp runs
@@ -577,16 +579,29 @@ stream_kernel(const __grid_constant__ XMaps xmaps, const StreamArgs a) {
                 tc_fence_after_sync();
             }
             if (!zero) {
+                // two halves of 32 columns: the first half's store runs while
+                // the second half decodes (the empty asm keeps the compiler
+                // from moving that decode ahead of the first store)
                 uint32_t p[64];
-                const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                const uint32_t cw[4] = {c0.x, c0.y, c0.z, c0.w};
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
+                for (int i = 0; i < 4; ++i) {
                     if (XF16)
                         decode_word_f16(cw[i], dk, p + 8 * i);
                     else
                         decode_word_bf16(cw[i], dk, p + 8 * i);
                 }
-                tmem_st_32x32b_x64(tm + al * kACols, p);
+                tmem_st_32x32b_x32(tm + al * kACols, p);
+                asm volatile("" : "+r"(c1.x), "+r"(c1.y), "+r"(c1.z), "+r"(c1.w));
+                const uint32_t cw2[4] = {c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    if (XF16)
+                        decode_word_f16(cw2[i], dk, p + 32 + 8 * i);
+                    else
+                        decode_word_bf16(cw2[i], dk, p + 32 + 8 * i);
+                }
+                tmem_st_32x32b_x32(tm + al * kACols + 32, p + 32);
             }
             tmem_st_wait();
             tc_fence_before_sync();
