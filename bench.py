@@ -15,11 +15,12 @@ Reported (one JSON line on rank 0):
   value      effective weight GB/s = algorithmic bytes / step time, where a
              linear moves N*K/4 (codes) + 2*N*K/128 (FP16 scales) +
              2*M*K (bf16 X) + 4*M*N (fp32 Y) bytes
-  roofline   the dominant kernel (the streaming kernel at the gate+up shape,
-             launched once per layer back to back): algorithmic bytes per
-             launch / average launch duration, against the measured copy
-             bandwidth; `traffic` is the DRAM bytes per launch from the
-             committed ncu summary while the kernel sources are unchanged
+  roofline   the dominant kernel (the streaming kernel serving one layer's
+             four linears, the step's only kernel, launched for every layer
+             back to back outside the graph): algorithmic bytes per launch /
+             average launch duration, against the measured copy bandwidth;
+             `traffic` is the DRAM bytes per launch from the committed ncu
+             summary while the kernel sources are unchanged
   e2e        the same metric with the step's X copied in from pinned host
              memory and all Y copied back, inside the timed region
   legs       the other listed configurations, each with its own clock record:
@@ -32,9 +33,9 @@ Reported (one JSON line on rank 0):
 
 `--impl reference` times the CPU oracle alone (the reference arm).
 `--profile NAME` runs one linear of layer 0 (qkv, o, gate_up, down,
-gate_up_swiglu) or the repack of it (repack) `--reps` times at batch `--M`
-and exits: the program the committed ncu summaries under profiles/ were
-captured from.
+gate_up_swiglu), the repack of gate_up (repack) or layer 0's four linears
+as one grouped launch (layer) `--reps` times at batch `--M` and exits: the
+program the committed ncu summaries under profiles/ were captured from.
 """
 from __future__ import annotations
 
@@ -384,11 +385,11 @@ def run_reference(args, world, rank):
 
 # ------------------------------------------------------------------ legs
 
-def traffic_from_profile(kernel_files):
+def traffic_from_profile(kernel_files, name="stream_layer_m1.txt"):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
     summary, or None if the kernel's sources changed since the capture."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", "stream_gate_up_m1.txt")
+    path = os.path.join(ROOT, "profiles", name)
     try:
         lines = open(path).read().splitlines()
     except OSError:
@@ -404,7 +405,7 @@ def traffic_from_profile(kernel_files):
     if kv.get("kernel_sources_sha256") != h.hexdigest():
         return None, "kernel changed since the capture"
     try:
-        return int(kv["dram_bytes_per_launch"]), "profiles/stream_gate_up_m1.txt"
+        return int(kv["dram_bytes_per_launch"]), "profiles/" + name
     except (KeyError, ValueError):
         return None, "no traffic line"
 
@@ -690,6 +691,28 @@ def run_profile(args):
         torch.cuda.synchronize()
         print("ok", name, args.M)
         return
+    if name == "layer":
+        # layer 0's four linears as one grouped launch
+        Xs, Ws, Ys, Ns, Ks = [], [], [], [], []
+        for lin in wl.linears:
+            t, s = synth.weights(wl, 0, lin)
+            t_d = torch.from_numpy(t).to(dev)
+            packed = torch.empty((lin.N, lin.K // 4), dtype=torch.uint8, device=dev)
+            tb.tern_pack(t_d, lin.N, lin.K, packed)
+            del t_d
+            tiled = torch.empty(tb.tern_tiled_bytes(lin.N, lin.K), dtype=torch.uint8, device=dev)
+            tb.tern_repack(packed, torch.from_numpy(s.view(np.int16)).to(dev), lin.N, lin.K, tiled)
+            Xs.append(torch.from_numpy(synth.activations(wl, 0, lin, args.M).view(np.int16)).to(dev))
+            Ws.append(tiled)
+            Ys.append(torch.empty((args.M, lin.N), dtype=torch.float32, device=dev))
+            Ns.append(lin.N)
+            Ks.append(lin.K)
+        ws = torch.zeros(max(tb.tern_grouped_workspace_bytes(args.M, Ns, Ks), 256), dtype=torch.uint8, device=dev)
+        for _ in range(args.reps):
+            tb.tern_linear_grouped(tb.TERN_X_BF16, args.M, Xs, Ks, Ws, Ns, Ks, Ys, Ns, tb.TERN_OUT_F32, ws)
+        torch.cuda.synchronize()
+        print("ok layer", args.M)
+        return
     lname = "gate_up" if name == "repack" else name
     lin = next(l for l in wl.linears if l.name == lname)
     t, s = synth.weights(wl, 0, lin)
@@ -734,7 +757,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--profile", default=None,
-                    help="run one layer-0 linear (or 'repack', 'gate_up_swiglu') --reps times and exit")
+                    help="run one layer-0 linear (or repack, gate_up_swiglu, layer) --reps times and exit")
     ap.add_argument("--reps", type=int, default=6)
     args = ap.parse_args()
 
@@ -797,19 +820,20 @@ def main():
                 "launches_per_step": step1.launches}
     del graph1, step1
 
-    # ---- the dominant kernel: the streaming kernel at the gate+up shape,
-    # launched once per layer back to back on the current stream; its
-    # average launch duration from CUDA events over those launches
-    gu = next(l for l in wl.linears if l.name == "gate_up")
-    per_lin = leg_per_linear(wl, layers, tiled, dev, tb, torch, [args.M], local)[str(args.M)]
-    avg_s = per_lin["gate_up"]["us"] * 1e-6
-    achieved = linear_bytes(args.M, gu.N, gu.K) / avg_s / 1e9
+    # ---- the dominant kernel: the streaming kernel serving one layer's four
+    # linears (the step's only kernel), launched for every layer back to back
+    # on the current stream; its average launch duration from CUDA events
+    layer_bytes = step.bytes // layers
+    ms_pass, _ = timed_region(torch, lambda: step.run(), 1, local, min_ms=100.0)
+    avg_s = ms_pass / 1e3 / step.launches
+    achieved = layer_bytes / avg_s / 1e9
     traffic, traffic_src = traffic_from_profile(KERNEL_FILES)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                 "frac": achieved / hbm_peak, "traffic": traffic, "traffic_source": traffic_src,
                 "peak_source": peak_src + " (copy bandwidth)",
-                "kernel": f"stream_kernel (tern_linear_multi, gate+up {gu.K}->{gu.N}, M={args.M})",
-                "bytes_per_launch": linear_bytes(args.M, gu.N, gu.K), "avg_launch_us": avg_s * 1e6}
+                "kernel": f"stream_kernel (tern_linear_grouped: one layer's qkv, o, gate_up, down; M={args.M})",
+                "bytes_per_launch": layer_bytes, "avg_launch_us": avg_s * 1e6}
+    per_lin = leg_per_linear(wl, layers, tiled, dev, tb, torch, [args.M], local)[str(args.M)]
 
     out = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
