@@ -126,6 +126,12 @@ constexpr int kBarStages = 256;                              // full[S], empty[S
 static_assert(kAbort + 4 <= kBarStages, "control block");
 static_assert(kBarStages + 16 * kMaxStages <= kCtrlBytes, "control block");
 static_assert(kPS % 2 == 0, "with activation tiles in the stages, each of the two MMA warps has units in every full stage");
+// A slot of stream q is used by units j, j + 2 kAQ, ...: the same MMA warp
+// must issue all of them, or a warp could test the slot's barrier two
+// phases ahead of its decoder and take the older phase (same parity) as the
+// one it waits for.  (The accumulator pairs need no such rule: before a
+// warp reaches pair k + 2 kDP it has waited for a pair after k.)
+static_assert((2 * kAQ) % kMaxMmaWarps == 0 && (2 * kAQ) % 2 == 0, "A ring depth and MMA warp count");
 
 // M == 1: shared memory for a problem's activation row (2K bytes) and 256
 // bytes the tensor cores may read past its end.  The rows of the problems a
