@@ -21,9 +21,9 @@
 //     stored with tcgen05.st (two stores of 32 columns, the first running
 //     while the second half decodes) into the stream's 3-unit ring of A
 //     operands;
-//   * two MMA warps, one per stream: eight tcgen05.mma (M = 128, N = 16,
-//     K = 16, bf16 -> fp32) per unit, A from tensor memory, B = X from
-//     shared memory, into one of 8 accumulator slots; the whole warp runs
+//   * three MMA warps taking units in turn: eight tcgen05.mma (M = 128,
+//     N = 16, K = 16, bf16 -> fp32) per unit, A from tensor memory, B = X
+//     from shared memory, into one of 8 accumulator slots; the whole warp runs
 //     the loop and one elected lane issues (warp-uniform descriptors issue
 //     far faster than a loop inside a single-lane branch);
 //   * promotion warpgroup: reads each unit's fp32 group partial with
@@ -74,9 +74,8 @@ namespace {
 // the issue slots of their sub-partition for hundreds of cycles at a time.
 // Warp w reaches tensor-memory lanes 32 (w mod 4) .. +31, so each
 // warpgroup of decode or promotion warps starts at a multiple of 4.
-// MMA warp m (warps 0, 1 and, at M = 1, 3) issues units m, m+W, ... for W
-// MMA warps: a warp's MMA issue is slow next to busy decoders, so M = 1,
-// with nothing else to copy, spreads it over three.
+// MMA warp m (warps 0, 1 and 3) issues units m, m+3, ...: a warp's MMA
+// issue is slow next to busy decoders, so it is spread over three warps.
 constexpr int kMaxMmaWarps = 3;
 constexpr int kProducerWarp = 2;
 constexpr int kAllocWarp = 0;
@@ -102,7 +101,7 @@ constexpr int kMaxStages = 48;
 
 template <bool ONE>
 struct SCfg {
-    static constexpr int MmaWarps = ONE ? 3 : 2;
+    static constexpr int MmaWarps = 3;
     static constexpr int NCOL = ONE ? 1 : kNtok;        // token columns promoted per unit
     static constexpr int XUnit = ONE ? 0 : kNtok * kGroup * 2;   // one unit's X tile
     static constexpr int OffCodes = kPS * XUnit;         // X tiles first (1024-byte aligned)
@@ -125,13 +124,13 @@ constexpr int kAbort = kTmemPtr + 4;
 constexpr int kBarStages = 256;                              // full[S], empty[S]
 static_assert(kAbort + 4 <= kBarStages, "control block");
 static_assert(kBarStages + 16 * kMaxStages <= kCtrlBytes, "control block");
-static_assert(kPS % 2 == 0, "with activation tiles in the stages, each of the two MMA warps has units in every full stage");
+static_assert(kPS >= kMaxMmaWarps, "with activation tiles in the stages, every MMA warp has units in every full stage");
 // A slot of stream q is used by units j, j + 2 kAQ, ...: the same MMA warp
 // must issue all of them, or a warp could test the slot's barrier two
 // phases ahead of its decoder and take the older phase (same parity) as the
 // one it waits for.  (The accumulator pairs need no such rule: before a
 // warp reaches pair k + 2 kDP it has waited for a pair after k.)
-static_assert((2 * kAQ) % kMaxMmaWarps == 0 && (2 * kAQ) % 2 == 0, "A ring depth and MMA warp count");
+static_assert((2 * kAQ) % kMaxMmaWarps == 0, "A ring depth and MMA warp count");
 
 // M == 1: shared memory for a problem's activation row (2K bytes) and 256
 // bytes the tensor cores may read past its end.  The rows of the problems a
@@ -441,7 +440,7 @@ stream_kernel(const __grid_constant__ XMaps xmaps, const StreamArgs a) {
         }
     } else if (mma_index(warp) >= 0 && mma_index(warp) < C::MmaWarps) {
         // --------------------------------------------------------------- MMA
-        // MMA warp m issues units j = m, m + 4, ... (stream j mod 2, that
+        // MMA warp m issues units j = m, m + 3, ... (stream j mod 2, that
         // stream's unit j / 2).  The whole warp runs the loop with
         // warp-uniform descriptors; one elected lane issues the MMAs and
         // commits.  Each unit's eight MMAs start its own accumulator, so the
@@ -459,7 +458,7 @@ stream_kernel(const __grid_constant__ XMaps xmaps, const StreamArgs a) {
         const int pf = problem_of(a, u0);
         const int pl = ONE && n > 0 ? problem_of(a, u0 + n - 1) : pf;
         uint32_t xoff = 0;
-        // stage of unit j (M > 1; kMmaWarps divides kPS): tracked, not divided
+        // stage of unit j (M > 1): tracked, not divided
         int us = m, s = 0;
         uint32_t full_ph = 0;
         int32_t j = m;
