@@ -28,7 +28,9 @@ Reported (one JSON line on rank 0):
              M = 32..256 (tokens/s), prefill M = 1024..4096 (TFLOP/s), the
              0.6B embedding-model layers at M = 1, 32, 512 and the single
              1024x1024 linear at M = 1, 8
-  repack     GB/s of tern_repack over all 48 layers (disk -> tiled)
+  repack     GB/s of the disk -> tiled repack of all 48 layers, one
+             tern_repack_grouped launch per layer (per_call_gbs: one
+             tern_repack per weight)
   cpu_baseline  the fp64 CPU oracle timed on a bounded sample
 
 `--impl reference` times the CPU oracle alone (the reference arm).
@@ -161,18 +163,30 @@ def build_stack(wl, layers, dev, tb, torch):
             tiled[(layer, lin.name)] = torch.empty(tb.tern_tiled_bytes(lin.N, lin.K), dtype=torch.uint8, device=dev)
     s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     repack_bytes = 0
+    for layer in range(layers):
+        for lin in wl.linears:
+            packed, sc = disk[(layer, lin.name)]
+            # read disk codes + scales, write tiled codes + scales
+            repack_bytes += packed.numel() + 2 * sc.numel() + tiled[(layer, lin.name)].numel()
+    # one tern_repack_grouped launch per layer (its four weights) ...
     torch.cuda.synchronize()
+    s0.record()
+    for layer in range(layers):
+        srcs = [disk[(layer, lin.name)] for lin in wl.linears]
+        tb.tern_repack_grouped([p for p, _ in srcs], [c for _, c in srcs], [lin.N for lin in wl.linears],
+                               [lin.K for lin in wl.linears], [tiled[(layer, lin.name)] for lin in wl.linears])
+    s1.record()
+    torch.cuda.synchronize()
+    grouped_s = s0.elapsed_time(s1) / 1e3
+    # ... and one tern_repack per weight (same results, written again)
     s0.record()
     for layer in range(layers):
         for lin in wl.linears:
             packed, sc = disk[(layer, lin.name)]
-            out = tiled[(layer, lin.name)]
-            tb.tern_repack(packed, sc, lin.N, lin.K, out)
-            # read disk codes + scales, write tiled codes + scales
-            repack_bytes += packed.numel() + 2 * sc.numel() + out.numel()
+            tb.tern_repack(packed, sc, lin.N, lin.K, tiled[(layer, lin.name)])
     s1.record()
     torch.cuda.synchronize()
-    return tiled, disk, repack_bytes, s0.elapsed_time(s1) / 1e3
+    return tiled, disk, repack_bytes, (grouped_s, s0.elapsed_time(s1) / 1e3)
 
 
 class Step:
@@ -866,8 +880,9 @@ def main():
         "per_call": per_call,
         "clocks": clocks,
         "per_linear_M1": {k: {"us": v["us"], "gbs": v["gbs"]} for k, v in per_lin.items()},
-        "repack": {"gbs": repack_bytes / repack_s / 1e9, "layers": layers,
-                   "bytes": repack_bytes, "ms": repack_s * 1e3},
+        "repack": {"gbs": repack_bytes / repack_s[0] / 1e9, "layers": layers, "bytes": repack_bytes,
+                   "ms": repack_s[0] * 1e3, "launch": "one tern_repack_grouped per layer",
+                   "per_call_gbs": repack_bytes / repack_s[1] / 1e9},
     }
     del step
     torch.cuda.empty_cache()

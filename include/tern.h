@@ -133,6 +133,18 @@ size_t tern_tiled_bytes(int64_t N, int64_t K);
 tern_status tern_repack(const uint8_t* d_packed, const uint16_t* d_scales, int64_t N, int64_t K,
                         void* d_tiled, size_t tiled_bytes, int32_t* d_err, void* stream);
 
+/* Several independent repacks in one launch (a library convenience, with no
+ * counterpart in the pages: a loader converting many weights at once shares
+ * the fixed costs of a launch).  Repack i is tern_repack(d_packed[i],
+ * d_scales[i], Ns[i], Ks[i], d_tiled[i], tiled_bytes[i]); every array is a
+ * HOST array of `count` entries (1 <= count <= TERN_MAX_GROUP) and the
+ * pointers in them follow tern_repack's rules.  Repacks with Ns[i] == 0 are
+ * skipped; invalid codes of all of them add up in *d_err.  The tiled
+ * buffers must not overlap one another or any source. */
+tern_status tern_repack_grouped(int count, const uint8_t* const* d_packed, const uint16_t* const* d_scales,
+                                const int64_t* Ns, const int64_t* Ks, void* const* d_tiled,
+                                const size_t* tiled_bytes, int32_t* d_err, void* stream);
+
 /* tiled -> on-disk (packed, scales), rows < N only; the inverse of
  * tern_repack on valid data (code 11 comes back as 00).  A stored value of
  * 3 (never written by tern_repack) unpacks to weight 0 and is counted in

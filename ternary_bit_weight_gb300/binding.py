@@ -28,7 +28,7 @@ EXPORTED = ("tern_status_string", "tern_version", "tern_pack", "tern_unpack", "t
             "tern_workspace_error", "tern_workspace_reset", "tern_xq_bytes", "tern_quantize_x",
             "tern_i8_workspace_bytes", "tern_linear_i8", "tern_tiled_s8_bytes", "tern_quantize_scales",
             "tern_repack_s8", "tern_linear_s8", "tern_unit_count", "tern_zero_units", "tern_linear_sparse",
-            "tern_grouped_workspace_bytes", "tern_linear_grouped")
+            "tern_grouped_workspace_bytes", "tern_linear_grouped", "tern_repack_grouped")
 
 MAX_GROUP = 8
 
@@ -77,6 +77,9 @@ def _load():
                                         ctypes.POINTER(i64), ctypes.POINTER(i64), ctypes.POINTER(vp),
                                         ctypes.POINTER(i64), i32, vp, sz, vp]
     lib.tern_linear_grouped.restype = i32
+    lib.tern_repack_grouped.argtypes = [i32, ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(i64),
+                                        ctypes.POINTER(i64), ctypes.POINTER(vp), ctypes.POINTER(sz), vp, vp]
+    lib.tern_repack_grouped.restype = i32
     lib.tern_tiled_glu_bytes.argtypes = [i64, i64]
     lib.tern_tiled_glu_bytes.restype = sz
     lib.tern_repack_glu.argtypes = [vp, vp, vp, vp, i64, i64, vp, sz, vp, vp]
@@ -255,6 +258,16 @@ def tern_linear_grouped(x_type: int, M: int, Xs, ldxs, tiled, Ns, Ks, Ys, ldys, 
     _check(_lib.tern_linear_grouped(x_type, M, count, _ptrs(Xs), _i64s(ldxs), _ptrs(tiled), _i64s(Ns), _i64s(Ks),
                                     _ptrs(Ys), _i64s(ldys), out_type, _p(ws), ws_bytes, _s(stream)),
            "tern_linear_grouped")
+
+
+def tern_repack_grouped(packed, scales, Ns, Ks, tiled, tiled_bytes=None, err=None, stream=None):
+    """Several disk -> tiled repacks in one launch."""
+    count = len(Ns)
+    if tiled_bytes is None:
+        tiled_bytes = [_nbytes(t) for t in tiled]
+    sizes = (ctypes.c_size_t * count)(*[int(v) for v in tiled_bytes])
+    _check(_lib.tern_repack_grouped(count, _ptrs(packed), _ptrs(scales), _i64s(Ns), _i64s(Ks), _ptrs(tiled), sizes,
+                                    _p(err), _s(stream)), "tern_repack_grouped")
 
 
 def tern_tiled_glu_bytes(I: int, K: int) -> int:

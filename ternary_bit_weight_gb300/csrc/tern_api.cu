@@ -123,6 +123,36 @@ tern_status tern_repack(const uint8_t* d_packed, const uint16_t* d_scales, int64
                                          d_err, as_stream(stream)));
 }
 
+tern_status tern_repack_grouped(int count, const uint8_t* const* d_packed, const uint16_t* const* d_scales,
+                                const int64_t* Ns, const int64_t* Ks, void* const* d_tiled,
+                                const size_t* tiled_bytes, int32_t* d_err, void* stream) {
+    if (count < 1 || count > tern::kMaxGroup) return TERN_ERR_SHAPE;
+    if (d_packed == nullptr || d_scales == nullptr || Ns == nullptr || Ks == nullptr || d_tiled == nullptr ||
+        tiled_bytes == nullptr)
+        return TERN_ERR_NULL;
+    if (d_err != nullptr && !aligned(d_err, 4)) return TERN_ERR_ALIGN;
+    const uint8_t* packed[tern::kMaxGroup];
+    const uint16_t* scales[tern::kMaxGroup];
+    int64_t n[tern::kMaxGroup], k[tern::kMaxGroup];
+    uint8_t* tiled[tern::kMaxGroup];
+    int P = 0;
+    for (int i = 0; i < count; ++i) {
+        if (!valid_group_shape(Ns[i], Ks[i])) return TERN_ERR_SHAPE;
+        if (Ns[i] == 0) continue;
+        if (d_packed[i] == nullptr || d_scales[i] == nullptr || d_tiled[i] == nullptr) return TERN_ERR_NULL;
+        if (!aligned(d_packed[i], 4) || !aligned(d_scales[i], 2) || !aligned(d_tiled[i], 16)) return TERN_ERR_ALIGN;
+        if (tiled_bytes[i] < tern_tiled_bytes(Ns[i], Ks[i])) return TERN_ERR_SIZE;
+        packed[P] = d_packed[i];
+        scales[P] = d_scales[i];
+        n[P] = Ns[i];
+        k[P] = Ks[i];
+        tiled[P] = static_cast<uint8_t*>(d_tiled[i]);
+        ++P;
+    }
+    if (P == 0) return TERN_OK;
+    return from_cuda(tern::launch_repack_grouped(packed, scales, n, k, tiled, P, d_err, as_stream(stream)));
+}
+
 tern_status tern_unrepack(const void* d_tiled, int64_t N, int64_t K, uint8_t* d_packed,
                           uint16_t* d_scales, int32_t* d_err, void* stream) {
     if (!valid_group_shape(N, K)) return TERN_ERR_SHAPE;

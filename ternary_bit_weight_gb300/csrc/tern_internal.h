@@ -15,6 +15,9 @@ cudaError_t launch_unpack(const uint8_t* packed, int64_t count, int8_t* t, int32
                           cudaStream_t stream);
 cudaError_t launch_repack(const uint8_t* packed, const uint16_t* scales, int64_t N, int64_t K,
                           uint8_t* tiled, int32_t* err, cudaStream_t stream);
+// P (<= kMaxGroup) independent repacks in one launch.
+cudaError_t launch_repack_grouped(const uint8_t* const* packed, const uint16_t* const* scales, const int64_t* N,
+                                  const int64_t* K, uint8_t* const* tiled, int P, int32_t* err, cudaStream_t stream);
 // GLU layout: gate and up rows interleaved in blocks of 16 (tiled row n is
 // gate row 16*(n/32) + n%32 when n%32 < 16, else the up row of that index);
 // glu_rows(I) combined rows, padded with zero rows.
@@ -36,6 +39,8 @@ cudaError_t launch_unrepack(const uint8_t* tiled, int64_t N, int64_t K, uint8_t*
 
 // ---------------------------------------------------------- linear layer
 constexpr int kMaxOutputs = 4;
+// Largest group of independent problems (linears, repacks) one launch serves.
+constexpr int kMaxGroup = 8;
 
 // Where the rows of the concatenated N go: rows [offset[j], offset[j+1])
 // to output j, element (m, n) at y[j][m * ldy[j] + n - offset[j]], stored as
@@ -73,8 +78,6 @@ struct StreamPlan {
     size_t ws_bytes;       // workspace: error word, tile counters, partial slots
 };
 
-// Largest group of independent linears one streaming launch serves.
-constexpr int kMaxGroup = 8;
 
 // One linear of a streaming launch: Y = X . W^T with X [M, K] (row stride
 // ldx), W in the tiled layout, N outputs rows.

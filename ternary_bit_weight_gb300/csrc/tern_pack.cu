@@ -194,53 +194,106 @@ __device__ __forceinline__ bool source_row(const RepackSrc& s, int64_t n, int& w
     return row < s.rows;
 }
 
-// One thread per (unit, row): the row's 32 disk bytes of the group (one
-// DRAM sector) become its two 16-byte runs of the unit (a warp writes 512
-// contiguous bytes per run) and its scale.  VEC: the sources are 16-byte
-// aligned, so the 32 bytes come in two vector loads.
+// One thread per (row, run of up to kRunGroups groups): the row's disk bytes
+// of those groups (contiguous, 32 per group) become the row's two 16-byte
+// runs in each of the units (a warp of 32 rows writes 512 contiguous bytes
+// per run), and its scales.  Reading a whole run per thread keeps the
+// warp's reads in long contiguous pieces of each row.  VEC: the sources are
+// 16-byte aligned, so each group's 32 bytes come in two vector loads.
+constexpr int kRunGroups = 2;
+
+__host__ __device__ constexpr int64_t repack_items(int64_t units, int64_t K) {
+    return units / (K / kGroup) * kTileRows * ceil_div(K / kGroup, kRunGroups);
+}
+
+// One repack of a launch: a weight (or, GLU, a pair of them) into its
+// tiled buffer; a launch serves up to kMaxGroup of them, their items one
+// after another.
+struct RepackJob {
+    RepackSrc src;
+    uint8_t* tiled;
+    int64_t K;
+    int64_t units;
+    int64_t item_begin;
+};
+struct RepackJobs {
+    RepackJob job[kMaxGroup];
+    int count;
+    int64_t items;
+};
+
 template <bool VEC>
 __global__ void __launch_bounds__(kThreads)
-repack_kernel(const RepackSrc src, int64_t K, int64_t units, uint8_t* __restrict__ tiled, int32_t* err) {
-    const int64_t G = K / kGroup;
-    const int64_t row_bytes = K / 4;
-    uint16_t* tscales = reinterpret_cast<uint16_t*>(tiled + units * kUnitCodeBytes);
-    int8_t* tscales8 = reinterpret_cast<int8_t*>(tiled + units * kUnitCodeBytes);
-    float* tfactor = reinterpret_cast<float*>(tiled + units * (kUnitCodeBytes + kUnitScaleBytesS8));
+repack_kernel(const RepackJobs jobs, int32_t* err) {
     int bad = 0;
-    for (int64_t i = blockIdx.x * (int64_t)kThreads + threadIdx.x; i < units * kTileRows;
+    int p = 0;   // job of item i (items rise along the loop)
+    for (int64_t i = blockIdx.x * (int64_t)kThreads + threadIdx.x; i < jobs.items;
          i += (int64_t)gridDim.x * kThreads) {
-        const int64_t unit = i >> 7;
-        const int r = static_cast<int>(i & 127);
-        const int64_t b = unit / G, g = unit - b * G;
+        while (p + 1 < jobs.count && i >= jobs.job[p + 1].item_begin) ++p;
+        const RepackJob& J = jobs.job[p];
+        const RepackSrc& src = J.src;
+        const int64_t K = J.K, units = J.units;
+        uint8_t* const tiled = J.tiled;
+        const int64_t G = K / kGroup;
+        const int64_t GB = ceil_div(G, kRunGroups);   // runs per row
+        const int64_t row_bytes = K / 4;
+        uint16_t* tscales = reinterpret_cast<uint16_t*>(tiled + units * kUnitCodeBytes);
+        int8_t* tscales8 = reinterpret_cast<int8_t*>(tiled + units * kUnitCodeBytes);
+        float* tfactor = reinterpret_cast<float*>(tiled + units * (kUnitCodeBytes + kUnitScaleBytesS8));
+        const int64_t li = i - J.item_begin;
+        const int r = static_cast<int>(li & 127);
+        const int64_t tb = li >> 7;                   // (tile, run)
+        const int64_t b = tb / GB, gb = tb - b * GB;
+        const int64_t g0 = gb * kRunGroups;
+        const int ng = static_cast<int>(G - g0 < kRunGroups ? G - g0 : kRunGroups);
         int which;
         int64_t row;
         const bool valid = source_row(src, b * kTileRows + r, which, row);
-        uint32_t w[8] = {0, 0, 0, 0, 0, 0, 0, 0};   // padding rows: code 00, weight 0
-        uint16_t sc = 0;
-        if (valid) {
-            const uint8_t* p = (which ? src.packed[1] : src.packed[0]) + row * row_bytes + 32 * g;
-            if (VEC) {
-                const uint4 a = __ldg(reinterpret_cast<const uint4*>(p));
-                const uint4 c = __ldg(reinterpret_cast<const uint4*>(p) + 1);
-                w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
-                w[4] = c.x; w[5] = c.y; w[6] = c.z; w[7] = c.w;
-            } else {
+        uint32_t w[kRunGroups][8];
+        uint16_t sc[kRunGroups];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) w[q] = __ldg(reinterpret_cast<const uint32_t*>(p) + q);
+        for (int q = 0; q < kRunGroups; ++q) {
+            sc[q] = 0;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) w[q][e] = 0;   // padding rows: code 00, weight 0
+        }
+        if (valid) {
+            const uint8_t* p = (which ? src.packed[1] : src.packed[0]) + row * row_bytes + 32 * g0;
+            const uint16_t* sp = (which ? src.scales[1] : src.scales[0]) + row * G + g0;
+#pragma unroll
+            for (int q = 0; q < kRunGroups; ++q) {
+                if (q < ng) {
+                    if (VEC) {
+                        const uint4 a = __ldg(reinterpret_cast<const uint4*>(p + 32 * q));
+                        const uint4 c = __ldg(reinterpret_cast<const uint4*>(p + 32 * q) + 1);
+                        w[q][0] = a.x; w[q][1] = a.y; w[q][2] = a.z; w[q][3] = a.w;
+                        w[q][4] = c.x; w[q][5] = c.y; w[q][6] = c.z; w[q][7] = c.w;
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) w[q][e] = __ldg(reinterpret_cast<const uint32_t*>(p + 32 * q) + e);
+                    }
+                    if (!src.s8) sc[q] = __ldg(sp + q);
+                }
             }
-            if (!src.s8) sc = __ldg((which ? src.scales[1] : src.scales[0]) + row * G + g);
         }
-        uint8_t* u = tiled + unit * kUnitCodeBytes + 16 * r;
-        *reinterpret_cast<uint4*>(u) = make_uint4(disk_to_tiled_word(w[0], bad), disk_to_tiled_word(w[1], bad),
-                                                  disk_to_tiled_word(w[2], bad), disk_to_tiled_word(w[3], bad));
-        *reinterpret_cast<uint4*>(u + 2048) = make_uint4(disk_to_tiled_word(w[4], bad), disk_to_tiled_word(w[5], bad),
-                                                         disk_to_tiled_word(w[6], bad), disk_to_tiled_word(w[7], bad));
-        if (src.s8) {
-            tscales8[unit * kTileRows + r] = valid ? src.q8[row * G + g] : int8_t(0);
-            if (g == 0) tfactor[b * kTileRows + r] = valid ? src.f[row] : 0.f;
-        } else {
-            tscales[unit * kTileRows + r] = sc;
+#pragma unroll
+        for (int q = 0; q < kRunGroups; ++q) {
+            if (q < ng) {
+                const int64_t unit = b * G + g0 + q;
+                uint8_t* u = tiled + unit * kUnitCodeBytes + 16 * r;
+                *reinterpret_cast<uint4*>(u) = make_uint4(disk_to_tiled_word(w[q][0], bad), disk_to_tiled_word(w[q][1], bad),
+                                                          disk_to_tiled_word(w[q][2], bad), disk_to_tiled_word(w[q][3], bad));
+                *reinterpret_cast<uint4*>(u + 2048) =
+                    make_uint4(disk_to_tiled_word(w[q][4], bad), disk_to_tiled_word(w[q][5], bad),
+                               disk_to_tiled_word(w[q][6], bad), disk_to_tiled_word(w[q][7], bad));
+                if (src.s8) {
+                    tscales8[unit * kTileRows + r] = valid ? src.q8[row * G + g0 + q] : int8_t(0);
+                } else {
+                    tscales[unit * kTileRows + r] = sc[q];
+                }
+            }
         }
+        if (src.s8 && gb == 0) tfactor[b * kTileRows + r] = valid ? src.f[row] : 0.f;
     }
     __threadfence();   // writes visible GPU-wide before exit (early-starting successors)
     count_errors(err, bad);
@@ -292,6 +345,30 @@ cudaError_t launch_flat(Kernel kernel, int64_t items, cudaStream_t stream, Args.
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// P repacks in one launch: source, tiled buffer, tiled rows and K of each.
+cudaError_t launch_repack_jobs(const RepackSrc* srcs, uint8_t* const* tiled, const int64_t* rows, const int64_t* K,
+                               int P, int32_t* err, cudaStream_t stream) {
+    if (P < 1 || P > kMaxGroup) return cudaErrorInvalidValue;
+    RepackJobs jobs = {};
+    jobs.count = P;
+    bool vec = true;
+    int64_t items = 0;
+    for (int i = 0; i < P; ++i) {
+        RepackJob& J = jobs.job[i];
+        J.src = srcs[i];
+        J.tiled = tiled[i];
+        J.K = K[i];
+        J.units = ceil_div(rows[i], kTileRows) * (K[i] / kGroup);
+        J.item_begin = items;
+        items += repack_items(J.units, K[i]);
+        vec = vec && ((reinterpret_cast<uintptr_t>(srcs[i].packed[0]) | reinterpret_cast<uintptr_t>(srcs[i].packed[1])) &
+                      15) == 0;
+    }
+    jobs.items = items;
+    return vec ? launch_flat(repack_kernel<true>, items, stream, jobs, err)
+               : launch_flat(repack_kernel<false>, items, stream, jobs, err);
+}
+
 }  // namespace
 
 cudaError_t launch_pack(const int8_t* t, int64_t count, uint8_t* packed, int32_t* err,
@@ -319,6 +396,18 @@ cudaError_t launch_unpack(const uint8_t* packed, int64_t count, int8_t* t, int32
     return launch_flat(unpack_bytes_kernel, bytes - 4 * words, stream, packed, 4 * words, bytes, t, err);
 }
 
+cudaError_t launch_repack_grouped(const uint8_t* const* packed, const uint16_t* const* scales, const int64_t* N,
+                                  const int64_t* K, uint8_t* const* tiled, int P, int32_t* err, cudaStream_t stream) {
+    RepackSrc src[kMaxGroup] = {};
+    if (P < 1 || P > kMaxGroup) return cudaErrorInvalidValue;
+    for (int i = 0; i < P; ++i) {
+        src[i].packed[0] = src[i].packed[1] = packed[i];
+        src[i].scales[0] = src[i].scales[1] = scales[i];
+        src[i].rows = N[i];
+    }
+    return launch_repack_jobs(src, tiled, N, K, P, err, stream);
+}
+
 cudaError_t launch_repack(const uint8_t* packed, const uint16_t* scales, int64_t N, int64_t K,
                           uint8_t* tiled, int32_t* err, cudaStream_t stream) {
     RepackSrc src = {};
@@ -326,10 +415,7 @@ cudaError_t launch_repack(const uint8_t* packed, const uint16_t* scales, int64_t
     src.scales[0] = src.scales[1] = scales;
     src.rows = N;
     src.glu = 0;
-    const int64_t units = ceil_div(N, kTileRows) * (K / kGroup);
-    const bool vec = (reinterpret_cast<uintptr_t>(packed) & 15) == 0;
-    return vec ? launch_flat(repack_kernel<true>, units * kTileRows, stream, src, K, units, tiled, err)
-               : launch_flat(repack_kernel<false>, units * kTileRows, stream, src, K, units, tiled, err);
+    return launch_repack_jobs(&src, &tiled, &N, &K, 1, err, stream);
 }
 
 // One warp per unit: 1024 code words, 32 per lane, one vote.
@@ -363,10 +449,7 @@ cudaError_t launch_repack_s8(const uint8_t* packed, const int8_t* q8, const floa
     src.f = f;
     src.rows = N;
     src.s8 = 1;
-    const int64_t units = ceil_div(N, kTileRows) * (K / kGroup);
-    const bool vec = (reinterpret_cast<uintptr_t>(packed) & 15) == 0;
-    return vec ? launch_flat(repack_kernel<true>, units * kTileRows, stream, src, K, units, tiled, err)
-               : launch_flat(repack_kernel<false>, units * kTileRows, stream, src, K, units, tiled, err);
+    return launch_repack_jobs(&src, &tiled, &N, &K, 1, err, stream);
 }
 
 // FP16 scales -> int8 scales and per-row factors, in fp32 with ties to
@@ -403,10 +486,8 @@ cudaError_t launch_repack_glu(const uint8_t* packed_gate, const uint16_t* scales
     src.scales[1] = scales_up;
     src.rows = I;
     src.glu = 1;
-    const int64_t units = ceil_div(glu_rows(I), kTileRows) * (K / kGroup);
-    const bool vec = ((reinterpret_cast<uintptr_t>(packed_gate) | reinterpret_cast<uintptr_t>(packed_up)) & 15) == 0;
-    return vec ? launch_flat(repack_kernel<true>, units * kTileRows, stream, src, K, units, tiled, err)
-               : launch_flat(repack_kernel<false>, units * kTileRows, stream, src, K, units, tiled, err);
+    const int64_t rows = glu_rows(I);
+    return launch_repack_jobs(&src, &tiled, &rows, &K, 1, err, stream);
 }
 
 cudaError_t launch_unrepack(const uint8_t* tiled, int64_t N, int64_t K, uint8_t* packed,

@@ -252,3 +252,25 @@ def test_grouped_sizes_and_argument_errors():
     assert f(0, 1, 2, X, ld, W, Ns, Ks, arr(vp, [FAKE + 2, FAKE]), ld, 0, None, 0, None) == 3   # fp32 Y
     assert f(0, 0, 2, X, ld, W, Ns, Ks, Y, ld, 0, None, 0, None) == 0            # M == 0
     assert f(0, 1, 1, X, ld, W, arr(i64, [0]), Ks, Y, ld, 0, None, 0, None) == 0  # N == 0 only
+
+
+def test_repack_grouped_argument_errors():
+    lib = binding.library()
+    i64, vp, sz = ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t
+
+    def arr(t, vals):
+        return (t * len(vals))(*vals)
+
+    P, S, T = arr(vp, [FAKE, FAKE]), arr(vp, [FAKE, FAKE]), arr(vp, [FAKE, FAKE])
+    Ns, Ks = arr(i64, [256, 100]), arr(i64, [256, 512])
+    big = arr(sz, [1 << 30, 1 << 30])
+    f = lib.tern_repack_grouped
+    assert f(0, P, S, Ns, Ks, T, big, None, None) == 2                       # count
+    assert f(binding.MAX_GROUP + 1, P, S, Ns, Ks, T, big, None, None) == 2
+    assert f(2, None, S, Ns, Ks, T, big, None, None) == 1                    # host arrays
+    assert f(2, P, S, Ns, arr(i64, [256, 200]), T, big, None, None) == 2      # K % 128
+    assert f(2, P, S, Ns, Ks, T, arr(sz, [1 << 30, 16]), None, None) == 4    # tiled too small
+    assert f(2, arr(vp, [FAKE, FAKE + 2]), S, Ns, Ks, T, big, None, None) == 3   # packed 4-byte aligned
+    assert f(2, P, S, Ns, Ks, arr(vp, [FAKE, FAKE + 8]), big, None, None) == 3   # tiled 16-byte aligned
+    assert f(2, P, arr(vp, [FAKE, None]), Ns, Ks, T, big, None, None) == 1
+    assert f(1, P, S, arr(i64, [0]), Ks, T, big, None, None) == 0            # N == 0: nothing to do

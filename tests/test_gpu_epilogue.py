@@ -81,6 +81,42 @@ def test_repack_unaligned_source_bit_exact(N, K):
     assert np.array_equal(host(tiled), ref)
 
 
+def test_repack_grouped_bit_exact():
+    # one launch over weights of several shapes (ragged N, K from 128), one
+    # of them from a source that is 4- but not 16-byte aligned
+    rng = np.random.default_rng(11)
+    shapes = [(1000, 512), (1, 128), (300, 1024), (129, 256), (0, 256), (517, 640)]
+    packed, scales, tiled, refs = [], [], [], []
+    for i, (N, K) in enumerate(shapes):
+        t, s = rand_ternary(rng, max(N, 1), K)[:N], rand_scales(rng, max(N, 1), K)[:N]
+        if N == 0:
+            packed.append(torch.zeros(16, dtype=torch.uint8, device=DEV))
+            scales.append(torch.zeros(16, dtype=torch.int16, device=DEV))
+            tiled.append(torch.zeros(16, dtype=torch.uint8, device=DEV))
+            refs.append(None)
+            continue
+        p = gpu_pack(t)
+        if i == 3:
+            buf = torch.zeros(p.numel() + 16, dtype=torch.uint8, device=DEV)
+            buf[4:4 + p.numel()] = p.reshape(-1)
+            packed.append(buf.data_ptr() + 4)
+            tiled_keep = buf
+        else:
+            packed.append(p)
+        scales.append(dev(s.view(np.int16)))
+        tiled.append(torch.full((tb.tern_tiled_bytes(N, K),), 0xAB, dtype=torch.uint8, device=DEV))
+        refs.append(oracle.repack(oracle.pack(t)[0], s, K)[0])
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    tb.tern_repack_grouped(packed, scales, [n for n, _ in shapes], [k for _, k in shapes], tiled,
+                           [t.numel() for t in tiled], err=err)
+    torch.cuda.synchronize()
+    del tiled_keep
+    for (N, K), t, ref in zip(shapes, tiled, refs):
+        if ref is not None:
+            assert np.array_equal(host(t), ref), f"{N}x{K}"
+    assert int(err.item()) == 0
+
+
 @pytest.mark.parametrize("I,K", [(1, 128), (20, 256), (200, 512), (1000, 1024)])
 def test_repack_glu_bit_exact(I, K):
     rng = np.random.default_rng(I + K)
