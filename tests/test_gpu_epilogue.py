@@ -136,7 +136,7 @@ def test_repack_glu_bit_exact(I, K):
 
 # ------------------------------------------------------------ output forms
 
-CASES = [(1, 1000), (5, 1000), (16, 300), (40, 1000), (200, 520)]
+CASES = [(1, 1000), (5, 1000), (16, 300), (32, 1000), (40, 1000), (200, 520)]
 
 
 @pytest.mark.parametrize("M,N", CASES)
@@ -161,7 +161,7 @@ def test_linear_ex_half_outputs(M, N, out_type):
         off += n
 
 
-@pytest.mark.parametrize("M", [1, 3, 16, 40, 300])
+@pytest.mark.parametrize("M", [1, 3, 16, 20, 40, 300])
 def test_linear_ex_fp16_activations(M):
     N, K = 700, 1024
     rng = np.random.default_rng(100 + M)
@@ -201,7 +201,7 @@ def run_swiglu(x, x_f16, tg, tu, sg, su, out_type):
     return host(H.float())
 
 
-@pytest.mark.parametrize("M,I", [(1, 200), (1, 1000), (7, 200), (16, 1000), (33, 200), (300, 520)])
+@pytest.mark.parametrize("M,I", [(1, 200), (1, 1000), (7, 200), (16, 1000), (32, 1000), (33, 200), (300, 520)])
 @pytest.mark.parametrize("out_type", [tb.TERN_OUT_F32, tb.TERN_OUT_BF16])
 def test_linear_swiglu(M, I, out_type):
     K = 512

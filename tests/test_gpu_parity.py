@@ -136,7 +136,7 @@ def test_linear_single_layer_workload(M):
 
 
 @pytest.mark.parametrize("N,K", [(1, 128), (15, 384), (17, 128), (200, 1280), (1000, 256)])
-@pytest.mark.parametrize("M", [1, 2, 3, 7, 8, 9, 15, 16, 17, 33])
+@pytest.mark.parametrize("M", [1, 2, 3, 7, 8, 9, 15, 16, 17, 24, 32, 33])
 def test_linear_ragged_shapes(N, K, M):
     rng = np.random.default_rng(N * 131 + K * 7 + M)
     t = rand_ternary(rng, N, K)

@@ -44,7 +44,7 @@ def test_quantize_and_repack_s8_bit_exact(N, K):
     assert np.array_equal(host(tiled), oracle.repack_s8(oracle.pack(t)[0], q_ref, f_ref, K))
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 1000, 512), (4, 300, 5120), (16, 1000, 1024), (33, 520, 512),
+@pytest.mark.parametrize("M,N,K", [(1, 1000, 512), (4, 300, 5120), (16, 1000, 1024), (24, 300, 512), (33, 520, 512),
                                    (300, 1000, 512)])
 def test_linear_s8(M, N, K):
     rng = np.random.default_rng(M + 3 * N + K)

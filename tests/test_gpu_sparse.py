@@ -39,7 +39,7 @@ def sparse_weights(rng, N, K, pattern):
 
 
 @pytest.mark.parametrize("pattern", ["half", "leading", "tile", "all"])
-@pytest.mark.parametrize("M,N,K", [(1, 1000, 1024), (5, 300, 512), (16, 1000, 512), (40, 520, 1024),
+@pytest.mark.parametrize("M,N,K", [(1, 1000, 1024), (5, 300, 512), (16, 1000, 512), (32, 520, 512), (40, 520, 1024),
                                    (300, 1000, 512)])
 def test_linear_sparse(M, N, K, pattern):
     rng = np.random.default_rng(M + N + K + len(pattern))
