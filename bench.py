@@ -305,11 +305,16 @@ def time_graph(torch, graph, steps, warmup, world, before=None, after=None, stre
     if world > 1:
         torch.distributed.barrier()
     ms = e0.elapsed_time(e1) / steps
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    return ms
+    return max_over_ranks(torch, ms, world, "cuda")
+
+
+def max_over_ranks(torch, value: float, world: int, device: str) -> float:
+    """The slowest replica's time: every rank gets the maximum over ranks."""
+    if world <= 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
 
 
 def capture(torch, fn):
