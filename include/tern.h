@@ -254,9 +254,10 @@ tern_status tern_linear_ex(const void* d_X, int x_type, int64_t ldx, const void*
  * it may differ from a separate call's in the last bits, as the CTAs split a
  * problem's groups differently and fp32 partial sums then add in another
  * order (a given group is still deterministic).  M <= 16 runs as one
- * launch; larger M as one launch per problem.
- * The workspace is sized by tern_grouped_workspace_bytes (0 for invalid
- * shapes) and follows the rules of tern_linear. */
+ * launch; larger M as one launch per problem.  The outputs must not overlap
+ * one another or any input.  The workspace is sized by
+ * tern_grouped_workspace_bytes (0 for invalid shapes) and follows the rules
+ * of tern_linear. */
 #define TERN_MAX_GROUP 8
 size_t tern_grouped_workspace_bytes(int64_t M, int count, const int64_t* Ns, const int64_t* Ks);
 
