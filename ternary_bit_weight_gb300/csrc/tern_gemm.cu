@@ -28,8 +28,8 @@
 //   * MMA warp (warp-uniform loop, one elected lane issues): per group and
 //     row tile eight tcgen05.mma (M = 128, N = NT, K = 16, f16 -> fp32);
 //   * epilogue warpgroup: tcgen05.ld of both accumulators, times 2^-c_m,
-//     stores (or, when K is split across items, a partial summed in split
-//     order by the last item of the tile to arrive).
+//     stores (or, when K is split across items, the item's fp32 partial,
+//     which split_reduce_kernel sums in split order after the GEMM).
 // Every wait is bounded; a timeout raises the workspace error word.
 
 #include <cuda.h>
@@ -107,8 +107,7 @@ struct GemmArgs {
     int64_t items;             // RP * T * KS
     OutputSplit out;
     int* err;
-    int* counters;             // [RP * T]
-    float* partial;            // [RP * T][KS][2][NT][128]
+    float* partial;            // [RP * T][KS][2][NT / 4][128][4]
     int tma_store;             // outputs written through ymaps (see launch_gemm)
 };
 
@@ -564,9 +563,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ YM
                 __syncwarp();
                 if (lane == 0) mbar_arrive(cb + kBarDEmpty);
             } else {
-                // publish this split's partial; the last split of the tile sums
-                // all partials in split order
-                float* base = a.partial + (tile * a.KS + it.ks) * (2 * (int64_t)NT * kTileRows);
+                // this split's partial, laid out [rt][token / 4][row][4]: a
+                // thread's four tokens are one 16-byte store, a warp's 512
+                // contiguous bytes; split_reduce_kernel sums the splits
+                float4* base = reinterpret_cast<float4*>(a.partial) + (tile * a.KS + it.ks) * (2 * (int64_t)NT * kTileRows / 4);
                 int g0, g1;
                 group_range(a, it.ks, g0, g1);
                 for (int rt = 0; rt < 2; ++rt) {
@@ -582,52 +582,16 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ YM
 #pragma unroll
                             for (int m = 0; m < 32; ++m) d[m] = 0u;
 #pragma unroll
-                        for (int m = 0; m < 32; ++m)
-                            if (c + m < NT) base[((int64_t)rt * NT + c + m) * kTileRows + r] = __uint_as_float(d[m]);
+                        for (int q = 0; q < 8; ++q)
+                            if (c + 4 * q < NT)
+                                base[((int64_t)(rt * NT + c) / 4 + q) * kTileRows + r] =
+                                    make_float4(__uint_as_float(d[4 * q]), __uint_as_float(d[4 * q + 1]),
+                                                __uint_as_float(d[4 * q + 2]), __uint_as_float(d[4 * q + 3]));
                     }
                 }
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(cb + kBarDEmpty);
-                // every epilogue thread's partial is visible GPU-wide before the count
-                __threadfence();
-                asm volatile("bar.sync 1, 128;" ::: "memory");
-                __shared__ int last_flag;
-                if (r == 0) {
-                    __threadfence();
-                    last_flag = atomicAdd(a.counters + tile, 1) == a.KS - 1;
-                    if (last_flag) __threadfence();
-                }
-                asm volatile("bar.sync 1, 128;" ::: "memory");
-                if (last_flag) {
-                    // 16 columns at a time: the loads of a split are independent
-                    const float* tb = a.partial + tile * a.KS * (2 * (int64_t)NT * kTileRows);
-                    for (int rt = 0; rt < 2; ++rt) {
-                        if (rt == 1 && !two) break;
-                        const int64_t row = (int64_t)(2 * it.bp + rt) * kTileRows + r;
-                        const bool live = row < a.N;
-                        const RowOut o = row_out(a.out, live ? row : 0);
-                        const float f = s8 ? a.row_factor[row] : 1.0f;
-                        for (int c = 0; c < mvalid; c += 16) {
-                            float v[16];
-#pragma unroll
-                            for (int m = 0; m < 16; ++m) v[m] = 0.f;
-                            for (int k = 0; k < a.KS; ++k) {
-                                const float* src = tb + ((int64_t)k * 2 * NT + rt * NT + c) * kTileRows + r;
-#pragma unroll
-                                for (int m = 0; m < 16; ++m) v[m] += __ldcg(src + m * kTileRows);
-                            }
-                            float inv[16];
-                            load_inv(a.inv_scale + m0 + c, inv);
-#pragma unroll
-                            for (int m = 0; m < 16; ++m) inv[m] *= f;
-#pragma unroll
-                            for (int m = 0; m < 16; ++m) v[m] *= inv[m];
-                            store_run(a.out, o, m0 + c, m0 + mvalid, row, v, live);
-                        }
-                    }
-                    if (r == 0) a.counters[tile] = 0;   // leave the workspace zeroed
-                }
             }
         }
     }
@@ -701,6 +665,70 @@ __global__ void __launch_bounds__(256) xprep_kernel(const uint16_t* __restrict__
     grid_launch_dependents();
 }
 
+// K split across items: the sum of a tile's partials in split order, times
+// 2^-c_m (and, with int8 scales, the row's factor), to the outputs.  One
+// thread per weight row, 16 tokens per CTA; the loads of kSumSplits splits
+// are in flight together.  Launched after gemm_kernel, whose completion it
+// waits for.
+struct ReduceArgs {
+    const float4* partial;     // [RP * T][KS][2][NT / 4][128] float4
+    const float* inv_scale;
+    const float* row_factor;   // null unless int8 scales
+    int M, NT, R, RP, KS;
+    int64_t N;
+    OutputSplit out;
+};
+
+__global__ void __launch_bounds__(kTileRows) split_reduce_kernel(const ReduceArgs a) {
+    grid_dependency_wait();   // every split's partial is written
+    grid_launch_dependents();
+    constexpr int kSumSplits = 4;
+    const int nb = a.NT / 16;                      // 16-token blocks per tile
+    const int cb = static_cast<int>(blockIdx.x % nb);
+    const int rt = static_cast<int>((blockIdx.x / nb) & 1);
+    const int64_t tile = blockIdx.x / (2 * nb);    // token tile * RP + row pair
+    const int bp = static_cast<int>(tile % a.RP);
+    const int m0 = static_cast<int>(tile / a.RP) * a.NT;
+    const int mvalid = a.M - m0 < a.NT ? a.M - m0 : a.NT;
+    const int c = 16 * cb;
+    if (c >= mvalid || 2 * bp + rt >= a.R) return;
+    const int r = threadIdx.x;
+    const int64_t split_stride = 2 * (int64_t)a.NT * kTileRows / 4;
+    const float4* src = a.partial + tile * a.KS * split_stride + ((int64_t)(rt * a.NT + c) / 4) * kTileRows + r;
+    float v[16];
+#pragma unroll
+    for (int m = 0; m < 16; ++m) v[m] = 0.f;
+    for (int k0 = 0; k0 < a.KS; k0 += kSumSplits) {
+        float4 t[kSumSplits][4];
+#pragma unroll
+        for (int kk = 0; kk < kSumSplits; ++kk)
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                t[kk][q] = k0 + kk < a.KS ? __ldcg(src + (k0 + kk) * split_stride + q * kTileRows)
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int kk = 0; kk < kSumSplits; ++kk) {
+            if (k0 + kk >= a.KS) break;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                v[4 * q] += t[kk][q].x;
+                v[4 * q + 1] += t[kk][q].y;
+                v[4 * q + 2] += t[kk][q].z;
+                v[4 * q + 3] += t[kk][q].w;
+            }
+        }
+    }
+    const int64_t row = (int64_t)(2 * bp + rt) * kTileRows + r;
+    const bool live = row < a.N;
+    const RowOut o = row_out(a.out, live ? row : 0);
+    const float f = a.row_factor != nullptr && live ? a.row_factor[row] : 1.0f;
+    float inv[16];
+    load_inv(a.inv_scale + m0 + c, inv);
+#pragma unroll
+    for (int m = 0; m < 16; ++m) v[m] *= inv[m] * f;
+    store_run(a.out, o, m0 + c, m0 + mvalid, row, v, live);
+}
+
 // ---------------------------------------------------------------- host
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -743,22 +771,36 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sm_count) {
     p.T = ceil_div(M, kMaxNT);
     p.NT = static_cast<int>(round_up(ceil_div(M, p.T), 16));
     // split K when there are too few (row pair, token tile) items to fill
-    // the SMs: as many splits as one wave holds, each at least 4 groups long
+    // the SMs: as many splits as one wave holds.  With more items than SMs,
+    // the fewest splits (up to 4) that cut the waves of whole-item time by
+    // a tenth (216 row pairs on 152 SMs: 2 waves -> 3 waves of half items),
+    // if the fp32 partials stay within 64 MB (about half of L2) or the
+    // split items are still long (64 groups or more), so that writing and
+    // summing the partials costs less than the waves save.
     const int64_t tiles = p.RP * p.T;
     int64_t ks = tiles < sm_count ? sm_count / tiles : 1;
+    if (tiles >= sm_count) {
+        const int64_t w1 = ceil_div(tiles, (int64_t)sm_count);
+        for (int64_t k = 2; k <= 4; ++k) {
+            const int64_t partial_bytes = tiles * k * 2 * p.NT * kTileRows * 4;
+            if (ceil_div(tiles * k, (int64_t)sm_count) * 10 <= w1 * k * 9 &&
+                (partial_bytes <= (int64_t(64) << 20) || p.G / k >= 64)) {
+                ks = k;
+                break;
+            }
+        }
+    }
     if (ks > p.G / 4) ks = p.G / 4;
     if (ks < 1) ks = 1;
     p.KS = ks;
     p.items = tiles * ks;
     p.grid = p.items < sm_count ? p.items : sm_count;
-    // workspace: error word | X16 [M][K] fp16 | 2^-c per row | tile counters | split partials
+    // workspace: error word | X16 [M][K] fp16 | 2^-c per row | split partials
     size_t off = kWorkspaceErrBytes;
     p.off_x16 = off;
     off += round_up(M * K * 2, 1024);
     p.off_inv = off;
     off += round_up((p.T * p.NT + 32) * 4, 256);   // read 32 at a time from any token tile
-    p.off_counters = off;
-    off += round_up(tiles * 4, 256);
     p.off_partial = off;
     if (p.KS > 1) off += static_cast<size_t>(tiles * p.KS * 2 * p.NT * kTileRows) * sizeof(float);
     p.ws_bytes = off;
@@ -820,7 +862,6 @@ cudaError_t launch_gemm(const uint16_t* X, bool x_f16, int64_t ldx, const uint8_
     a.items = plan.items;
     a.out = out;
     a.err = reinterpret_cast<int*>(w);
-    a.counters = reinterpret_cast<int*>(w + plan.off_counters);
     a.partial = reinterpret_cast<float*>(w + plan.off_partial);
     // outputs by TMA when every row tile falls in one output and the
     // outputs meet TMA's alignment (else the plain stores)
@@ -858,8 +899,24 @@ cudaError_t launch_gemm(const uint16_t* X, bool x_f16, int64_t ldx, const uint8_
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return ext ? cudaLaunchKernelEx(&cfg, gemm_kernel<true>, map, ymaps, a)
-               : cudaLaunchKernelEx(&cfg, gemm_kernel<false>, map, ymaps, a);
+    e = ext ? cudaLaunchKernelEx(&cfg, gemm_kernel<true>, map, ymaps, a)
+            : cudaLaunchKernelEx(&cfg, gemm_kernel<false>, map, ymaps, a);
+    if (e != cudaSuccess || plan.KS == 1) return e;
+    ReduceArgs ra = {};
+    ra.partial = reinterpret_cast<const float4*>(a.partial);
+    ra.inv_scale = inv;
+    ra.row_factor = a.row_factor;
+    ra.M = a.M;
+    ra.NT = a.NT;
+    ra.R = a.R;
+    ra.RP = a.RP;
+    ra.KS = a.KS;
+    ra.N = N;
+    ra.out = out;
+    cfg.gridDim = dim3(static_cast<unsigned>(plan.RP * plan.T * 2 * (plan.NT / 16)));
+    cfg.blockDim = dim3(kTileRows);
+    cfg.dynamicSmemBytes = 0;
+    return cudaLaunchKernelEx(&cfg, split_reduce_kernel, ra);
 }
 
 }  // namespace tern

@@ -110,7 +110,7 @@ struct GemmPlan {
     int64_t KS;            // splits of K
     int64_t items;
     int64_t grid;
-    size_t off_x16, off_inv, off_counters, off_partial;   // workspace layout
+    size_t off_x16, off_inv, off_partial;   // workspace layout
     size_t ws_bytes;
 };
 
