@@ -58,9 +58,12 @@ constexpr int kThreads = (kEpiWarp0 + 4) * 32;
 constexpr int kMaxNT = 128;                     // tokens per tile (UMMA N)
 constexpr int kTmemCols = 512;
 constexpr int kACols = 64;                      // one unit of fp16 A (128 per row)
-constexpr int kAU = 2;                          // A ring per row tile
-constexpr int kDCol0 = 2 * kAU * kACols;        // two accumulators of NT columns
-static_assert(kDCol0 + 2 * kMaxNT <= kTmemCols, "tensor-memory budget");
+// A ring per row tile: AU slots of kACols columns for each of the two row
+// tiles, then the two accumulators of NT columns.  Three slots fit beside
+// accumulators of up to 64 tokens, two beside 128 (see au_for).
+constexpr int kAUMax = 3;
+constexpr int kMaxNTForAU3 = (kTmemCols - 2 * 3 * kACols) / 2;
+static_assert(2 * 2 * kACols + 2 * kMaxNT <= kTmemCols, "tensor-memory budget");
 constexpr int kWG = 4;                          // groups per weight stage
 constexpr int kWS = 2;                          // weight stages
 constexpr int kXG = 1;                          // groups per activation stage (one TMA copy)
@@ -79,9 +82,9 @@ constexpr int kBarXFull = 0;                                 // [kXS]
 constexpr int kBarXEmpty = kBarXFull + 8 * kXS;              // [kXS]
 constexpr int kBarWFull = kBarXEmpty + 8 * kXS;              // [kWS]
 constexpr int kBarWEmpty = kBarWFull + 8 * kWS;              // [kWS]
-constexpr int kBarAFull = kBarWEmpty + 8 * kWS;              // [kAU], both row tiles
-constexpr int kBarAEmpty = kBarAFull + 8 * kAU;              // [kAU]
-constexpr int kBarDFull = kBarAEmpty + 8 * kAU;
+constexpr int kBarAFull = kBarWEmpty + 8 * kWS;              // [AU], both row tiles
+constexpr int kBarAEmpty = kBarAFull + 8 * kAUMax;           // [AU]
+constexpr int kBarDFull = kBarAEmpty + 8 * kAUMax;
 constexpr int kBarDEmpty = kBarDFull + 8;
 constexpr int kBarDrain = kBarDEmpty + 8;
 constexpr int kTmemPtr = kBarDrain + 8;
@@ -189,9 +192,13 @@ __device__ __forceinline__ void group_range(const GemmArgs& a, int ks, int& g0, 
 
 // EXT: the weights may carry int8 scales (a.s8) or zero-unit flags
 // (a.zflags); the plain instantiation has neither check on its hot paths.
-template <bool EXT>
+// AU: A-ring slots per row tile (3 needs a.NT <= kMaxNTForAU3).
+template <bool EXT, int AU>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ YMaps ymaps, const GemmArgs a) {
+    static_assert(AU == 2 || AU == kAUMax, "A-ring depth");
+    constexpr int kAU = AU;
+    constexpr int kDCol0 = 2 * kAU * kACols;   // two accumulators of NT columns follow the A rings
     const bool s8 = EXT && a.s8 != 0;
     const uint8_t* const zflags = EXT ? a.zflags : nullptr;
     const int scale_unit = EXT ? a.scale_unit : kUnitScaleBytes;
@@ -750,15 +757,20 @@ EncodeTiledFn encode_tiled_fn() {
     return fn;
 }
 
-template <bool EXT>
+template <bool EXT, int AU>
 cudaError_t set_smem_limit() {
     static cudaError_t status = cudaErrorUnknown;
     static std::once_flag once;
     std::call_once(once, [] {
-        status = cudaFuncSetAttribute(gemm_kernel<EXT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        status = cudaFuncSetAttribute(gemm_kernel<EXT, AU>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     });
     return status;
 }
+
+// A-ring depth for a token tile of NT: the deeper ring wherever tensor
+// memory holds it beside the accumulators (the decode -> MMA hand-off of
+// a slot is latency-bound at small NT).
+int au_for(int NT) { return NT <= kMaxNTForAU3 ? kAUMax : 2; }
 
 }  // namespace
 
@@ -840,7 +852,9 @@ cudaError_t launch_gemm(const uint16_t* X, bool x_f16, int64_t ldx, const uint8_
         CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     const bool ext = s8 || zflags != nullptr;
-    cudaError_t e = ext ? set_smem_limit<true>() : set_smem_limit<false>();
+    const int au = au_for(plan.NT);
+    cudaError_t e = ext ? (au == 3 ? set_smem_limit<true, 3>() : set_smem_limit<true, 2>())
+                        : (au == 3 ? set_smem_limit<false, 3>() : set_smem_limit<false, 2>());
     if (e != cudaSuccess) return e;
     GemmArgs a = {};
     a.codes = tiled;
@@ -899,8 +913,12 @@ cudaError_t launch_gemm(const uint16_t* X, bool x_f16, int64_t ldx, const uint8_
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = ext ? cudaLaunchKernelEx(&cfg, gemm_kernel<true>, map, ymaps, a)
-            : cudaLaunchKernelEx(&cfg, gemm_kernel<false>, map, ymaps, a);
+    if (ext)
+        e = au == 3 ? cudaLaunchKernelEx(&cfg, gemm_kernel<true, 3>, map, ymaps, a)
+                    : cudaLaunchKernelEx(&cfg, gemm_kernel<true, 2>, map, ymaps, a);
+    else
+        e = au == 3 ? cudaLaunchKernelEx(&cfg, gemm_kernel<false, 3>, map, ymaps, a)
+                    : cudaLaunchKernelEx(&cfg, gemm_kernel<false, 2>, map, ymaps, a);
     if (e != cudaSuccess || plan.KS == 1) return e;
     ReduceArgs ra = {};
     ra.partial = reinterpret_cast<const float4*>(a.partial);
