@@ -192,9 +192,11 @@ def build_stack(wl, layers, dev, tb, torch):
 class Step:
     """All linears of the stack at batch M, with X/Y arenas on the device.
     out_type: the outputs' element type (fp32 by default; bf16 through
-    tern_linear_ex).  grouped (M <= 16): each layer's linears -- independent
-    problems here, every one with its own synthetic X -- in one
-    tern_linear_grouped launch instead of one launch each."""
+    tern_linear_ex).  grouped: each layer's linears -- independent problems
+    here, every one with its own synthetic X -- in one tern_linear_grouped
+    call (one streaming launch for M <= 16; for larger M one activation
+    conversion, one GEMM and at most one split reduction) instead of one
+    call each."""
 
     def __init__(self, wl, layers, M, tiled, dev, tb, torch, host_copies=True, out_type=0, grouped=False):
         import synth
@@ -224,7 +226,7 @@ class Step:
             ws_need = max(ws_need, tb.tern_workspace_bytes(M, lin.N, lin.K))
             self.bytes += linear_bytes(M, lin.N, lin.K) - (4 - out_size) * M * lin.N
             self.flops += 2 * M * lin.N * lin.K
-        self.grouped = grouped and M <= 16
+        self.grouped = grouped
         if self.grouped:
             ws_need = max(ws_need, tb.tern_grouped_workspace_bytes(M, [l.N for l in wl.linears],
                                                                    [l.K for l in wl.linears]))
@@ -468,19 +470,28 @@ def timed_region(torch, fn, reps, local, min_ms=300.0):
 
 
 def leg_stack_batched(wl, layers, tiled, dev, tb, torch, Ms, local):
-    """27B-class stack at continuous-batching sizes: tokens/s per step."""
+    """27B-class stack at continuous-batching sizes: tokens/s per step, with
+    each layer's four linears as one grouped call (as the M = 1 headline) and
+    with one call per linear (per_call)."""
     out = {}
     for M in Ms:
-        st = Step(wl, layers, M, tiled, dev, tb, torch, host_copies=False)
-        g = capture(torch, st.run)
-        for _ in range(2):
-            g.replay()
-        ms, clocks = timed_region(torch, g.replay, 2, local, min_ms=200.0)
-        out[str(M)] = {"ms_per_step": ms, "tokens_per_s": M / (ms / 1e3),
-                       "weight_gbs": st.bytes / (ms / 1e3) / 1e9, "tflops": st.flops / (ms / 1e3) / 1e12,
-                       "clocks": clocks}
-        del g, st
-        torch.cuda.empty_cache()
+        row = {}
+        for grouped in (True, False):
+            st = Step(wl, layers, M, tiled, dev, tb, torch, host_copies=False, grouped=grouped)
+            g = capture(torch, st.run)
+            for _ in range(2):
+                g.replay()
+            ms, clocks = timed_region(torch, g.replay, 2, local, min_ms=200.0)
+            r = {"ms_per_step": ms, "tokens_per_s": M / (ms / 1e3),
+                 "weight_gbs": st.bytes / (ms / 1e3) / 1e9, "tflops": st.flops / (ms / 1e3) / 1e12,
+                 "clocks": clocks}
+            if grouped:
+                row.update(r)
+            else:
+                row["per_call"] = r
+            del g, st
+            torch.cuda.empty_cache()
+        out[str(M)] = row
     return out
 
 

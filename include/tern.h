@@ -254,7 +254,9 @@ tern_status tern_linear_ex(const void* d_X, int x_type, int64_t ldx, const void*
  * it may differ from a separate call's in the last bits, as the CTAs split a
  * problem's groups differently and fp32 partial sums then add in another
  * order (a given group is still deterministic).  M <= 16 runs as one
- * launch; larger M as one launch per problem.  The outputs must not overlap
+ * streaming launch; larger M as one tensor-core GEMM launch over all the
+ * problems' tiles (after one activation conversion, and followed by one
+ * reduction of the problems whose K is split).  The outputs must not overlap
  * one another or any input.  The workspace is sized by
  * tern_grouped_workspace_bytes (0 for invalid shapes) and follows the rules
  * of tern_linear. */

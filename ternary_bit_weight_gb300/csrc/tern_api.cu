@@ -35,9 +35,10 @@ tern_status run_linear(const uint16_t* X, bool x_f16, int64_t ldx, const void* t
         tern::StreamProblem prob = {X, ldx, w, N, K, out};
         e = tern::launch_stream(&prob, 1, x_f16, s8, zflags, M, ws, plan, stream);
     } else {
-        const tern::GemmPlan plan = tern::plan_gemm(M, N, K, sms);
+        const tern::GemmPlan plan = tern::plan_gemm(M, &N, &K, 1, sms);
         if (ws_bytes < plan.ws_bytes) return TERN_ERR_SIZE;
-        e = tern::launch_gemm(X, x_f16, ldx, w, s8, zflags, M, N, K, out, ws, plan, stream);
+        tern::StreamProblem prob = {X, ldx, w, N, K, out};
+        e = tern::launch_gemm(&prob, 1, x_f16, s8, zflags, M, ws, plan, stream);
     }
     return e == cudaSuccess ? TERN_OK : TERN_ERR_CUDA;
 }
@@ -45,7 +46,7 @@ tern_status run_linear(const uint16_t* X, bool x_f16, int64_t ldx, const void* t
 size_t workspace_bytes(int64_t M, int64_t N, int64_t K) {
     const int sms = tern::device_sm_count();
     if (M <= tern::kStreamMaxM) return tern::plan_stream(M, &N, &K, 1, sms).ws_bytes;
-    return tern::plan_gemm(M, N, K, sms).ws_bytes;
+    return tern::plan_gemm(M, &N, &K, 1, sms).ws_bytes;
 }
 
 tern_status check_x_w(const uint16_t* X, int64_t ldx, const void* tiled, int64_t M, int64_t K) {
@@ -242,18 +243,15 @@ size_t tern_grouped_workspace_bytes(int64_t M, int count, const int64_t* Ns, con
     if (M <= 0 || count < 1 || count > tern::kMaxGroup || Ns == nullptr || Ks == nullptr) return 0;
     int64_t n[tern::kMaxGroup], k[tern::kMaxGroup];
     int P = 0;
-    size_t most = 0;
     for (int i = 0; i < count; ++i) {
         if (!valid_group_shape(Ns[i], Ks[i])) return 0;
         if (Ns[i] == 0) continue;
         n[P] = Ns[i];
         k[P] = Ks[i];
         ++P;
-        const size_t w = workspace_bytes(M, Ns[i], Ks[i]);
-        if (w > most) most = w;
     }
     if (P == 0) return 256;
-    if (M > tern::kStreamMaxM) return most;   // one launch per problem, one after another
+    if (M > tern::kStreamMaxM) return tern::plan_gemm(M, n, k, P, tern::device_sm_count()).ws_bytes;
     return tern::plan_stream(M, n, k, P, tern::device_sm_count()).ws_bytes;
 }
 
@@ -293,18 +291,16 @@ tern_status tern_linear_grouped(int x_type, int64_t M, int count, const void* co
         ++P;
     }
     if (P == 0) return TERN_OK;
-    if (M > tern::kStreamMaxM) {
-        for (int i = 0; i < P; ++i) {
-            tern_status st = run_linear(probs[i].x, x_type == TERN_X_F16, probs[i].ldx, probs[i].tiled, M, probs[i].N,
-                                        probs[i].K, probs[i].out, d_ws, ws_bytes, as_stream(stream));
-            if (st != TERN_OK) return st;
-        }
-        return TERN_OK;
-    }
     const int sms = tern::device_sm_count();
     if (sms <= 0) return TERN_ERR_UNSUPPORTED;
     if (d_ws == nullptr) return TERN_ERR_NULL;
     if (!aligned(d_ws, 256)) return TERN_ERR_ALIGN;
+    if (M > tern::kStreamMaxM) {
+        const tern::GemmPlan plan = tern::plan_gemm(M, n, k, P, sms);
+        if (ws_bytes < plan.ws_bytes) return TERN_ERR_SIZE;
+        return from_cuda(tern::launch_gemm(probs, P, x_type == TERN_X_F16, false, nullptr, M, d_ws, plan,
+                                           as_stream(stream)));
+    }
     const tern::StreamPlan plan = tern::plan_stream(M, n, k, P, sms);
     if (ws_bytes < plan.ws_bytes) return TERN_ERR_SIZE;
     return from_cuda(tern::launch_stream(probs, P, x_type == TERN_X_F16, false, nullptr, M, d_ws, plan,

@@ -100,25 +100,29 @@ cudaError_t launch_stream(const StreamProblem* probs, int P, bool x_f16, bool s8
                           void* ws, const StreamPlan& plan, cudaStream_t stream);
 
 // Tensor-core GEMM plan for M > kStreamMaxM: items of 256 weight rows x NT
-// tokens x a range of groups along K, persistent CTAs.
+// tokens x a range of groups along K, persistent CTAs.  One launch serves up
+// to kMaxGroup independent linears with the same M (their items
+// concatenated).
 struct GemmPlan {
-    int64_t R;             // 128-row tiles
-    int64_t RP;            // pairs of row tiles
-    int64_t G;             // groups along K
-    int64_t T;             // token tiles
-    int NT;                // tokens per tile
-    int64_t KS;            // splits of K
+    int P;                          // problems
+    int64_t T;                      // token tiles
+    int NT;                         // tokens per tile
+    int64_t R[kMaxGroup];           // 128-row tiles
+    int64_t RP[kMaxGroup];          // pairs of row tiles
+    int64_t G[kMaxGroup];           // groups along K
+    int64_t KS[kMaxGroup];          // splits of K
+    int64_t item_begin[kMaxGroup];  // items of the problems before
     int64_t items;
     int64_t grid;
-    size_t off_x16, off_inv, off_partial;   // workspace layout
+    size_t off_x16[kMaxGroup], off_inv[kMaxGroup], off_partial[kMaxGroup];   // workspace layout
     size_t ws_bytes;
 };
 
-GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sm_count);
+GemmPlan plan_gemm(int64_t M, const int64_t* N, const int64_t* K, int P, int sm_count);
 
-cudaError_t launch_gemm(const uint16_t* X, bool x_f16, int64_t ldx, const uint8_t* tiled, bool s8,
-                        const uint8_t* zflags, int64_t M, int64_t N, int64_t K, const OutputSplit& out, void* ws,
-                        const GemmPlan& plan, cudaStream_t stream);
+// s8 and zflags need P == 1.
+cudaError_t launch_gemm(const StreamProblem* probs, int P, bool x_f16, bool s8, const uint8_t* zflags, int64_t M,
+                        void* ws, const GemmPlan& plan, cudaStream_t stream);
 
 // int8-activation variant: quantised activations in the code words' field
 // order, one CTA per (row tile, K split).

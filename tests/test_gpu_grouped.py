@@ -1,5 +1,6 @@
 """GPU-vs-oracle parity of tern_linear_grouped: independent linears of
-different shapes in one launch (M <= 16) or one launch each (M > 16).
+different shapes in one streaming launch (M <= 16) or one GEMM launch with
+the items of all problems (M > 16).
 
 Tolerance: every output within 1e-4 * sum_k |x w| of the oracle's fp64
 value (the layer's bound), plus half an ulp of the result for bf16 / fp16
@@ -87,7 +88,7 @@ def check_all(probs, ys, out_type, x_f16, what):
 SHAPES = [(1000, 512), (300, 1024), (129, 256), (64, 128), (0, 256), (517, 640)]
 
 
-@pytest.mark.parametrize("M", [1, 2, 16, 32, 40])
+@pytest.mark.parametrize("M", [1, 2, 16, 32, 40, 130])
 @pytest.mark.parametrize("out_type", [tb.TERN_OUT_F32, tb.TERN_OUT_BF16])
 def test_grouped_matches_oracle(M, out_type):
     rng = np.random.default_rng(7 * M + out_type)
@@ -96,7 +97,7 @@ def test_grouped_matches_oracle(M, out_type):
     check_all(probs, ys, out_type, False, f"M={M}")
 
 
-@pytest.mark.parametrize("M", [1, 5])
+@pytest.mark.parametrize("M", [1, 5, 64])
 def test_grouped_fp16_activations_eight_problems(M):
     # the largest group, with problems of one tile and of several hundred units
     rng = np.random.default_rng(40 + M)
@@ -106,21 +107,22 @@ def test_grouped_fp16_activations_eight_problems(M):
     check_all(probs, ys, tb.TERN_OUT_F16, True, f"M={M}")
 
 
-def test_grouped_workspace_serves_again_and_is_deterministic():
-    rng = np.random.default_rng(3)
-    probs = make_problems(rng, [(1500, 512), (700, 1024), (90, 128)], 1, False)
-    ys1, ws = run_grouped(probs, 1, False, tb.TERN_OUT_F32)
-    ys2, _ = run_grouped(probs, 1, False, tb.TERN_OUT_F32, ws=ws)
+@pytest.mark.parametrize("M", [1, 40])
+def test_grouped_workspace_serves_again_and_is_deterministic(M):
+    rng = np.random.default_rng(3 + M)
+    probs = make_problems(rng, [(1500, 512), (700, 1024), (90, 128)], M, False)
+    ys1, ws = run_grouped(probs, M, False, tb.TERN_OUT_F32)
+    ys2, _ = run_grouped(probs, M, False, tb.TERN_OUT_F32, ws=ws)
     for a, b in zip(ys1, ys2):
         assert np.array_equal(np.nan_to_num(a, nan=7.0), np.nan_to_num(b, nan=7.0))
     check_all(probs, ys2, tb.TERN_OUT_F32, False, "second call")
 
 
-def test_grouped_27b_layer_m1_sampled():
+@pytest.mark.parametrize("M", [1, 32])
+def test_grouped_27b_layer_sampled(M):
     # the four linears of a 27B-class layer in one launch (synthetic weights
     # of the workload's recipe); 64 sampled rows per problem against the oracle
     wl = synth.WORKLOADS["stack27b"]
-    M = 1
     probs, Xs, tiled, Ns, Ks, Ys = [], [], [], [], [], []
     for lin in wl.linears:
         t, s = synth.weights(wl, 0, lin)
