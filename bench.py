@@ -542,22 +542,29 @@ def leg_prefill(wl, tiled, dev, tb, torch, Ms, local, out_type=0):
     return out
 
 
-def leg_workload(name, Ms, dev, tb, torch, local, reps=20):
-    """A small workload end to end (its own weights): per-step time at each M."""
+def leg_workload(name, Ms, dev, tb, torch, local, reps=20, grouped=False):
+    """A small workload end to end (its own weights): per-step time at each M,
+    one call per linear; with `grouped` also each layer's linears as one
+    grouped call (under "grouped")."""
     import synth
     wl = synth.WORKLOADS[name]
     tiled, disk, _, _ = build_stack(wl, wl.layers, dev, tb, torch)
     del disk
     out = {}
     for M in Ms:
-        st = Step(wl, wl.layers, M, tiled, dev, tb, torch, host_copies=False)
-        g = capture(torch, st.run)
-        for _ in range(3):
-            g.replay()
-        ms, clocks = timed_region(torch, g.replay, reps, local, min_ms=100.0)
-        out[str(M)] = {"ms_per_step": ms, "tokens_per_s": M / (ms / 1e3),
-                       "weight_gbs": st.bytes / (ms / 1e3) / 1e9, "clocks": clocks}
-        del g, st
+        for grp in ((False, True) if grouped else (False,)):
+            st = Step(wl, wl.layers, M, tiled, dev, tb, torch, host_copies=False, grouped=grp)
+            g = capture(torch, st.run)
+            for _ in range(3):
+                g.replay()
+            ms, clocks = timed_region(torch, g.replay, reps, local, min_ms=100.0)
+            r = {"ms_per_step": ms, "tokens_per_s": M / (ms / 1e3),
+                 "weight_gbs": st.bytes / (ms / 1e3) / 1e9, "clocks": clocks}
+            if grp:
+                out[str(M)]["grouped"] = r
+            else:
+                out[str(M)] = r
+            del g, st
     del tiled
     torch.cuda.empty_cache()
     return out
@@ -907,6 +914,7 @@ def main():
     if not args.no_legs and world == 1:
         legs = {}
         legs["dec27b_per_linear"] = leg_per_linear(wl, layers, tiled, dev, tb, torch, [2, 4, 8, 16], local)
+        legs["stack27b_small_batch"] = leg_stack_batched(wl, layers, tiled, dev, tb, torch, [2, 4, 8, 16], local)
         legs["stack27b_batched"] = leg_stack_batched(wl, layers, tiled, dev, tb, torch, [32, 64, 128, 256], local)
         legs["prefill27b"] = leg_prefill(wl, tiled, dev, tb, torch, [1024, 2048, 4096], local)
         for v in legs["prefill27b"].values():
@@ -918,7 +926,7 @@ def main():
         legs["variants27b"] = leg_variants(wl, min(layers, 8), dev, tb, torch, local)
         del tiled
         torch.cuda.empty_cache()
-        legs["embed06b"] = leg_workload("embed06b", [1, 32, 512], dev, tb, torch, local)
+        legs["embed06b"] = leg_workload("embed06b", [1, 32, 512], dev, tb, torch, local, grouped=True)
         legs["single"] = leg_workload("single", [1, 8], dev, tb, torch, local, reps=200)
         legs["single"]["note"] = "one 1024x1024 linear: 0.28 MB of weights, L2-resident and launch-bound"
         out["legs"] = legs
