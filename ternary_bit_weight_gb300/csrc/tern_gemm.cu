@@ -11,20 +11,23 @@
 // `xprep_kernel` to fp16 after scaling each token row by a power of two
 // 2^c_m chosen so that its largest magnitude lies in [2^14, 2^15): every
 // bf16 value at most 2^-32 of the row's maximum converts exactly.  The
-// products are then exact in fp32 and the whole K range accumulates in fp32
-// in tensor memory; the epilogue multiplies by 2^-c_m (exact).
+// products are then exact in fp32 and each item's K range accumulates in
+// fp32 in tensor memory; the epilogue multiplies by 2^-c_m (exact).
 //
 // Work item = 256 weight rows (two 128-row tiles) x NT tokens x a range of
 // 128-wide groups along K.  Both row tiles share every activation tile,
-// halving the activation traffic per flop.  Warp roles of the persistent
-// CTA (one per SM):
-//   * producer warp: weights by bulk copy, 4 groups per copy per row tile;
-//     activations by one 3-D TMA copy of 2 groups (4 chunks of 64 along K,
-//     128-byte swizzle) -- a CTA's copy engine completes only a few copies
-//     per microsecond, so copies are few and large;
+// halving the activation traffic per flop.  One launch may serve up to
+// kMaxGroup independent linears with the same M (their items concatenated).
+// Warp roles of the persistent CTA (one per SM):
+//   * weight producer warp: bulk copies of 4 groups per row tile per stage;
+//     two activation producer warps, alternate stages: one 3-D TMA copy of
+//     a group (2 chunks of 64 along K, 128-byte swizzle) per stage -- a
+//     CTA's copy engine completes only a few copies per microsecond per
+//     issuing warp, so copies are few and large;
 //   * two decode warpgroups, one per row tile (one thread per weight row =
 //     one tensor-memory lane): code word -> exact fp16 t (LOP3 + FMA), times
-//     the row's scale (one multiply) -> tcgen05.st into a 2-unit A ring;
+//     the row's scale (one multiply) -> tcgen05.st into the row tile's A
+//     ring (2 units, 3 when NT <= 64);
 //   * MMA warp (warp-uniform loop, one elected lane issues): per group and
 //     row tile eight tcgen05.mma (M = 128, N = NT, K = 16, f16 -> fp32);
 //   * epilogue warpgroup: tcgen05.ld of both accumulators, times 2^-c_m,
