@@ -88,7 +88,7 @@ def check_all(probs, ys, out_type, x_f16, what):
 SHAPES = [(1000, 512), (300, 1024), (129, 256), (64, 128), (0, 256), (517, 640)]
 
 
-@pytest.mark.parametrize("M", [1, 2, 16, 32, 40, 130])
+@pytest.mark.parametrize("M", [1, 2, 16, 32, 40, 130, 300])
 @pytest.mark.parametrize("out_type", [tb.TERN_OUT_F32, tb.TERN_OUT_BF16])
 def test_grouped_matches_oracle(M, out_type):
     rng = np.random.default_rng(7 * M + out_type)
