@@ -25,8 +25,9 @@ Reported (one JSON line on rank 0):
              memory and all Y copied back, inside the timed region
   legs       the other listed configurations, each with its own clock record:
              27B-class linears one by one at M = 2..16 (GB/s), the stack at
-             M = 32..256 (tokens/s), prefill M = 1024..4096 (TFLOP/s), the
-             0.6B embedding-model layers at M = 1, 32, 512 and the single
+             M = 2..16 and 32..256 (grouped per layer and one call per
+             linear), prefill M = 1024..4096 (TFLOP/s), the 0.6B
+             embedding-model layers at M = 1, 32, 512 and the single
              1024x1024 linear at M = 1, 8
   repack     GB/s of the disk -> tiled repack of all 48 layers, one
              tern_repack_grouped launch per layer (per_call_gbs: one

@@ -251,7 +251,8 @@ def tern_grouped_workspace_bytes(M: int, Ns, Ks) -> int:
 
 def tern_linear_grouped(x_type: int, M: int, Xs, ldxs, tiled, Ns, Ks, Ys, ldys, out_type: int, ws=None,
                         ws_bytes: int | None = None, stream=None):
-    """Independent linears (one output each) in one launch (M <= 16)."""
+    """Independent linears (one output each, the same M) in one launch: the
+    streaming kernel for M <= 16, the tensor-core GEMM above."""
     count = len(Ns)
     if ws_bytes is None:
         ws_bytes = _nbytes(ws)
