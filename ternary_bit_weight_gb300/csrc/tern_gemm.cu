@@ -957,6 +957,12 @@ int64_t splits_one(int64_t tiles, int64_t G, int NT, int sm_count) {
 // the lowest maximum wins (the longer items on a tie).  Targets that make
 // more than 16 items per SM are not considered.
 void splits_group(int P, const int64_t* tiles, const int64_t* G, int NT, int sm_count, int64_t* KS) {
+    int64_t whole = 0;
+    for (int q = 0; q < P; ++q) {
+        KS[q] = 1;
+        whole += tiles[q];
+    }
+    if (whole > 16 * int64_t(sm_count)) return;   // no split can help: already more items than any target allows
     // longest items first: the unsplit plan is always tallied
     static const int64_t kTargets[] = {int64_t(1) << 40, 216, 108, 64, 54, 40, 32, 27, 20, 16, 12, 8};
     constexpr int64_t kItemCost = 2, kReduceCost = 4;
