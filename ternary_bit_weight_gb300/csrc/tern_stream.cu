@@ -262,15 +262,16 @@ __device__ __forceinline__ bool vote_wait(uint32_t bar, uint32_t parity, bool ac
     return __all_sync(0xffffffffu, got);
 }
 
-// EXT: the weights may carry int8 scales (a.s8) or zero-unit flags
-// (a.zflags); the plain instantiation has neither check on its hot paths.
-template <bool ONE, bool XF16, bool EXT>
+// EXT: 0 plain weights; 1 int8 scales (a.s8); 2 zero-unit flags
+// (a.zflags).  Each form is its own instantiation, so that the scale width
+// and the flag checks are compile-time on the hot paths.
+template <bool ONE, bool XF16, int EXT>
 __global__ void __launch_bounds__(kThreads, 1)
 stream_kernel(const __grid_constant__ XMaps xmaps, const StreamArgs a) {
     using C = SCfg<ONE>;
-    const bool s8 = EXT && a.s8 != 0;
-    const uint8_t* const zflags = EXT ? a.zflags : nullptr;
-    const int scale_unit = EXT ? a.scale_unit : kUnitScaleBytes;
+    constexpr bool s8 = EXT == 1;
+    const uint8_t* const zflags = EXT == 2 ? a.zflags : nullptr;
+    constexpr int scale_unit = s8 ? kUnitScaleBytesS8 : kUnitScaleBytes;
     constexpr int NCOL = C::NCOL;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base (swizzle atoms)
@@ -317,22 +318,21 @@ stream_kernel(const __grid_constant__ XMaps xmaps, const StreamArgs a) {
             }
         } else {
             // (single problem)
-            // zero units are not copied: one copy per run of non-zero units
+            // one pair of copies from the stage's first to its last non-zero
+            // unit (zero units between them come along): a CTA's copy engine
+            // completes few copies per microsecond, so a copy per run of
+            // non-zero units would cost more than the bytes it saves
             uint32_t live = 0;
-            for (int32_t i = 0; i < cnt; ++i) live |= (zflags[uf + i] ? 0u : 1u) << i;
-            mbar_arrive_expect_tx(bar, __popc(live) * (kUnitCodeBytes + scale_unit) + cnt * C::XUnit);
-            for (int32_t i = 0; i < cnt;) {
-                if (!((live >> i) & 1u)) {
-                    ++i;
-                    continue;
-                }
-                int32_t e = i;
-                while (e < cnt && ((live >> e) & 1u)) ++e;
-                bulk_load(st + C::OffCodes + i * kUnitCodeBytes, a.prob[0].codes + (uf + i) * kUnitCodeBytes,
-                          (e - i) * kUnitCodeBytes, bar);
-                bulk_load(st + C::OffScales + i * scale_unit, a.prob[0].scales + (uf + i) * scale_unit,
-                          (e - i) * scale_unit, bar);
-                i = e;
+            for (int32_t i = 0; i < cnt; ++i) live |= (__ldg(zflags + uf + i) ? 0u : 1u) << i;
+            if (live == 0) {
+                mbar_arrive_expect_tx(bar, cnt * C::XUnit);
+            } else {
+                const int32_t i0 = __ffs(live) - 1, i1 = 32 - __clz(live);   // [i0, i1)
+                mbar_arrive_expect_tx(bar, (i1 - i0) * (kUnitCodeBytes + scale_unit) + cnt * C::XUnit);
+                bulk_load(st + C::OffCodes + i0 * kUnitCodeBytes, a.prob[0].codes + (uf + i0) * kUnitCodeBytes,
+                          (i1 - i0) * kUnitCodeBytes, bar);
+                bulk_load(st + C::OffScales + i0 * scale_unit, a.prob[0].scales + (uf + i0) * scale_unit,
+                          (i1 - i0) * scale_unit, bar);
             }
         }
     };
@@ -502,7 +502,7 @@ stream_kernel(const __grid_constant__ XMaps xmaps, const StreamArgs a) {
                 first = false;
                 const uint64_t b0 = ONE ? bdesc_p + 16u * (uint32_t)g
                                         : bdesc_ring + ((uint32_t)(s * C::StageBytes + us * C::XUnit) >> 4);
-                const bool zero = zflags != nullptr && zflags[u0 + j] != 0;
+                const bool zero = zflags != nullptr && __ldg(zflags + u0 + j) != 0;
                 if (elect_one()) {
                     if (!zero) {
     #pragma unroll
@@ -564,7 +564,7 @@ stream_kernel(const __grid_constant__ XMaps xmaps, const StreamArgs a) {
         for (int32_t j = q; j < n; j += 2) {
             const int us = j % kPS;
             if (us < 2 && !warp_wait(bar_full + 8 * s, full_ph, abort_flag)) break;   // first unit of the stage
-            const bool zero = zflags != nullptr && zflags[u0 + j] != 0;   // nothing to decode
+            const bool zero = zflags != nullptr && __ldg(zflags + u0 + j) != 0;   // nothing to decode
             const uint8_t* cp = ring_ptr + s * C::StageBytes + codes_off + us * kUnitCodeBytes;
             uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0;
             if (!zero) {
@@ -682,7 +682,7 @@ stream_kernel(const __grid_constant__ XMaps xmaps, const StreamArgs a) {
                 if (i == 1 && !two) break;
                 const float sc = i == 0 ? sc0 : sc1;
                 const int32_t u = f + i;
-                if (zflags == nullptr || zflags[u0 + u] == 0)
+                if (zflags == nullptr || __ldg(zflags + u0 + u) == 0)
 #pragma unroll
                     for (int m = 0; m < NCOL; ++m) acc[m] = fmaf(sc, __uint_as_float(d[i * NCOL + m]), acc[m]);
                 if (pg == G - 1 || u == n - 1) {
@@ -736,7 +736,7 @@ EncodeTiledFn encode_tiled_fn() {
     return fn;
 }
 
-template <bool ONE, bool XF16, bool EXT>
+template <bool ONE, bool XF16, int EXT>
 cudaError_t set_smem_limit() {
     static cudaError_t status = cudaErrorUnknown;
     static std::once_flag once;
@@ -747,7 +747,7 @@ cudaError_t set_smem_limit() {
     return status;
 }
 
-template <bool ONE, bool XF16, bool EXT>
+template <bool ONE, bool XF16, int EXT>
 cudaError_t launch_one(const StreamProblem* probs, const StreamArgs& a, const StreamPlan& plan,
                        cudaStream_t stream) {
     XMaps maps;
@@ -861,19 +861,25 @@ cudaError_t launch_stream(const StreamProblem* probs, int P, bool x_f16, bool s8
     a.err = reinterpret_cast<int*>(w);
     a.counters = reinterpret_cast<int*>(w + kWorkspaceErrBytes);
     a.slots = reinterpret_cast<float*>(w + kWorkspaceErrBytes + static_cast<size_t>(round_up(plan.tiles * 4 * 4, 256)));
-    const bool ext = s8 || zflags != nullptr;
-    if (ext) {
+    if (s8) {
         if (x_f16)
-            return plan.one ? launch_one<true, true, true>(probs, a, plan, stream)
-                            : launch_one<false, true, true>(probs, a, plan, stream);
-        return plan.one ? launch_one<true, false, true>(probs, a, plan, stream)
-                        : launch_one<false, false, true>(probs, a, plan, stream);
+            return plan.one ? launch_one<true, true, 1>(probs, a, plan, stream)
+                            : launch_one<false, true, 1>(probs, a, plan, stream);
+        return plan.one ? launch_one<true, false, 1>(probs, a, plan, stream)
+                        : launch_one<false, false, 1>(probs, a, plan, stream);
+    }
+    if (zflags != nullptr) {
+        if (x_f16)
+            return plan.one ? launch_one<true, true, 2>(probs, a, plan, stream)
+                            : launch_one<false, true, 2>(probs, a, plan, stream);
+        return plan.one ? launch_one<true, false, 2>(probs, a, plan, stream)
+                        : launch_one<false, false, 2>(probs, a, plan, stream);
     }
     if (x_f16)
-        return plan.one ? launch_one<true, true, false>(probs, a, plan, stream)
-                        : launch_one<false, true, false>(probs, a, plan, stream);
-    return plan.one ? launch_one<true, false, false>(probs, a, plan, stream)
-                    : launch_one<false, false, false>(probs, a, plan, stream);
+        return plan.one ? launch_one<true, true, 0>(probs, a, plan, stream)
+                        : launch_one<false, true, 0>(probs, a, plan, stream);
+    return plan.one ? launch_one<true, false, 0>(probs, a, plan, stream)
+                    : launch_one<false, false, 0>(probs, a, plan, stream);
 }
 
 }  // namespace tern
