@@ -51,8 +51,8 @@ def test_quantize_x_bit_exact(M, K, x_f16):
     assert np.array_equal(host(a), a_ref)
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 300, 512), (3, 1000, 512), (16, 300, 5120), (17, 1000, 1024),
-                                   (40, 130, 256)])
+@pytest.mark.parametrize("M,N,K", [(1, 300, 512), (1, 1000, 5120), (1, 300, 27648), (3, 1000, 512),
+                                   (16, 300, 5120), (17, 1000, 1024), (40, 130, 256)])
 def test_linear_i8(M, N, K):
     rng = np.random.default_rng(M * 11 + N + K)
     u = rng.random((N, K))
@@ -72,13 +72,14 @@ def test_linear_i8(M, N, K):
     assert tb.tern_workspace_error(ws) == 0
 
 
-def test_linear_i8_27b_down_sampled():
-    # full-size 27B-class down projection (K = 27648 -> N = 5120) at M = 4
+@pytest.mark.parametrize("M", [1, 4])
+def test_linear_i8_27b_down_sampled(M):
+    # full-size 27B-class down projection (K = 27648 -> N = 5120): the
+    # single-token kernel (M = 1) and the batched one
     wl = synth.WORKLOADS["dec27b"]
     lin = next(l for l in wl.linears if l.name == "down")
     t, s = synth.weights(wl, 0, lin)
     tiled = tiled_from_ternary(t, s)
-    M = 4
     x = synth.activations(wl, 0, lin, M)
     xq, a = gpu_quantize(x, False)
     Y = torch.empty((M, lin.N), device=DEV)
