@@ -190,16 +190,16 @@ __device__ __forceinline__ int64_t owner_worker(int64_t u, int64_t U, int64_t V)
 // that row quarter sums all partials in CTA order.
 template <int NCOL>
 __device__ __forceinline__ void flush_tile(const StreamArgs& a, int64_t v, int p, int64_t b, bool first,
-                                           bool whole, float (&acc)[NCOL], int r, bool s8) {
+                                           bool whole, float (&acc)[NCOL], int r, bool s8, float row_f) {
     const StreamProb& pr = a.prob[p];
     const int lane = r & 31, quad = r >> 5;
     const int64_t row = b * kTileRows + r;
     const int mvalid = a.M < NCOL ? a.M : NCOL;
     if (s8) {
-        // int8 scales: the group sums were weighted by q; the row's factor once
-        const float f = a.row_factor[b * kTileRows + r];
+        // int8 scales: the group sums were weighted by q; the row's factor
+        // (row_f, loaded when the tile began) once
 #pragma unroll
-        for (int m = 0; m < NCOL; ++m) acc[m] *= f;
+        for (int m = 0; m < NCOL; ++m) acc[m] *= row_f;
     }
     const bool live = row < pr.N;
     const RowOut o = row_out(pr.out, live ? row : 0);
@@ -630,6 +630,9 @@ stream_kernel(const __grid_constant__ XMaps xmaps, const StreamArgs a) {
         const int32_t first_g = static_cast<int32_t>((u0 - a.prob[pp].u_begin) % G);
         int64_t pb = first_tile;
         int32_t pg = first_g;
+        // int8 scales (one problem): the current tile's row factor, loaded a
+        // tile ahead of its use
+        float row_f = s8 && pb < R ? a.row_factor[pb * kTileRows + r] : 1.f;
         float acc[NCOL];
 #pragma unroll
         for (int m = 0; m < NCOL; ++m) acc[m] = 0.f;
@@ -688,7 +691,7 @@ stream_kernel(const __grid_constant__ XMaps xmaps, const StreamArgs a) {
                 if (pg == G - 1 || u == n - 1) {
                     const bool first = pp == first_p && pb == first_tile;
                     const bool whole = (!first || first_g == 0) && pg == G - 1;
-                    flush_tile<NCOL>(a, v, pp, pb, first, whole, acc, r, s8);
+                    flush_tile<NCOL>(a, v, pp, pb, first, whole, acc, r, s8, row_f);
 #pragma unroll
                     for (int m = 0; m < NCOL; ++m) acc[m] = 0.f;
                 }
@@ -700,6 +703,7 @@ stream_kernel(const __grid_constant__ XMaps xmaps, const StreamArgs a) {
                         G = a.prob[pp].G;
                         R = a.prob[pp].R;
                     }
+                    if (s8 && pb < R) row_f = a.row_factor[pb * kTileRows + r];
                 }
             }
         }
