@@ -463,7 +463,7 @@ tern_status tern_linear_i8(const void* d_xq, const float* d_a, const void* d_til
     out.y[0] = d_Y;
     out.ldy[0] = ldy;
     return from_cuda(tern::launch_i8(static_cast<const int8_t*>(d_xq), d_a, static_cast<const uint8_t*>(d_tiled),
-                                     M, N, K, out, d_ws, plan, as_stream(stream)));
+                                     M, N, out, d_ws, plan, as_stream(stream)));
 }
 
 tern_status tern_workspace_error(const void* d_ws, int32_t* h_err, void* stream) {

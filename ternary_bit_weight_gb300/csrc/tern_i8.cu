@@ -294,7 +294,7 @@ I8Plan plan_i8(int64_t M, int64_t N, int64_t K, int sm_count) {
     return p;
 }
 
-cudaError_t launch_i8(const int8_t* xq, const float* a, const uint8_t* tiled, int64_t M, int64_t N, int64_t K,
+cudaError_t launch_i8(const int8_t* xq, const float* a, const uint8_t* tiled, int64_t M, int64_t N,
                       const OutputSplit& out, void* ws, const I8Plan& plan, cudaStream_t stream) {
     float* partial = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kWorkspaceErrBytes);
     const uint8_t* codes = tiled;

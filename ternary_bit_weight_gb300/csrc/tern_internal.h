@@ -134,7 +134,7 @@ size_t i8_xq_bytes(int64_t M, int64_t K);
 I8Plan plan_i8(int64_t M, int64_t N, int64_t K, int sm_count);
 cudaError_t launch_quantize_x(const uint16_t* X, bool x_f16, int64_t ldx, int64_t M, int64_t K, int8_t* xq, float* a,
                               cudaStream_t stream);
-cudaError_t launch_i8(const int8_t* xq, const float* a, const uint8_t* tiled, int64_t M, int64_t N, int64_t K,
+cudaError_t launch_i8(const int8_t* xq, const float* a, const uint8_t* tiled, int64_t M, int64_t N,
                       const OutputSplit& out, void* ws, const I8Plan& plan, cudaStream_t stream);
 
 // Size of the error word + padding at the start of every linear workspace.
